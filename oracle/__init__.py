@@ -1,0 +1,31 @@
+"""CPU oracle of the output head -- TEST INFRASTRUCTURE ONLY.
+
+A plain, slow, obviously correct restatement of what the output head
+computes, used to check the CUDA library. Only the tests, the smoke check and
+the benchmark's CPU-baseline leg may import it; the library never does, and
+the library shares no code with it (only the seeded generators in ``synth``
+serve both sides).
+
+Everything is computed exactly or in float64 with numpy:
+
+* float heads: inputs decoded exactly from their bf16 / fp16 bit patterns to
+  float64; logits by a float64 matrix product; the per-entry error base
+  ``A = |h|·|W|ᵀ`` for the tolerance ``1e-6·A``;
+* the integer head: exact int64 matrix product (every partial sum is far
+  below 2^63), cross-checked on samples with Python big-integer dots;
+* greedy token (lowest index among the maxima), runner-up value of the
+  multiset, top-2 gap in bf16 ulps of the winning logit, logsumexp and the
+  log-probability of a target.
+
+Parity pins: every function here is pinned by tests that do not re-use its
+own formula (hand-worked tiny cases, brute force with exact rationals,
+closed forms, invariants, and planted-mistake checks). Nothing is marked
+"parity unpinned".
+"""
+from .head import (  # noqa: F401
+    decode_bf16, decode_fp16, decode_int8, decode,
+    logits_float, logits_int, bigint_dot,
+    ulp_bf16, top2, greedy, greedy_int, gap_from_top2_f32,
+    logsumexp, logprob,
+    head_greedy, head_logprob,
+)

@@ -1,0 +1,227 @@
+"""CPU oracle of the output head -- TEST INFRASTRUCTURE ONLY (see package doc).
+
+Sources, by page title:
+
+* [Precision] "Greedy Decoding Has a Precision Clause" -- section "Token-ranking
+  margins explain why numerical error sometimes matters": the lm_head maps the
+  final hidden representation to vocabulary scores (logits); greedy decoding
+  takes the highest score; the top-two logit margin decides how easily a
+  perturbation flips the choice.
+* [DetLLM] "Eliminating Nondeterminism in LLM Inference with Integer-Only
+  Arithmetic" -- section "DetLLM" (int8 x int8 -> int32 matmul; argmax breaks
+  ties toward the lowest token id) and section "What if we don't use floats at
+  all?" (integer sums are order-free while they cannot overflow, and the
+  overflow can be bounded in advance).
+* [Exactness] "TandemLLM docs, 12 Exactness" -- section 12.2 "The exception:
+  near ties": the head returns fp32 logits; the gap between the two best
+  logits is reported in bf16 units in the last place (ulps); observed gaps are
+  fractions of an ulp, so the gap is a real number, not a count.
+* [Decoding] "Inference and Decoding" -- section 3 "The sampling methods",
+  Temperature: p_i = exp(z_i / tau) / sum_j exp(z_j / tau); tau = 1 here.
+* [LogprobGap] "batch-logprob-gap" -- the trainer's per-token log-probability
+  log p(target) and the ratio exp(logp_new - logp_old).
+
+Readings where the pages are silent (each also listed with the design notes):
+
+* the logit is the raw product h . w, no bias, no temperature, no rounding of
+  the logit to bf16 ([Exactness] 12.2: the head returns fp32 logits);
+* "second value" is the runner-up of the multiset of logits, so an exact tie
+  gives a gap of zero;
+* the ulp is the bf16 ulp of the winning logit m:
+  ulp(m) = 2^(max(floor(log2|m|), -126) - 7), i.e. bf16's 8-bit significand
+  at m's binade, never below bf16's smallest normal binade;
+* with a single vocabulary entry there is no runner-up: s = -inf, gap = +inf
+  (float heads) and gap = INT32_MAX (integer head);
+* the integer head's gap is the exact integer m - s (a bf16 ulp has no meaning
+  for int32 logits);
+* a target id outside [0, V) has no log-probability: NaN.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+INT32_MAX = 2**31 - 1
+
+
+# --------------------------------------------------------------------------
+# Exact decoding of the stored formats
+# --------------------------------------------------------------------------
+
+def decode_bf16(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> float64, exactly (bf16 is the top half of fp32)."""
+    u32 = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u32.view(np.float32).astype(np.float64)
+
+
+def decode_fp16(bits: np.ndarray) -> np.ndarray:
+    """IEEE binary16 bit patterns -> float64, exactly (subnormals included)."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def decode_int8(x: np.ndarray) -> np.ndarray:
+    return np.asarray(x, dtype=np.int8).astype(np.int64)
+
+
+def decode(arr: np.ndarray, fmt: str) -> np.ndarray:
+    if fmt == "bf16":
+        return decode_bf16(arr)
+    if fmt == "fp16":
+        return decode_fp16(arr)
+    if fmt == "int8":
+        return decode_int8(arr)
+    raise ValueError(f"unknown format {fmt!r}")
+
+
+# --------------------------------------------------------------------------
+# Logits
+# --------------------------------------------------------------------------
+
+def logits_float(W: np.ndarray, h: np.ndarray):
+    """Float head logits z[n, v] = sum_k h[n, k] * W[v, k]   ([Precision]).
+
+    ``W`` [V, d] and ``h`` [B, d] are float64 (exactly decoded inputs). Every
+    product of two bf16/fp16 values is exact in float64; the float64 sum adds
+    at most d * 2^-53 * sum|w h| of error, negligible against the 1e-6 * sum|w h|
+    tolerance the GPU is held to.
+
+    Returns (z, A) where A[n, v] = sum_k |h[n, k] * W[v, k]| is the error base
+    of the per-entry tolerance.
+    """
+    z = h @ W.T
+    A = np.abs(h) @ np.abs(W).T
+    return z, A
+
+
+def logits_int(W: np.ndarray, h: np.ndarray) -> np.ndarray:
+    """Integer head logits z[n, v] = sum_k h[n, k] * W[v, k], exactly ([DetLLM]).
+
+    int64 accumulation: |z| <= d * 128^2, far below 2^63, so the int64 sum
+    is exact in any order.
+    """
+    return np.asarray(h, dtype=np.int64) @ np.asarray(W, dtype=np.int64).T
+
+
+def bigint_dot(w_row, h_row) -> int:
+    """One logit by Python big-integer arithmetic (no overflow possible)."""
+    return sum(int(a) * int(b) for a, b in zip(w_row.tolist(), h_row.tolist()))
+
+
+# --------------------------------------------------------------------------
+# Token decision: argmax, runner-up, gap in bf16 ulps
+# --------------------------------------------------------------------------
+
+def ulp_bf16(m) -> np.ndarray:
+    """bf16 unit in the last place at the binade of m ([Exactness] 12.2).
+
+    2^(E - 7) with E = floor(log2 |m|) clamped below at -126 (bf16's smallest
+    normal exponent; m = 0 falls there too).
+    """
+    m = np.asarray(m, dtype=np.float64)
+    _, e = np.frexp(np.abs(m))          # |m| = f * 2^e, f in [0.5, 1)
+    E = np.where(m == 0, -126, np.maximum(e - 1, -126))
+    return np.ldexp(1.0, E - 7)
+
+
+def top2(z: np.ndarray):
+    """Greedy winner and runner-up value, row by row ([DetLLM], [Precision]).
+
+    token = the lowest index attaining the row maximum (numpy's argmax returns
+    the first occurrence); m = the maximum; s = the second element of the row
+    sorted in descending order (equal to m on an exact tie; -inf if V = 1).
+    """
+    z = np.asarray(z)
+    token = np.argmax(z, axis=1).astype(np.int64)
+    m = z[np.arange(z.shape[0]), token]
+    if z.shape[1] >= 2:
+        s = np.sort(z, axis=1)[:, -2]
+    else:
+        s = np.full(z.shape[0], -np.inf if z.dtype.kind == "f" else None)
+    return token, m, s
+
+
+def greedy(z: np.ndarray):
+    """Float head decision: (token, gap in bf16 ulps of the winner, m, s)."""
+    token, m, s = top2(np.asarray(z, dtype=np.float64))
+    with np.errstate(invalid="ignore"):
+        gap = (m - s) / ulp_bf16(m)
+    return token, gap, m, s
+
+
+def greedy_int(z: np.ndarray):
+    """Integer head decision: (token, exact gap m - s, m, s) ([DetLLM])."""
+    z = np.asarray(z, dtype=np.int64)
+    token = np.argmax(z, axis=1).astype(np.int64)
+    m = z[np.arange(z.shape[0]), token]
+    if z.shape[1] >= 2:
+        s = np.sort(z, axis=1)[:, -2]
+        gap = m - s
+    else:
+        s = np.full(z.shape[0], np.iinfo(np.int64).min)
+        gap = np.full(z.shape[0], INT32_MAX, dtype=np.int64)
+    return token, gap, m, s
+
+
+def gap_from_top2_f32(m32: np.ndarray, s32: np.ndarray) -> np.ndarray:
+    """The float32 gap the head reports for its own float32 top-2 values.
+
+    (m - s) / ulp_bf16(m) evaluated exactly (float64 difference of two float32
+    values, scaling by a power of two) and rounded once to float32.
+    """
+    m = np.asarray(m32, dtype=np.float32).astype(np.float64)
+    s = np.asarray(s32, dtype=np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        return ((m - s) / ulp_bf16(m)).astype(np.float32)
+
+
+# --------------------------------------------------------------------------
+# Log-sum-exp and the target log-probability
+# --------------------------------------------------------------------------
+
+def logsumexp(z: np.ndarray) -> np.ndarray:
+    """log sum_v exp(z[n, v]) at temperature 1 ([Decoding] section 3).
+
+    Shifted by the row maximum M so that no exp overflows:
+    lse = M + log(sum_v exp(z_v - M)).
+    """
+    z = np.asarray(z, dtype=np.float64)
+    M = np.max(z, axis=1)
+    return M + np.log(np.sum(np.exp(z - M[:, None]), axis=1))
+
+
+def logprob(z: np.ndarray, targets: np.ndarray) -> np.ndarray:
+    """log p(target) = z[n, target_n] - logsumexp(z[n])   ([LogprobGap]).
+
+    Targets outside [0, V) give NaN.
+    """
+    z = np.asarray(z, dtype=np.float64)
+    t = np.asarray(targets, dtype=np.int64)
+    B, V = z.shape
+    ok = (t >= 0) & (t < V)
+    zt = np.where(ok, z[np.arange(B), np.where(ok, t, 0)], np.nan)
+    return zt - logsumexp(z)
+
+
+# --------------------------------------------------------------------------
+# Whole-head entry points (what one library call computes)
+# --------------------------------------------------------------------------
+
+def head_greedy(W_raw: np.ndarray, h_raw: np.ndarray, fmt: str) -> dict:
+    """Greedy call: logits, token and top-2 gap for every hidden row."""
+    if fmt == "int8":
+        z = logits_int(decode_int8(W_raw), decode_int8(h_raw))
+        token, gap, m, s = greedy_int(z)
+        return {"logits": z, "token": token, "gap": gap, "m": m, "s": s}
+    z, A = logits_float(decode(W_raw, fmt), decode(h_raw, fmt))
+    token, gap, m, s = greedy(z)
+    return {"logits": z, "A": A, "token": token, "gap": gap, "m": m, "s": s}
+
+
+def head_logprob(W_raw: np.ndarray, h_raw: np.ndarray, targets: np.ndarray,
+                 fmt: str) -> dict:
+    """Log-prob call: logp of each row's target, with lse and the logits."""
+    if fmt not in ("bf16", "fp16"):
+        raise ValueError("the log-probability is defined for the float heads")
+    z, A = logits_float(decode(W_raw, fmt), decode(h_raw, fmt))
+    lse = logsumexp(z)
+    lp = logprob(z, targets)
+    return {"logits": z, "A": A, "lse": lse, "logp": lp}

@@ -1,0 +1,370 @@
+"""Pins for the CPU oracle: checks that do not re-use the oracle's formulas.
+
+Each ``pin_*`` takes an oracle object (the ``oracle`` package, or a copy with
+a planted mistake) and raises AssertionError when the oracle disagrees with
+what the pages or the mathematics fix. The pins use independent routes:
+
+* hand-worked values (``golden/tiny_head_d8_v16.txt``) and values printed on
+  the pages (``golden/page_examples.txt``);
+* brute force with exact rationals (``fractions.Fraction``) and Python big
+  integers, with inputs decoded through ``struct`` instead of numpy views;
+* 60-digit ``mpmath`` log-sum-exp and scipy's ``logsumexp`` as an outside
+  library routine;
+* closed forms (uniform logits, one dominant logit, the int32 bound) and
+  invariants (row permutation, duplicated rows, logp <= 0, lse >= max,
+  probabilities summing to one, the token-flip criterion).
+"""
+from __future__ import annotations
+
+import math
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------
+# fixture readers and independent helpers
+# --------------------------------------------------------------------------
+
+def read_tiny():
+    W, h, z, tok, gap = {}, {}, {}, {}, {}
+    with open(os.path.join(GOLDEN, "tiny_head_d8_v16.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, vals = line.split(":", 1)
+            kind, idx = key.split()
+            idx = int(idx)
+            nums = [Fraction(x) for x in vals.split()]
+            {"W": W, "h": h, "z": z, "token": tok, "gap": gap}[kind][idx] = nums
+    Wm = [W[i] for i in range(len(W))]
+    hm = [h[i] for i in range(len(h))]
+    zm = [z[i] for i in range(len(z))]
+    return Wm, hm, zm, [int(tok[i][0]) for i in range(len(tok))], \
+        [gap[i][0] for i in range(len(gap))]
+
+
+def read_page_examples():
+    out = {}
+    with open(os.path.join(GOLDEN, "page_examples.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split(":", 1)
+            out[k.strip()] = float(v)
+    return out
+
+
+def bf16_bits_of(x: Fraction) -> int:
+    """bf16 bit pattern of a value that is exact in bf16 (via struct)."""
+    b = struct.unpack(">I", struct.pack(">f", float(x)))[0]
+    assert b & 0xFFFF == 0, f"{x} is not exact in bf16"
+    return b >> 16
+
+
+def exact_bf16(bits: int) -> Fraction:
+    return Fraction(struct.unpack(">f", struct.pack(">I", int(bits) << 16))[0])
+
+
+def exact_fp16(bits: int) -> Fraction:
+    return Fraction(struct.unpack("<e", struct.pack("<H", int(bits)))[0])
+
+
+def exact_ulp_bf16(m: Fraction) -> Fraction:
+    """bf16 ulp at m's binade by exact search over powers of two."""
+    a = abs(m)
+    if a == 0:
+        E = -126
+    else:
+        E = 0
+        while Fraction(2) ** E > a:
+            E -= 1
+        while Fraction(2) ** (E + 1) <= a:
+            E += 1
+        E = max(E, -126)
+    return Fraction(2) ** (E - 7)
+
+
+def loop_argmax_lowest(row):
+    best = 0
+    for v in range(1, len(row)):
+        if row[v] > row[best]:
+            best = v
+    return best
+
+
+def _rand_bf16_bits(rng, shape, scale):
+    x = (rng.standard_normal(shape) * scale).astype(np.float32)
+    u = x.view(np.uint32)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+# --------------------------------------------------------------------------
+# pins
+# --------------------------------------------------------------------------
+
+def pin_tiny_golden(o):
+    """Hand-worked d=8, V=16 case: logits, tokens, gaps, ln 16."""
+    Wf, hf, zf, toks, gaps = read_tiny()
+    W_bits = np.array([[bf16_bits_of(x) for x in r] for r in Wf], np.uint16)
+    h_bits = np.array([[bf16_bits_of(x) for x in r] for r in hf], np.uint16)
+    out = o.head_greedy(W_bits, h_bits, "bf16")
+    z = out["logits"]
+    assert z.shape == (len(hf), len(Wf)), z.shape
+    for n in range(len(hf)):
+        for v in range(len(Wf)):
+            assert Fraction(float(z[n, v])) == zf[n][v], (n, v, z[n, v], zf[n][v])
+        assert int(out["token"][n]) == toks[n], (n, out["token"][n], toks[n])
+        assert Fraction(float(out["gap"][n])) == gaps[n], (n, out["gap"][n], gaps[n])
+    lp = o.head_logprob(W_bits, h_bits, np.arange(len(hf), dtype=np.int32), "bf16")
+    # h1 has all-zero logits: lse = ln 16, logp = -ln 16 (closed form)
+    assert abs(lp["lse"][1] - math.log(16)) <= 1e-15
+    assert abs(lp["logp"][1] + math.log(16)) <= 1e-15
+
+
+def pin_bruteforce_float(o):
+    """Random tiny bf16 and fp16 heads against exact rational dot products."""
+    rng = np.random.default_rng(7)
+    for fmt in ("bf16", "fp16"):
+        V, d, B = 16, 8, 5
+        if fmt == "bf16":
+            Wb = _rand_bf16_bits(rng, (V, d), 0.5)
+            hb = _rand_bf16_bits(rng, (B, d), 2.0)
+            dec = exact_bf16
+        else:
+            Wb = (rng.standard_normal((V, d)) * 0.5).astype(np.float16).view(np.uint16)
+            hb = (rng.standard_normal((B, d)) * 2.0).astype(np.float16).view(np.uint16)
+            dec = exact_fp16
+        Wq = [[dec(Wb[v, k]) for k in range(d)] for v in range(V)]
+        hq = [[dec(hb[n, k]) for k in range(d)] for n in range(B)]
+        out = o.head_greedy(Wb, hb, fmt)
+        z = out["logits"]
+        assert z.shape == (B, V)
+        for n in range(B):
+            ex = [sum(hq[n][k] * Wq[v][k] for k in range(d)) for v in range(V)]
+            Aex = [sum(abs(hq[n][k] * Wq[v][k]) for k in range(d)) for v in range(V)]
+            for v in range(V):
+                # float64 sum of exact products: error <= d * 2^-53 * A
+                assert abs(Fraction(float(z[n, v])) - ex[v]) <= \
+                    d * Fraction(1, 2**53) * Aex[v], (fmt, n, v)
+                assert abs(Fraction(float(out["A"][n, v])) - Aex[v]) <= \
+                    d * Fraction(1, 2**53) * Aex[v]
+            t = loop_argmax_lowest(ex)
+            assert int(out["token"][n]) == t, (fmt, n)
+            srt = sorted(ex, reverse=True)
+            g = (srt[0] - srt[1]) / exact_ulp_bf16(srt[0])
+            assert abs(Fraction(float(out["gap"][n])) - g) <= abs(g) * Fraction(1, 2**40) + \
+                Fraction(1, 2**40), (fmt, n, float(out["gap"][n]), float(g))
+
+
+def pin_logsumexp_mpmath(o):
+    """log-sum-exp and logp against 60-digit mpmath and scipy's routine."""
+    import mpmath
+    from scipy.special import logsumexp as scipy_lse
+    mpmath.mp.dps = 60
+    rng = np.random.default_rng(11)
+    V, d, B = 16, 8, 4
+    Wb = _rand_bf16_bits(rng, (V, d), 1.0)
+    hb = _rand_bf16_bits(rng, (B, d), 3.0)
+    t = rng.integers(0, V, size=B).astype(np.int32)
+    out = o.head_logprob(Wb, hb, t, "bf16")
+    assert out["lse"].shape == (B,) and out["logp"].shape == (B,)
+    Wq = [[exact_bf16(Wb[v, k]) for k in range(d)] for v in range(V)]
+    hq = [[exact_bf16(hb[n, k]) for k in range(d)] for n in range(B)]
+    for n in range(B):
+        ex = [sum(hq[n][k] * Wq[v][k] for k in range(d)) for v in range(V)]
+        lse = mpmath.log(mpmath.fsum(mpmath.exp(mpmath.mpf(x.numerator) / x.denominator)
+                                     for x in ex))
+        lp = mpmath.mpf(ex[t[n]].numerator) / ex[t[n]].denominator - lse
+        assert abs(out["lse"][n] - float(lse)) <= 1e-13 * max(1.0, abs(float(lse)))
+        assert abs(out["logp"][n] - float(lp)) <= 1e-13 * max(1.0, abs(float(lse)))
+        zz = np.array([float(x) for x in ex])
+        assert abs(out["lse"][n] - scipy_lse(zz)) <= 1e-12 * max(1.0, abs(float(lse)))
+
+
+def pin_closed_forms(o):
+    """Uniform logits, a dominant logit, tiny winners, out-of-range targets."""
+    V = 16
+    # uniform logits c: lse = c + ln V, logp = -ln V for every target
+    z = np.full((3, V), [[-3.0], [0.0], [7.5]])
+    lse = o.logsumexp(z)
+    assert np.allclose(lse, np.array([-3.0, 0.0, 7.5]) + math.log(V), rtol=0, atol=1e-14)
+    lp = o.logprob(z, np.array([0, 5, 15]))
+    assert np.allclose(lp, -math.log(V), rtol=0, atol=1e-14)
+    # one dominant logit L: lse = L (to double precision), no overflow at L = 1000
+    z = np.zeros((1, V))
+    z[0, 9] = 1000.0
+    assert o.logsumexp(z)[0] == 1000.0
+    assert o.logprob(z, np.array([9]))[0] == 0.0
+    assert o.logprob(z, np.array([3]))[0] == -1000.0
+    # large negative logits: lse stays finite
+    assert np.isfinite(o.logsumexp(np.full((1, V), -1000.0)))[0]
+    # out-of-range target -> NaN
+    assert np.isnan(o.logprob(np.zeros((2, V)), np.array([-1, V]))).all()
+    # the ulp's lower clamp: m = 2^-127, s = 0 -> ulp 2^-133, gap 64
+    z = np.zeros((1, 4))
+    z[0, 2] = 2.0 ** -127
+    tok, gap, m, s = o.greedy(z)
+    assert tok[0] == 2 and gap[0] == 64.0
+    # negative winner: m = -1, s = -1 - 2^-7; ulp(-1) = 2^-7 -> gap 1
+    z = np.array([[-4.0, -1.0 - 2.0 ** -7, -1.0, -2.0]])
+    tok, gap, m, s = o.greedy(z)
+    assert tok[0] == 2 and gap[0] == 1.0
+    # V = 1: no runner-up
+    tok, gap, m, s = o.greedy(np.array([[0.25]]))
+    assert tok[0] == 0 and gap[0] == np.inf
+    # ulp on both sides of a binade edge
+    assert o.ulp_bf16(np.array([1.0]))[0] == 2.0 ** -7
+    assert o.ulp_bf16(np.array([0.99609375]))[0] == 2.0 ** -8
+    assert o.ulp_bf16(np.array([-3.5]))[0] == 2.0 ** -6
+
+
+def pin_page_examples(o):
+    """Values printed on the pages: ties, the step-0 cushion, fp limits."""
+    pe = read_page_examples()
+    # float non-associativity (harness arithmetic is IEEE double)
+    assert (0.1 + 1e20) - 1e20 == pe["nonassoc_left"]
+    assert 0.1 + (1e20 - 1e20) == pe["nonassoc_right"]
+    # 2^24 + 1 rounds to 2^24 in fp32
+    lim = np.float32(pe["fp32_int_limit"])
+    assert lim + np.float32(1) == lim and lim - np.float32(1) != lim
+    # step 457: a 0.03 lead wins; an exact tie goes to the lower id (" is")
+    id_is, id_introduces = 3, 11
+    z = np.zeros((2, 16))
+    z[0, id_introduces] = 5.0 + pe["step457_lead"]
+    z[0, id_is] = 5.0
+    z[1, id_introduces] = 5.0
+    z[1, id_is] = 5.0
+    tok, gap, _, _ = o.greedy(z)
+    assert tok[0] == id_introduces and tok[1] == id_is and gap[1] == 0.0
+    # step 0: shifts of at most 0.094 cannot move a winner with a 2.66 gap
+    rng = np.random.default_rng(3)
+    base = rng.uniform(-5, 5, size=(200, 64))
+    w = rng.integers(0, 64, size=200)
+    base[np.arange(200), w] = base.max(axis=1) + pe["step0_top2_gap"]
+    shift = rng.uniform(-pe["step0_max_shift"], pe["step0_max_shift"], size=base.shape)
+    t0, _, _, _ = o.greedy(base)
+    t1, _, _, _ = o.greedy(base + shift)
+    assert (t0 == w).all() and (t1 == w).all()
+    # near-tie gaps are fractions of an ulp: in the binade [1, 2) the bf16 ulp
+    # is 2^-7, so logits 1.5 and 1.5 - g * 2^-7 are g ulp apart
+    for g in (pe["near_tie_gap_min_ulp"], pe["near_tie_gap_max_ulp"]):
+        z = np.array([[1.5 - g * 2.0 ** -7, 1.5, -2.0]])
+        tok, gap, m, s = o.greedy(z)
+        assert tok[0] == 1
+        assert abs(gap[0] - g) <= 1e-12 and gap[0] < pe["one_ulp_rule"]
+
+
+def pin_int_head(o):
+    """Integer head: closed-form bound, big-integer dots, int ties."""
+    d = 4096
+    W = np.full((3, d), 127, np.int8)
+    W[1] = -127
+    W[2, :] = -128
+    h = np.full((2, d), 127, np.int8)
+    h[1] = -128
+    out = o.head_greedy(W, h, "int8")
+    z = out["logits"]
+    assert z.shape == (2, 3)
+    # d * 127^2 = 66,064,384 < 2^31: the int32 accumulator cannot overflow
+    assert int(z[0, 0]) == 66_064_384 == d * 127 * 127 < 2**31
+    assert int(z[0, 1]) == -66_064_384
+    assert int(z[1, 2]) == d * 128 * 128 == 2**26
+    rng = np.random.default_rng(5)
+    V, d, B = 40, 24, 6
+    W = rng.integers(-128, 128, size=(V, d), dtype=np.int8)
+    W[33] = W[7]                      # exact tie: rows 7 and 33
+    h = rng.integers(-128, 128, size=(B, d), dtype=np.int8)
+    h[0] = W[7]
+    out = o.head_greedy(W, h, "int8")
+    for n in range(B):
+        ex = [sum(int(a) * int(b) for a, b in zip(W[v].tolist(), h[n].tolist()))
+              for v in range(V)]
+        assert [int(x) for x in out["logits"][n]] == ex, n
+        t = loop_argmax_lowest(ex)
+        assert int(out["token"][n]) == t
+        srt = sorted(ex, reverse=True)
+        assert int(out["gap"][n]) == srt[0] - srt[1]
+    assert int(out["token"][0]) == 7 and int(out["gap"][0]) == 0
+    assert o.bigint_dot(W[3], h[2]) == sum(int(a) * int(b) for a, b in
+                                            zip(W[3].tolist(), h[2].tolist()))
+
+
+def pin_invariants(o):
+    """Row permutation, duplicated rows, logp <= 0, lse >= max, sum p = 1, flips."""
+    rng = np.random.default_rng(21)
+    V, d, B = 37, 16, 9
+    Wb = _rand_bf16_bits(rng, (V, d), 0.3)
+    hb = _rand_bf16_bits(rng, (B, d), 1.0)
+    hb[4] = hb[1]                                  # duplicated row
+    t = rng.integers(0, V, size=B).astype(np.int32)
+    g = o.head_greedy(Wb, hb, "bf16")
+    lp = o.head_logprob(Wb, hb, t, "bf16")
+    perm = rng.permutation(B)
+    gp = o.head_greedy(Wb, hb[perm], "bf16")
+    lpp = o.head_logprob(Wb, hb[perm], t[perm], "bf16")
+    assert (gp["token"] == g["token"][perm]).all()
+    assert (gp["gap"] == g["gap"][perm]).all()
+    assert (lpp["logp"] == lp["logp"][perm]).all()
+    assert g["token"][4] == g["token"][1] and g["gap"][4] == g["gap"][1]
+    assert (lp["logp"] <= 0).all()
+    assert (lp["lse"] >= g["logits"].max(axis=1)).all()
+    # sum over all targets of p = 1
+    allt = o.logprob(np.repeat(lp["logits"][:1], V, axis=0), np.arange(V))
+    assert abs(np.exp(allt).sum() - 1.0) <= 1e-12
+    assert (g["gap"] >= 0).all()
+    # gap == 0 exactly when the maximum is attained twice
+    z = g["logits"]
+    ties = (z == z.max(axis=1, keepdims=True)).sum(axis=1) >= 2
+    assert ((g["gap"] == 0) == ties).all()
+    # token-flip criterion ("Greedy Decoding Has a Precision Clause", section
+    # "Token-ranking margins ..."): with winner v1 and perturbation D, the
+    # winner changes iff some v != v1 has D(v) - D(v1) >= z(v1) - z(v), with
+    # equality enough only for v < v1 (an exact tie goes to the lower id).
+    # Dyadic values keep every sum exact.
+    for _ in range(300):
+        z = rng.integers(-64, 64, size=(1, 12)) / 8.0
+        D = rng.integers(-8, 9, size=(1, 12)) / 8.0
+        v1 = int(o.greedy(z)[0][0])
+        changed = int(o.greedy(z + D)[0][0]) != v1
+        pred = False
+        for v in range(12):
+            if v == v1:
+                continue
+            lhs = D[0, v] - D[0, v1]
+            rhs = z[0, v1] - z[0, v]
+            if lhs > rhs or (lhs == rhs and v < v1):
+                pred = True
+        assert changed == pred
+
+
+def pin_gap_from_top2(o):
+    """The float32 gap the library must report for its own top-2 values."""
+    m = np.array([1.0, 4.03125, 0.5, -1.0, 3.0], np.float32)
+    s = np.array([0.99609375, 4.0, 0.5, -1.0078125, -3.0], np.float32)
+    g = o.gap_from_top2_f32(m, s)
+    assert g.dtype == np.float32
+    assert g.tolist() == [0.5, 1.0, 0.0, 1.0, 6.0 / 2.0 ** -6]
+
+
+ALL_PINS = [pin_tiny_golden, pin_bruteforce_float, pin_logsumexp_mpmath,
+            pin_closed_forms, pin_page_examples, pin_int_head, pin_invariants,
+            pin_gap_from_top2]
+
+
+def failing_pins(o):
+    """Names of the pins that fail (AssertionError or any exception)."""
+    bad = []
+    for p in ALL_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                p(o)
+        except Exception:   # noqa: BLE001 - a mutated oracle may fail any way
+            bad.append(p.__name__)
+    return bad

@@ -1,0 +1,84 @@
+"""The CPU oracle against its pins, and planted mistakes against the pins.
+
+No GPU: these run in the CPU suite.
+"""
+import os
+import types
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import oracle_pins as pins
+
+ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                          "oracle", "head.py")
+
+
+@pytest.mark.parametrize("pin", pins.ALL_PINS, ids=lambda p: p.__name__)
+def test_oracle_pin(pin):
+    pin(oracle)
+
+
+# Each mutant is a plausible mistake in the oracle: (snippet, replacement).
+MUTANTS = {
+    "tie_to_highest_id": ("token = np.argmax(z, axis=1).astype(np.int64)\n    m = z[np.arange(z.shape[0]), token]\n    if z.shape[1] >= 2:\n        s = np.sort(z, axis=1)[:, -2]\n    else:\n        s = np.full(z.shape[0], -np.inf",
+                          "token = (z.shape[1] - 1 - np.argmax(z[:, ::-1], axis=1)).astype(np.int64)\n    m = z[np.arange(z.shape[0]), token]\n    if z.shape[1] >= 2:\n        s = np.sort(z, axis=1)[:, -2]\n    else:\n        s = np.full(z.shape[0], -np.inf"),
+    "runner_up_distinct": ("        s = np.sort(z, axis=1)[:, -2]\n    else:\n        s = np.full(z.shape[0], -np.inf",
+                           "        s = np.array([np.unique(r)[-2] if len(np.unique(r)) > 1 else r[0] for r in z])\n    else:\n        s = np.full(z.shape[0], -np.inf"),
+    "ulp_exponent_off_by_one": ("return np.ldexp(1.0, E - 7)", "return np.ldexp(1.0, E - 8)"),
+    "ulp_no_clamp": ("E = np.where(m == 0, -126, np.maximum(e - 1, -126))",
+                     "E = np.where(m == 0, -126, e - 1)"),
+    "ulp_floor_wrong": ("np.maximum(e - 1, -126)", "np.maximum(e, -126)"),
+    "logits_transposed": ("    z = h @ W.T\n", "    z = (W @ h.T)\n"),
+    "logits_dropped_term": ("    z = h @ W.T\n", "    z = h[:, :-1] @ W[:, :-1].T\n"),
+    "logits_sign": ("    z = h @ W.T\n", "    z = -(h @ W.T)\n"),
+    "abs_bound_signed": ("A = np.abs(h) @ np.abs(W).T", "A = np.abs(h @ W.T)"),
+    "lse_no_shift": ("return M + np.log(np.sum(np.exp(z - M[:, None]), axis=1))",
+                     "return np.log(np.sum(np.exp(z), axis=1))"),
+    "lse_drops_max": ("return M + np.log(np.sum(np.exp(z - M[:, None]), axis=1))",
+                      "return np.log(np.sum(np.exp(z - M[:, None]), axis=1))"),
+    "logp_sign": ("return zt - logsumexp(z)", "return logsumexp(z) - zt"),
+    "logp_wrong_index": ("zt = np.where(ok, z[np.arange(B), np.where(ok, t, 0)], np.nan)",
+                         "zt = np.where(ok, z[np.arange(B), np.where(ok, (t + 1) % V, 0)], np.nan)"),
+    "bf16_decode_shift": ("astype(np.uint32) << np.uint32(16)", "astype(np.uint32) << np.uint32(15)"),
+    "fp16_as_bf16": ("return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)",
+                     "return decode_bf16(bits)"),
+    "int_narrow_accumulator": ("return np.asarray(h, dtype=np.int64) @ np.asarray(W, dtype=np.int64).T",
+                               "return (np.asarray(h, dtype=np.int64) @ np.asarray(W, dtype=np.int64).T).astype(np.int16).astype(np.int64)"),
+    "int_gap_reversed": ("        gap = m - s\n", "        gap = s - m\n"),
+    "gap_f32_rounded_difference": ("    with np.errstate(invalid=\"ignore\"):\n        return ((m - s) / ulp_bf16(m)).astype(np.float32)",
+                                   "    with np.errstate(invalid=\"ignore\"):\n        return ((m - s) / ulp_bf16(s)).astype(np.float32)"),
+}
+
+
+def _mutant(name):
+    src = open(ORACLE_SRC).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) >= 1, f"mutant {name}: snippet not found in the oracle"
+    mod = types.ModuleType(f"oracle_mutant_{name}")
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), mod.__dict__)
+    return mod
+
+
+def test_unmutated_copy_passes():
+    src = open(ORACLE_SRC).read()
+    mod = types.ModuleType("oracle_copy")
+    exec(compile(src, "<copy>", "exec"), mod.__dict__)
+    assert pins.failing_pins(mod) == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name):
+    assert pins.failing_pins(_mutant(name)), f"no pin catches mutant {name}"
+
+
+def test_synth_is_deterministic_and_formats():
+    import synth
+    a = synth.small_float(1, 50, 24, 3)
+    b = synth.small_float(1, 50, 24, 3)
+    assert (a["W"] == b["W"]).all() and (a["h"] == b["h"]).all()
+    assert a["W"].dtype == np.uint16 and a["W"].shape == (50, 24)
+    x = np.array([1.0, 1.00390625, 1.01171875, -3.0], np.float32)
+    # ties to even at the halfway points 1 + 2^-8 and 1 + 3 * 2^-8
+    assert synth.bf16_bits_from_f32(x).tolist() == [0x3F80, 0x3F80, 0x3F82, 0xC040]
