@@ -1,0 +1,155 @@
+/*
+ * detlm_head.h -- batch-invariant LLM output head (lm_head) for GB300 (sm_103a).
+ *
+ * The output head maps final hidden rows h [B, d] to vocabulary logits
+ * z = h . W^T [B, V] and decides the next token ("Greedy Decoding Has a
+ * Precision Clause", section "Token-ranking margins explain why numerical
+ * error sometimes matters": the lm_head converts the final transformer
+ * representation into vocabulary scores). Each call fuses the decision into
+ * the projection: greedy argmax with ties to the lowest token id, the gap
+ * between the two best logits in bf16 ulps, or the log-probability of a
+ * target token.
+ *
+ * Row invariance: every output of a row is bit-identical whatever the batch
+ * size B and whatever other rows share the call, because every reduction
+ * order is fixed by the weight's shape (V, d) and never by the row count
+ * ("TandemLLM docs, 12 Exactness", section 12.2: matrix-product kernels fix
+ * their reduction order by the weight's shape, never by the row count).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *_dev are device pointers (or managed memory); pointers
+ *    named *_host are host pointers. The library never frees caller memory.
+ *  - Layouts are row-major with d (the reduction axis) contiguous: W is
+ *    [V, d] as a linear layer stores its weight, h is [B, d], logits [B, V].
+ *  - Element types: DETLM_BF16 and DETLM_FP16 heads take 16-bit inputs and
+ *    accumulate in fp32; the DETLM_INT8 head takes int8 inputs and computes
+ *    int32 logits exactly.
+ *  - Calls that take a stream are asynchronous on that stream; outputs are
+ *    ready when the stream reaches that point. One handle serves one stream
+ *    at a time (a handle owns one workspace); handles are not thread-safe.
+ *  - Errors: every call returns a detlm_status_t and never aborts the
+ *    process. Argument errors are found on the host before any GPU work
+ *    (DETLM_EINVAL). Device-side conditions (a bounded wait that ran out, an
+ *    out-of-range target id) set the handle's device error word; they are
+ *    reported by detlm_head_check() and by the *_host calls.
+ */
+#ifndef DETLM_HEAD_H
+#define DETLM_HEAD_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct detlm_head detlm_head_t;     /* opaque handle */
+
+typedef enum {
+  DETLM_BF16 = 0,   /* bf16 W and h, fp32 accumulation, fp32 logits        */
+  DETLM_FP16 = 1,   /* IEEE fp16 W and h, fp32 accumulation, fp32 logits   */
+  DETLM_INT8 = 2    /* int8 W and h, exact int32 accumulation and logits   */
+} detlm_dtype_t;
+
+typedef enum {
+  DETLM_OK = 0,
+  DETLM_EINVAL = -1,        /* bad argument (null, size, alignment, dtype)  */
+  DETLM_EUNSUPPORTED = -2,  /* operation not defined for this head's dtype  */
+  DETLM_ECUDA = -3,         /* a CUDA runtime call failed (no GPU, launch)  */
+  DETLM_ETIMEOUT = -4,      /* a device-side bounded wait ran out           */
+  DETLM_ENOMEM = -5,        /* device or host allocation failed             */
+  DETLM_ETARGET = -6        /* a target id was outside [0, V); logp = NaN  */
+} detlm_status_t;
+
+/* Create a head over the weight W_dev [V, d] of the given dtype.
+ *
+ * "Greedy Decoding Has a Precision Clause", section "Token-ranking margins
+ * ...": the weight of the lm_head projection. W is BORROWED: the caller keeps
+ * it alive and unchanged until detlm_head_destroy. The handle owns its TMA
+ * descriptors, its workspace and a device error word, all made on the
+ * current device.
+ * Requirements: 1 <= V < 2^31; d >= 1; for BF16/FP16 d % 8 == 0 and for INT8
+ * d % 16 == 0 (rows start on 16-byte boundaries); W_dev 16-byte aligned.
+ * Returns DETLM_EINVAL on a bad argument, DETLM_ECUDA when no usable GPU. */
+int detlm_head_create(detlm_head_t** out, const void* W_dev, int64_t V,
+                      int64_t d, int dtype);
+
+/* Grow the workspace so that calls with up to max_B rows allocate nothing.
+ * Optional: calls grow it on demand (a synchronous allocation). Call it
+ * before capturing calls into a CUDA graph. */
+int detlm_head_reserve(detlm_head_t* head, int64_t max_B);
+
+/* Greedy decision for B hidden rows h_dev [B, d].
+ *
+ * token_dev  int32 [B]: lowest index v attaining max_v z[n, v]
+ *            ("Eliminating Nondeterminism in LLM Inference with Integer-Only
+ *            Arithmetic", section "DetLLM": argmax breaks ties toward the
+ *            lowest token id).
+ * gap_dev    BF16/FP16 heads: float [B], (m - s) / ulp_bf16(m), m the best
+ *            logit, s the runner-up value of the multiset (s == m on a tie),
+ *            ulp_bf16(m) = 2^(max(floor(log2|m|), -126) - 7), computed from
+ *            the fp32 logits and rounded once to float ("TandemLLM docs, 12
+ *            Exactness", section 12.2: the top-two gap in bf16 ulps). V == 1
+ *            gives +inf.
+ *            INT8 head: int32 [B], the exact m - s (INT32_MAX when V == 1).
+ * logits_dev optional (NULL to skip): float [B, V] fp32 logits (int32 for
+ *            INT8) ("TandemLLM docs, 12 Exactness", 12.2: the head returns
+ *            fp32 logits).
+ * B == 0 is a no-op. h_dev must be 16-byte aligned; outputs 4-byte aligned. */
+int detlm_head_greedy(detlm_head_t* head, const void* h_dev, int64_t B,
+                      int32_t* token_dev, void* gap_dev, void* logits_dev,
+                      cudaStream_t stream);
+
+/* Log-probability of one target token per row (BF16/FP16 heads only).
+ *
+ * logp_dev[n] = z[n, targets[n]] - log sum_v exp(z[n, v]) in fp32
+ * ("batch-logprob-gap": the trainer's per-token log-probability;
+ * "Inference and Decoding", section 3, Temperature: softmax at tau = 1).
+ * A target outside [0, V) gives NaN and sets DETLM_ETARGET in the error word.
+ * INT8 heads return DETLM_EUNSUPPORTED. */
+int detlm_head_logprob(detlm_head_t* head, const void* h_dev,
+                       const int32_t* targets_dev, int64_t B, float* logp_dev,
+                       cudaStream_t stream);
+
+/* Host-buffer forms of the two calls: copy h (and targets) from host memory,
+ * run the call, copy the results back, wait for the stream, and report the
+ * error word. Host buffers may be pageable; pinned buffers copy faster.
+ * Device staging buffers are owned by the handle and grow on demand. */
+int detlm_head_greedy_host(detlm_head_t* head, const void* h_host, int64_t B,
+                           int32_t* token_host, void* gap_host,
+                           void* logits_host, cudaStream_t stream);
+int detlm_head_logprob_host(detlm_head_t* head, const void* h_host,
+                            const int32_t* targets_host, int64_t B,
+                            float* logp_host, cudaStream_t stream);
+
+/* Wait for the stream, read and clear the handle's device error word.
+ * DETLM_ETIMEOUT if a kernel's bounded wait ran out (its outputs are then
+ * undefined), else DETLM_ETARGET if a target id was out of range, else OK. */
+int detlm_head_check(detlm_head_t* head, cudaStream_t stream);
+
+/* Record start/stop around the projection kernel of the NEXT call only (one
+ * shot), for timing that kernel with CUDA events on the call's stream. */
+int detlm_head_time_next(detlm_head_t* head, cudaEvent_t start,
+                         cudaEvent_t stop);
+
+/* Test hook for failure detection. flags = DETLM_DEBUG_STALL makes the next
+ * calls' MMA issuer wait on a barrier nothing arrives on, so the kernel's
+ * bounded wait runs out after timeout_ns and the call reports
+ * DETLM_ETIMEOUT; flags = 0 restores normal operation. timeout_ns = 0 keeps
+ * the default limit (2 s). */
+#define DETLM_DEBUG_STALL 1
+int detlm_head_debug(detlm_head_t* head, int flags, uint64_t timeout_ns);
+
+/* Shape queries: number of 128-row vocabulary tiles, and the column tile
+ * (padded rows of h per MMA) a call with B rows uses. */
+int detlm_head_tiles(const detlm_head_t* head, int64_t B, int32_t* n_vtiles,
+                     int32_t* n_cols);
+
+void detlm_head_destroy(detlm_head_t* head);
+
+const char* detlm_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DETLM_HEAD_H */

@@ -1,0 +1,215 @@
+"""Thin ctypes binding of the C ABI in ``include/detlm_head.h``.
+
+Argument marshalling only: every step of the output head runs in the CUDA
+library. Functions keep the C names; ``Head`` wraps a handle for torch
+tensors (device memory and streams come from PyTorch). There is no fallback:
+if the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib",
+                         "libdetlm_head.so")
+
+DETLM_BF16, DETLM_FP16, DETLM_INT8 = 0, 1, 2
+DTYPES = {"bf16": DETLM_BF16, "fp16": DETLM_FP16, "int8": DETLM_INT8}
+DETLM_OK, DETLM_EINVAL, DETLM_EUNSUPPORTED, DETLM_ECUDA = 0, -1, -2, -3
+DETLM_ETIMEOUT, DETLM_ENOMEM, DETLM_ETARGET = -4, -5, -6
+DETLM_DEBUG_STALL = 1
+
+_vp, _i64, _i32, _u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64
+_SIGS = {
+    "detlm_head_create": (_i32, [ctypes.POINTER(_vp), _vp, _i64, _i64, _i32]),
+    "detlm_head_reserve": (_i32, [_vp, _i64]),
+    "detlm_head_greedy": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp]),
+    "detlm_head_logprob": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
+    "detlm_head_greedy_host": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp]),
+    "detlm_head_logprob_host": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
+    "detlm_head_check": (_i32, [_vp, _vp]),
+    "detlm_head_time_next": (_i32, [_vp, _vp, _vp]),
+    "detlm_head_debug": (_i32, [_vp, _i32, _u64]),
+    "detlm_head_tiles": (_i32, [_vp, _i64, ctypes.POINTER(ctypes.c_int32),
+                                ctypes.POINTER(ctypes.c_int32)]),
+    "detlm_head_destroy": (None, [_vp]),
+    "detlm_status_string": (ctypes.c_char_p, [_i32]),
+}
+
+_lib = None
+
+
+class DetlmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load the CUDA library (built by ``invariant_output_head_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"{_LIB_PATH} is missing: build it with "
+            "`python -m invariant_output_head_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().detlm_status_string(status).decode()
+
+
+def _check(st: int, what: str):
+    if st != DETLM_OK:
+        raise DetlmError(st, what)
+
+
+# ---- the C entry points, by name (pointers and streams as ints) ----------
+
+def detlm_head_create(W_ptr: int, V: int, d: int, dtype: int) -> int:
+    out = _vp()
+    _check(load_library().detlm_head_create(ctypes.byref(out), W_ptr, V, d, dtype),
+           "detlm_head_create")
+    return out.value
+
+
+def detlm_head_reserve(handle: int, max_B: int) -> None:
+    _check(load_library().detlm_head_reserve(handle, max_B), "detlm_head_reserve")
+
+
+def detlm_head_greedy(handle, h_ptr, B, token_ptr, gap_ptr, logits_ptr, stream) -> None:
+    _check(load_library().detlm_head_greedy(handle, h_ptr, B, token_ptr, gap_ptr,
+                                            logits_ptr, stream), "detlm_head_greedy")
+
+
+def detlm_head_logprob(handle, h_ptr, targets_ptr, B, logp_ptr, stream) -> None:
+    _check(load_library().detlm_head_logprob(handle, h_ptr, targets_ptr, B, logp_ptr,
+                                             stream), "detlm_head_logprob")
+
+
+def detlm_head_greedy_host(handle, h_ptr, B, token_ptr, gap_ptr, logits_ptr, stream) -> None:
+    _check(load_library().detlm_head_greedy_host(handle, h_ptr, B, token_ptr, gap_ptr,
+                                                 logits_ptr, stream),
+           "detlm_head_greedy_host")
+
+
+def detlm_head_logprob_host(handle, h_ptr, targets_ptr, B, logp_ptr, stream) -> None:
+    _check(load_library().detlm_head_logprob_host(handle, h_ptr, targets_ptr, B,
+                                                  logp_ptr, stream),
+           "detlm_head_logprob_host")
+
+
+def detlm_head_check(handle, stream) -> int:
+    return load_library().detlm_head_check(handle, stream)
+
+
+def detlm_head_time_next(handle, start_evt: int, stop_evt: int) -> None:
+    _check(load_library().detlm_head_time_next(handle, start_evt, stop_evt),
+           "detlm_head_time_next")
+
+
+def detlm_head_debug(handle, flags: int, timeout_ns: int = 0) -> None:
+    _check(load_library().detlm_head_debug(handle, flags, timeout_ns), "detlm_head_debug")
+
+
+def detlm_head_tiles(handle, B: int):
+    nv, nc = ctypes.c_int32(), ctypes.c_int32()
+    _check(load_library().detlm_head_tiles(handle, B, ctypes.byref(nv), ctypes.byref(nc)),
+           "detlm_head_tiles")
+    return nv.value, nc.value
+
+
+def detlm_head_destroy(handle) -> None:
+    if handle:
+        load_library().detlm_head_destroy(handle)
+
+
+def detlm_status_string(status: int) -> str:
+    return status_string(status)
+
+
+# ---- torch convenience wrapper ------------------------------------------
+
+def _stream_ptr(stream) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class Head:
+    """One output head over a device weight W [V, d] (bf16, fp16 or int8 tensor).
+
+    The handle borrows W: keep the tensor alive while the Head is in use.
+    """
+
+    def __init__(self, W, dtype: str | None = None):
+        import torch
+        if dtype is None:
+            dtype = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.int8: "int8"}[W.dtype]
+        if not W.is_cuda or not W.is_contiguous() or W.dim() != 2:
+            raise ValueError("W must be a contiguous 2-D CUDA tensor [V, d]")
+        self.W = W
+        self.dtype = dtype
+        self.V, self.d = int(W.shape[0]), int(W.shape[1])
+        self.handle = detlm_head_create(W.data_ptr(), self.V, self.d, DTYPES[dtype])
+
+    def close(self):
+        if getattr(self, "handle", None):
+            detlm_head_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:   # noqa: BLE001 - interpreter shutdown
+            pass
+
+    def _check_h(self, h):
+        if not h.is_cuda or not h.is_contiguous() or h.dim() != 2 or h.shape[1] != self.d:
+            raise ValueError(f"h must be a contiguous CUDA tensor [B, {self.d}]")
+
+    def greedy(self, h, with_logits: bool = False, stream=None, out=None):
+        """Returns (token int32 [B], gap [B], logits [B, V] or None) on h's device."""
+        import torch
+        self._check_h(h)
+        B = int(h.shape[0])
+        gdt = torch.int32 if self.dtype == "int8" else torch.float32
+        if out is None:
+            token = torch.empty(B, dtype=torch.int32, device=h.device)
+            gap = torch.empty(B, dtype=gdt, device=h.device)
+            logits = torch.empty((B, self.V), dtype=gdt, device=h.device) if with_logits else None
+        else:
+            token, gap, logits = out
+        detlm_head_greedy(self.handle, h.data_ptr(), B, token.data_ptr(), gap.data_ptr(),
+                          logits.data_ptr() if logits is not None else None,
+                          _stream_ptr(stream))
+        return token, gap, logits
+
+    def logprob(self, h, targets, stream=None, out=None):
+        import torch
+        self._check_h(h)
+        B = int(h.shape[0])
+        if targets.dtype != torch.int32 or not targets.is_cuda or targets.numel() != B:
+            raise ValueError("targets must be an int32 CUDA tensor [B]")
+        logp = torch.empty(B, dtype=torch.float32, device=h.device) if out is None else out
+        detlm_head_logprob(self.handle, h.data_ptr(), targets.data_ptr(), B, logp.data_ptr(),
+                           _stream_ptr(stream))
+        return logp
+
+    def check(self, stream=None) -> int:
+        return detlm_head_check(self.handle, _stream_ptr(stream))
+
+    def tiles(self, B: int):
+        return detlm_head_tiles(self.handle, B)

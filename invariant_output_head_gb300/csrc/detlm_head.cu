@@ -1,0 +1,514 @@
+// detlm_head.cu -- the C ABI of the output-head library (host side).
+//
+// Validates every argument on the host before any GPU work, owns the TMA
+// descriptor of W, the split-V record workspace and the device error word,
+// encodes the TMA descriptor of h per call (a pure host computation), and
+// launches kernel 1 (projection + per-tile records) and kernel 2 (fixed-order
+// merge, launched with programmatic dependent launch so that its launch
+// overlaps kernel 1's tail).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "detlm_head.h"
+#include "head_kernels.cuh"
+#include "int8_kernels.cuh"
+
+using namespace detlm;
+
+struct detlm_head {
+  int device = 0;
+  int dtype = 0;
+  int64_t V = 0, d = 0;
+  const void* W = nullptr;
+  CUtensorMap tmW;
+  int n_vt = 0, nk = 0, num_sms = 0;
+  int* d_err = nullptr;
+  // split-V record workspace
+  void* ws = nullptr;
+  int64_t ws_B = 0;
+  // device staging for the *_host calls
+  void* stage = nullptr;
+  size_t stage_bytes = 0;
+  // test hook and timing hook
+  int stall = 0;
+  uint64_t timeout_ns = 2000000000ull;
+  cudaEvent_t t_start = nullptr, t_stop = nullptr;
+};
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool load_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+size_t elem_bytes(int dtype) { return dtype == DETLM_INT8 ? 1 : 2; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// 2-D K-major tensor map: dims {d, rows}, box {128 bytes of K, box_rows},
+// 128-byte swizzle, zero fill outside the tensor.
+bool encode_2d(CUtensorMap* m, int dtype, const void* base, int64_t d, int64_t rows,
+               uint32_t box_rows) {
+  const CUtensorMapDataType t = dtype == DETLM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                : dtype == DETLM_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                      : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const size_t eb = elem_bytes(dtype);
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * eb};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / eb), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, t, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Hidden rows per MMA (N): B rounded up to 16, at most 128. Larger B is
+// covered by several column tiles. The result of a row does not depend on N.
+int cols_for(int64_t B) {
+  if (B >= kMaxN) return kMaxN;
+  const int n = static_cast<int>((B + 15) / 16) * 16;
+  return n < 16 ? 16 : n;
+}
+
+uint32_t tmem_cols_for(int ncols) {
+  uint32_t c = 32;
+  while (c < static_cast<uint32_t>(ncols)) c <<= 1;
+  return c;
+}
+
+int stages_for(int N) {
+  const SmemLayout L1 = smem_layout(N, 1);
+  const uint32_t fixed = L1.total - L1.stage_bytes + 2u * kMaxStages * 8u + 1024u;
+  int s = static_cast<int>((kSmemLimit - fixed) / L1.stage_bytes);
+  if (s > kMaxStages) s = kMaxStages;
+  return s;
+}
+
+int status_from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return DETLM_OK;
+  if (e == cudaErrorMemoryAllocation) return DETLM_ENOMEM;
+  return DETLM_ECUDA;
+}
+
+// workspace: rec_m, rec_i, rec_s [n_vt, B] and zt [B], 256-byte aligned parts
+size_t ws_part(int64_t n) { return (static_cast<size_t>(n) * 4 + 255) & ~static_cast<size_t>(255); }
+size_t ws_bytes_for(const detlm_head* h, int64_t B) {
+  return 3 * ws_part(static_cast<int64_t>(h->n_vt) * B) + ws_part(B);
+}
+
+int ensure_ws(detlm_head* h, int64_t B, cudaStream_t stream) {
+  if (B <= h->ws_B) return DETLM_OK;
+  if (h->ws != nullptr) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return status_from_cuda(e);
+    cudaFree(h->ws);
+    h->ws = nullptr;
+    h->ws_B = 0;
+  }
+  void* p = nullptr;
+  cudaError_t e = cudaMalloc(&p, ws_bytes_for(h, B));
+  if (e != cudaSuccess) return status_from_cuda(e);
+  h->ws = p;
+  h->ws_B = B;
+  return DETLM_OK;
+}
+
+struct WsView { float* m; int32_t* i; float* s; float* zt; };
+WsView ws_view(const detlm_head* h, int64_t B) {
+  uint8_t* b = static_cast<uint8_t*>(h->ws);
+  const size_t part = ws_part(static_cast<int64_t>(h->n_vt) * B);
+  WsView w;
+  w.m = reinterpret_cast<float*>(b);
+  w.i = reinterpret_cast<int32_t*>(b + part);
+  w.s = reinterpret_cast<float*>(b + 2 * part);
+  w.zt = reinterpret_cast<float*>(b + 3 * part);
+  return w;
+}
+
+template <int MODE>
+int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* targets,
+                 int32_t* token, float* gap, float* logits, float* logp, cudaStream_t stream) {
+  const int N = cols_for(B);
+  CUtensorMap tmH;
+  if (!encode_2d(&tmH, h->dtype, h_dev, h->d, B, static_cast<uint32_t>(N))) return DETLM_EINVAL;
+  int st = ensure_ws(h, B, stream);
+  if (st != DETLM_OK) return st;
+  const WsView w = ws_view(h, B);
+
+  HeadParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.V = static_cast<int32_t>(h->V);
+  p.d = static_cast<int32_t>(h->d);
+  p.B = static_cast<int32_t>(B);
+  p.N = N;
+  p.n_vt = h->n_vt;
+  p.n_nt = static_cast<int32_t>((B + N - 1) / N);
+  p.nk = h->nk;
+  p.n_chunks = static_cast<int32_t>((h->d + kChunkK - 1) / kChunkK);
+  p.stages = stages_for(N);
+  p.tmem_cols = tmem_cols_for(2 * N);
+  p.idesc = idesc_f16(h->dtype == DETLM_BF16 ? 1u : 0u, kBM, static_cast<uint32_t>(N));
+  p.logits = logits;
+  p.targets = targets;
+  p.rec_m = w.m;
+  p.rec_i = w.i;
+  p.rec_s = w.s;
+  p.zt = w.zt;
+  p.err = h->d_err;
+  p.stall = h->stall;
+  p.timeout_ns = h->timeout_ns;
+
+  const SmemLayout L = smem_layout(N, p.stages);
+  const size_t smem = L.total + 1024;
+  auto kern = head_gemm_kernel<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return status_from_cuda(e);
+  const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
+  const int grid = static_cast<int>(units < h->num_sms ? units : h->num_sms);
+
+  if (h->t_start) cudaEventRecord(h->t_start, stream);
+  kern<<<grid, kThreads, smem, stream>>>(h->tmW, tmH, p);
+  e = cudaGetLastError();
+  if (h->t_stop) {
+    cudaEventRecord(h->t_stop, stream);
+    h->t_start = h->t_stop = nullptr;
+  }
+  if (e != cudaSuccess) return status_from_cuda(e);
+
+  MergeParams mp;
+  mp.V = p.V;
+  mp.B = p.B;
+  mp.n_vt = p.n_vt;
+  mp.rec_m = w.m;
+  mp.rec_i = w.i;
+  mp.rec_s = w.s;
+  mp.zt = w.zt;
+  mp.targets = targets;
+  mp.token = token;
+  mp.gap = gap;
+  mp.logp = logp;
+  mp.err = h->d_err;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>((B + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, merge_kernel<MODE>, mp);
+  return status_from_cuda(e);
+}
+
+int launch_int8(detlm_head* h, const void* h_dev, int64_t B, int32_t* token, int32_t* gap,
+                int32_t* logits, cudaStream_t stream) {
+  const int N = int8_cols_for(B, h->d);
+  CUtensorMap tmH;
+  if (!encode_2d(&tmH, DETLM_INT8, h_dev, h->d, B, static_cast<uint32_t>(N))) return DETLM_EINVAL;
+  int st = ensure_ws(h, B, stream);
+  if (st != DETLM_OK) return st;
+  const WsView w = ws_view(h, B);
+
+  Int8Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.V = static_cast<int32_t>(h->V);
+  p.d = static_cast<int32_t>(h->d);
+  p.B = static_cast<int32_t>(B);
+  p.N = N;
+  p.n_vt = h->n_vt;
+  p.n_nt = static_cast<int32_t>((B + N - 1) / N);
+  p.nk = h->nk;
+  p.n_chunks = int8_chunks(h->d);
+  // fp16 ring of 3 stages when that leaves at least 4 int8 stages, else 2
+  const uint32_t fixed = int8_layout(N, 0, 0).total + (2u * kI8MaxStages8 + 2u * 3u) * 8u + 1024u;
+  const Int8Layout one = int8_layout(N, 1, 1);
+  p.s16 = 3;
+  if (static_cast<int64_t>(kSmemLimit) - fixed - 3 * one.st16 < 4 * static_cast<int64_t>(one.st8)) p.s16 = 2;
+  p.s8 = static_cast<int32_t>((kSmemLimit - fixed - p.s16 * one.st16) / one.st8);
+  if (p.s8 > kI8MaxStages8) p.s8 = kI8MaxStages8;
+  if (p.s8 < 2) return DETLM_EINVAL;   // cannot happen for N <= kI8MaxN
+  p.tmem_cols = tmem_cols_for(2 * p.n_chunks * N);
+  p.idesc = idesc_f16(0u, kBM, static_cast<uint32_t>(N));
+  p.logits = logits;
+  p.rec_m = reinterpret_cast<int32_t*>(w.m);
+  p.rec_i = w.i;
+  p.rec_s = reinterpret_cast<int32_t*>(w.s);
+  p.err = h->d_err;
+  p.stall = h->stall;
+  p.timeout_ns = h->timeout_ns;
+
+  const size_t smem = int8_layout(N, p.s8, p.s16).total + 1024;
+  cudaError_t e = cudaFuncSetAttribute(int8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return status_from_cuda(e);
+  const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
+  const int grid = static_cast<int>(units < h->num_sms ? units : h->num_sms);
+  if (h->t_start) cudaEventRecord(h->t_start, stream);
+  int8_gemm_kernel<<<grid, kI8Threads, smem, stream>>>(h->tmW, tmH, p);
+  e = cudaGetLastError();
+  if (h->t_stop) {
+    cudaEventRecord(h->t_stop, stream);
+    h->t_start = h->t_stop = nullptr;
+  }
+  if (e != cudaSuccess) return status_from_cuda(e);
+
+  Int8MergeParams mp;
+  mp.B = p.B;
+  mp.n_vt = p.n_vt;
+  mp.rec_m = p.rec_m;
+  mp.rec_i = p.rec_i;
+  mp.rec_s = p.rec_s;
+  mp.token = token;
+  mp.gap = gap;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>((B + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, int8_merge_kernel, mp);
+  return status_from_cuda(e);
+}
+
+int read_err(detlm_head* h, cudaStream_t stream) {
+  int hv = 0;
+  cudaError_t e = cudaMemcpyAsync(&hv, h->d_err, sizeof(int), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return status_from_cuda(e);
+  if (hv != 0) {
+    e = cudaMemsetAsync(h->d_err, 0, sizeof(int), stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return status_from_cuda(e);
+  }
+  if (hv & ERR_TIMEOUT) return DETLM_ETIMEOUT;
+  if (hv & ERR_TARGET) return DETLM_ETARGET;
+  return DETLM_OK;
+}
+
+int ensure_stage(detlm_head* h, size_t bytes, cudaStream_t stream) {
+  if (bytes <= h->stage_bytes) return DETLM_OK;
+  if (h->stage != nullptr) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return status_from_cuda(e);
+    cudaFree(h->stage);
+    h->stage = nullptr;
+    h->stage_bytes = 0;
+  }
+  cudaError_t e = cudaMalloc(&h->stage, bytes);
+  if (e != cudaSuccess) return status_from_cuda(e);
+  h->stage_bytes = bytes;
+  return DETLM_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool bad_B(int64_t B) { return B < 0 || B >= (int64_t{1} << 31); }
+
+}  // namespace
+
+extern "C" {
+
+const char* detlm_status_string(int status) {
+  switch (status) {
+    case DETLM_OK: return "ok";
+    case DETLM_EINVAL: return "invalid argument";
+    case DETLM_EUNSUPPORTED: return "operation not supported for this head's dtype";
+    case DETLM_ECUDA: return "CUDA runtime error (no usable GPU, or a launch failed)";
+    case DETLM_ETIMEOUT: return "a device-side bounded wait ran out";
+    case DETLM_ENOMEM: return "out of memory";
+    case DETLM_ETARGET: return "a target id was outside [0, V)";
+    default: return "unknown status";
+  }
+}
+
+int detlm_head_create(detlm_head_t** out, const void* W_dev, int64_t V, int64_t d, int dtype) {
+  if (out == nullptr) return DETLM_EINVAL;
+  *out = nullptr;
+  if (W_dev == nullptr || !aligned(W_dev, 16)) return DETLM_EINVAL;
+  if (dtype != DETLM_BF16 && dtype != DETLM_FP16 && dtype != DETLM_INT8) return DETLM_EINVAL;
+  if (V < 1 || V >= (int64_t{1} << 31) || d < 1 || d >= (int64_t{1} << 31)) return DETLM_EINVAL;
+  if ((d * static_cast<int64_t>(elem_bytes(dtype))) % 16 != 0) return DETLM_EINVAL;
+  if (dtype == DETLM_INT8 && d > kI8MaxD) return DETLM_EINVAL;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return DETLM_ECUDA;
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (major != 10 || sms <= 0) return DETLM_ECUDA;   // built for sm_103a only
+  if (!load_encode()) return DETLM_ECUDA;
+
+  detlm_head* h = new (std::nothrow) detlm_head();
+  if (h == nullptr) return DETLM_ENOMEM;
+  h->device = dev;
+  h->dtype = dtype;
+  h->V = V;
+  h->d = d;
+  h->W = W_dev;
+  h->num_sms = sms;
+  h->n_vt = static_cast<int>((V + kBM - 1) / kBM);
+  h->nk = static_cast<int>((d * static_cast<int64_t>(elem_bytes(dtype)) + kRowBytes - 1) / kRowBytes);
+  h->timeout_ns = kDefaultTimeoutNs;
+  if (!encode_2d(&h->tmW, dtype, W_dev, d, V, kBM)) {
+    delete h;
+    return DETLM_EINVAL;
+  }
+  e = cudaMalloc(&h->d_err, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
+  if (e != cudaSuccess) {
+    if (h->d_err) cudaFree(h->d_err);
+    delete h;
+    return status_from_cuda(e);
+  }
+  *out = h;
+  return DETLM_OK;
+}
+
+int detlm_head_reserve(detlm_head_t* h, int64_t max_B) {
+  if (h == nullptr || bad_B(max_B)) return DETLM_EINVAL;
+  return ensure_ws(h, max_B, nullptr);
+}
+
+int detlm_head_greedy(detlm_head_t* h, const void* h_dev, int64_t B, int32_t* token_dev,
+                      void* gap_dev, void* logits_dev, cudaStream_t stream) {
+  if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
+  if (B == 0) return DETLM_OK;
+  if (h_dev == nullptr || !aligned(h_dev, 16)) return DETLM_EINVAL;
+  if (token_dev == nullptr || !aligned(token_dev, 4)) return DETLM_EINVAL;
+  if (gap_dev == nullptr || !aligned(gap_dev, 4)) return DETLM_EINVAL;
+  if (logits_dev != nullptr && !aligned(logits_dev, 4)) return DETLM_EINVAL;
+  if (h->dtype == DETLM_INT8)
+    return launch_int8(h, h_dev, B, token_dev, static_cast<int32_t*>(gap_dev),
+                       static_cast<int32_t*>(logits_dev), stream);
+  return launch_float<MODE_GREEDY>(h, h_dev, B, nullptr, token_dev, static_cast<float*>(gap_dev),
+                                   static_cast<float*>(logits_dev), nullptr, stream);
+}
+
+int detlm_head_logprob(detlm_head_t* h, const void* h_dev, const int32_t* targets_dev, int64_t B,
+                       float* logp_dev, cudaStream_t stream) {
+  if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
+  if (h->dtype == DETLM_INT8) return DETLM_EUNSUPPORTED;
+  if (B == 0) return DETLM_OK;
+  if (h_dev == nullptr || !aligned(h_dev, 16)) return DETLM_EINVAL;
+  if (targets_dev == nullptr || !aligned(targets_dev, 4)) return DETLM_EINVAL;
+  if (logp_dev == nullptr || !aligned(logp_dev, 4)) return DETLM_EINVAL;
+  return launch_float<MODE_LOGPROB>(h, h_dev, B, targets_dev, nullptr, nullptr, nullptr, logp_dev,
+                                    stream);
+}
+
+int detlm_head_greedy_host(detlm_head_t* h, const void* h_host, int64_t B, int32_t* token_host,
+                           void* gap_host, void* logits_host, cudaStream_t stream) {
+  if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
+  if (B == 0) return DETLM_OK;
+  if (h_host == nullptr || token_host == nullptr || gap_host == nullptr) return DETLM_EINVAL;
+  const size_t hb = static_cast<size_t>(B) * h->d * elem_bytes(h->dtype);
+  const size_t ob = static_cast<size_t>(B) * 4;
+  const size_t lb = logits_host ? static_cast<size_t>(B) * h->V * 4 : 0;
+  int st = ensure_stage(h, round256(hb) + 2 * round256(ob) + round256(lb), stream);
+  if (st != DETLM_OK) return st;
+  uint8_t* s = static_cast<uint8_t*>(h->stage);
+  void* dh = s;
+  int32_t* dtok = reinterpret_cast<int32_t*>(s + round256(hb));
+  void* dgap = s + round256(hb) + round256(ob);
+  void* dlog = logits_host ? s + round256(hb) + 2 * round256(ob) : nullptr;
+  cudaError_t e = cudaMemcpyAsync(dh, h_host, hb, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return status_from_cuda(e);
+  st = detlm_head_greedy(h, dh, B, dtok, dgap, dlog, stream);
+  if (st != DETLM_OK) return st;
+  e = cudaMemcpyAsync(token_host, dtok, ob, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(gap_host, dgap, ob, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess && logits_host)
+    e = cudaMemcpyAsync(logits_host, dlog, lb, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return status_from_cuda(e);
+  return read_err(h, stream);
+}
+
+int detlm_head_logprob_host(detlm_head_t* h, const void* h_host, const int32_t* targets_host,
+                            int64_t B, float* logp_host, cudaStream_t stream) {
+  if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
+  if (h->dtype == DETLM_INT8) return DETLM_EUNSUPPORTED;
+  if (B == 0) return DETLM_OK;
+  if (h_host == nullptr || targets_host == nullptr || logp_host == nullptr) return DETLM_EINVAL;
+  const size_t hb = static_cast<size_t>(B) * h->d * elem_bytes(h->dtype);
+  const size_t ob = static_cast<size_t>(B) * 4;
+  int st = ensure_stage(h, round256(hb) + 2 * round256(ob), stream);
+  if (st != DETLM_OK) return st;
+  uint8_t* s = static_cast<uint8_t*>(h->stage);
+  void* dh = s;
+  int32_t* dt = reinterpret_cast<int32_t*>(s + round256(hb));
+  float* dlp = reinterpret_cast<float*>(s + round256(hb) + round256(ob));
+  cudaError_t e = cudaMemcpyAsync(dh, h_host, hb, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(dt, targets_host, ob, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return status_from_cuda(e);
+  st = detlm_head_logprob(h, dh, dt, B, dlp, stream);
+  if (st != DETLM_OK) return st;
+  e = cudaMemcpyAsync(logp_host, dlp, ob, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return status_from_cuda(e);
+  return read_err(h, stream);
+}
+
+int detlm_head_check(detlm_head_t* h, cudaStream_t stream) {
+  if (h == nullptr) return DETLM_EINVAL;
+  return read_err(h, stream);
+}
+
+int detlm_head_time_next(detlm_head_t* h, cudaEvent_t start, cudaEvent_t stop) {
+  if (h == nullptr || (start == nullptr) != (stop == nullptr)) return DETLM_EINVAL;
+  h->t_start = start;
+  h->t_stop = stop;
+  return DETLM_OK;
+}
+
+int detlm_head_debug(detlm_head_t* h, int flags, uint64_t timeout_ns) {
+  if (h == nullptr || (flags & ~DETLM_DEBUG_STALL) != 0) return DETLM_EINVAL;
+  h->stall = (flags & DETLM_DEBUG_STALL) ? 1 : 0;
+  h->timeout_ns = timeout_ns ? timeout_ns : kDefaultTimeoutNs;
+  return DETLM_OK;
+}
+
+int detlm_head_tiles(const detlm_head_t* h, int64_t B, int32_t* n_vtiles, int32_t* n_cols) {
+  if (h == nullptr || bad_B(B) || n_vtiles == nullptr || n_cols == nullptr) return DETLM_EINVAL;
+  *n_vtiles = h->n_vt;
+  *n_cols = h->dtype == DETLM_INT8 ? int8_cols_for(B, h->d) : cols_for(B);
+  return DETLM_OK;
+}
+
+void detlm_head_destroy(detlm_head_t* h) {
+  if (h == nullptr) return;
+  if (h->ws) cudaFree(h->ws);
+  if (h->stage) cudaFree(h->stage);
+  if (h->d_err) cudaFree(h->d_err);
+  delete h;
+}
+
+}  // extern "C"

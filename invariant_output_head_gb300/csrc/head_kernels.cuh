@@ -1,0 +1,500 @@
+// head_kernels.cuh -- the output-head kernels for GB300 (sm_103a).
+//
+// Kernel 1 (head_gemm_kernel): a persistent, warp-specialised projection
+//   z[n, v] = sum_k h[n, k] * W[v, k]
+// with W as the 128-row M operand of tcgen05.mma ("swap-AB": the vocabulary
+// runs along the tensor core's M axis and TMEM lanes, the hidden rows along
+// N). A unit of work is one 128-row vocabulary tile x N hidden rows, N a
+// multiple of 16 (the hidden rows padded with zeros). The K loop walks d in
+// ascending 128-byte blocks, four MMAs of K=16 each, always the same steps
+// for a given d: the reduction order of every logit is fixed by the weight's
+// shape, never by the row count ("TandemLLM docs, 12 Exactness", section
+// 12.2).
+//
+// Accumulation in K chunks: the tensor core's fp32 accumulation rounds each
+// K=16 step toward zero-ish, so a long K loop in one accumulator drifts by
+// about half an ulp per step when all products share a sign. K is therefore
+// cut into chunks of kChunkK elements (a function of d only); each chunk is
+// accumulated from zero in one of two TMEM slots (ping-pong), and the
+// epilogue adds the chunk sums in fp32 registers with round-to-nearest, in
+// ascending chunk order. This keeps every logit within 1e-6 * sum|w h| and
+// is the same arithmetic for every B.
+//
+// Warp 0 issues TMA loads into an S-stage ring, warp 1 issues the MMAs into
+// the two chunk slots, warps 2..5 drain each slot into running sums (one
+// thread per vocabulary row, up to 128 hidden rows per thread), then write
+// the optional fp32 logits and the per-tile decision record of each hidden
+// row:
+//   greedy : (m, i, s) = tile maximum, lowest index attaining it, runner-up
+//            value of the tile's multiset;
+//   logprob: (m, S) = tile maximum and sum_v exp(z_v - m), plus z[target].
+//
+// Kernel 2 (merge_kernel): one warp per hidden row folds the n_vt tile
+// records in a fixed order (lane l takes tiles l, l+32, ... in ascending
+// order, then a butterfly over lanes 1, 2, 4, 8, 16) -- a function of V only.
+// No atomics take part in any result.
+//
+// Both reductions are written so that a row's bits do not depend on its
+// column position in the tile or on B: the within-tile tree over the 128
+// vocabulary rows has the same shape for every column, and both merge
+// operators are commutative bit for bit.
+#pragma once
+#include <cuda.h>
+#include <cstdint>
+#include <cmath>
+#include "ptx.cuh"
+
+namespace detlm {
+
+constexpr int kBM = 128;          // vocabulary rows per tile = MMA M = TMEM lanes
+constexpr int kRowBytes = 128;    // bytes of K per stage and tile row (one swizzle row)
+constexpr int kThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kEpiThreads = 128;
+constexpr int kMaxN = 128;        // largest MMA N (running sums live in registers)
+constexpr int kChunkK = 128;      // K elements per accumulation chunk
+constexpr int kBlocksPerChunk = kChunkK / 64;   // 128-byte K blocks of 16-bit data
+constexpr int kMaxStages = 12;
+constexpr int kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
+
+enum : int { MODE_GREEDY = 0, MODE_LOGPROB = 1 };
+enum : int { ERR_TIMEOUT = 1, ERR_TARGET = 2 };
+
+struct HeadParams {
+  int32_t V, d, B;
+  int32_t N;            // hidden rows per unit (MMA N), multiple of 16, <= kMaxN
+  int32_t n_vt, n_nt;   // vocabulary tiles, hidden-row tiles
+  int32_t nk;           // K blocks of 128 bytes
+  int32_t n_chunks;     // K chunks of kChunkK elements
+  int32_t stages;
+  uint32_t tmem_cols;
+  uint32_t idesc;
+  float* logits;            // optional fp32 [B, V]
+  const int32_t* targets;   // logprob: [B]
+  float* rec_m;             // [n_vt, B] tile maximum
+  int32_t* rec_i;           // [n_vt, B] greedy: lowest index of the maximum
+  float* rec_s;             // [n_vt, B] greedy: runner-up; logprob: sum exp
+  float* zt;                // [B] logprob: target logit
+  int* err;                 // device error word
+  int32_t stall;            // test hook: MMA issuer waits on a dead barrier
+  uint64_t timeout_ns;
+};
+
+struct MergeParams {
+  int32_t V, B, n_vt;
+  const float* rec_m;
+  const int32_t* rec_i;
+  const float* rec_s;
+  const float* zt;
+  const int32_t* targets;
+  int32_t* token;
+  float* gap;
+  float* logp;
+  int* err;
+};
+
+// ------------------------------------------------------------ merge rules
+struct Top2 { float m; int32_t i; float s; };   // max, its lowest index, runner-up
+struct Lse { float m; float S; };               // max, sum exp(z - max)
+
+// Top-2 of a multiset with index tie-break: exact, associative, commutative.
+__device__ __forceinline__ Top2 top2_merge(const Top2& a, const Top2& b) {
+  const bool aw = (a.m > b.m) || (a.m == b.m && a.i < b.i);
+  Top2 r;
+  r.m = aw ? a.m : b.m;
+  r.i = aw ? a.i : b.i;
+  r.s = fmaxf(aw ? a.s : b.s, aw ? b.m : a.m);
+  return r;
+}
+
+// (m, S) pairs of log-sum-exp: commutative bit for bit (equal maxima add the
+// two sums with one rounding; otherwise the smaller side is scaled).
+__device__ __forceinline__ Lse lse_merge(const Lse& a, const Lse& b) {
+  Lse hi = a, lo = b;
+  if (a.m < b.m) { hi = b; lo = a; }
+  if (lo.m == -INFINITY) return hi;
+  const float e = (lo.m == hi.m) ? 1.0f : __expf(lo.m - hi.m);
+  return Lse{hi.m, fmaf(lo.S, e, hi.S)};
+}
+
+__device__ __forceinline__ Top2 shfl_xor(const Top2& x, int b) {
+  return Top2{__shfl_xor_sync(0xffffffffu, x.m, b), __shfl_xor_sync(0xffffffffu, x.i, b),
+              __shfl_xor_sync(0xffffffffu, x.s, b)};
+}
+__device__ __forceinline__ Lse shfl_xor(const Lse& x, int b) {
+  return Lse{__shfl_xor_sync(0xffffffffu, x.m, b), __shfl_xor_sync(0xffffffffu, x.S, b)};
+}
+__device__ __forceinline__ Top2 merge(const Top2& a, const Top2& b) { return top2_merge(a, b); }
+__device__ __forceinline__ Lse merge(const Lse& a, const Lse& b) { return lse_merge(a, b); }
+
+// One halving step of the transposed reduction over 16 columns held by each
+// lane: the lane keeps one half of its columns, sends the other half to the
+// partner lane ^ b and merges what it receives into the kept half.
+template <int H, typename T>
+__device__ __forceinline__ void transpose_step(T (&g)[16], int lane, int b) {
+  const bool up = (lane & b) != 0;
+#pragma unroll
+  for (int j = 0; j < H; ++j) {
+    const T keep = up ? g[j + H] : g[j];
+    const T send = up ? g[j] : g[j + H];
+    g[j] = merge(keep, shfl_xor(send, b));
+  }
+}
+
+// Reduce 16 columns over the warp's 32 lanes (vocabulary rows). Afterwards
+// lanes l and l ^ 16 hold column brev4(l & 15). The tree is the same for
+// every column: pairs (l, l^1), then ^2, ^4, ^8, ^16.
+template <typename T>
+__device__ __forceinline__ T warp_reduce16(T (&g)[16], int lane) {
+  transpose_step<8>(g, lane, 1);
+  transpose_step<4>(g, lane, 2);
+  transpose_step<2>(g, lane, 4);
+  transpose_step<1>(g, lane, 8);
+  return merge(g[0], shfl_xor(g[0], 16));
+}
+
+__device__ __forceinline__ int brev4(int l) {
+  return ((l & 1) << 3) | ((l & 2) << 1) | ((l & 4) >> 1) | ((l & 8) >> 3);
+}
+
+// Barrier over the 128 epilogue threads that also ORs a predicate, so every
+// thread takes the same branch afterwards.
+__device__ __forceinline__ bool epi_bar_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r) : "r"(static_cast<uint32_t>(pred)) : "memory");
+  return r != 0;
+}
+
+// ----------------------------------------------------------- shared layout
+struct SmemLayout {
+  uint32_t a_bytes, b_bytes, stage_bytes, ctrl_off, red_off, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int N, int stages) {
+  SmemLayout L;
+  L.a_bytes = kBM * kRowBytes;
+  L.b_bytes = static_cast<uint32_t>(N) * kRowBytes;
+  L.stage_bytes = L.a_bytes + L.b_bytes;
+  L.ctrl_off = static_cast<uint32_t>(stages) * L.stage_bytes;
+  // barriers: full[S], empty[S], slot_full[2], slot_empty[2], never, drain;
+  // then the TMEM address holder and the abort flag
+  L.red_off = L.ctrl_off + (2u * stages + 6u) * 8u + 16u;
+  // per-quadrant column results: 3 words x 4 quadrants x N columns
+  L.total = L.red_off + 3u * 4u * static_cast<uint32_t>(N) * 4u;
+  return L;
+}
+
+// ----------------------------------------------------------------- kernel 1
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
+                 const __grid_constant__ CUtensorMap tmH, const HeadParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = p.stages;
+  const int N = p.N;
+  const SmemLayout L = smem_layout(N, S);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.ctrl_off);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+  const uint32_t never_bar = bar0 + 8u * (2 * S + 4);
+  const uint32_t drain_bar = bar0 + 8u * (2 * S + 5);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.ctrl_off + (2 * S + 6) * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  float* red_m = reinterpret_cast<float*>(smem + L.red_off);
+  int32_t* red_i = reinterpret_cast<int32_t*>(red_m + 4 * N);
+  float* red_s = reinterpret_cast<float*>(red_i + 4 * N);
+  const uint32_t smem_base = smem_u32(smem);
+  auto sA = [&](int s) { return smem_base + static_cast<uint32_t>(s) * L.stage_bytes; };
+  auto sB = [&](int s) { return sA(s) + L.a_bytes; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), 4);
+    }
+    mbar_init(never_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmH);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int n_units = p.n_vt * p.n_nt;
+  const int kElems = kRowBytes / 2;     // 16-bit elements per 128-byte row
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_h = policy_evict_last();
+      uint32_t stage = 0, phase = 0, outstanding = 0, out_par = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const int vt = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
+        for (int kb = 0; kb < p.nk; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          outstanding &= ~(1u << stage);
+          mbar_arrive_expect_tx(full_bar(stage), L.stage_bytes);
+          tma_load_2d(sA(stage), &tmW, kb * kElems, vt * kBM, full_bar(stage), pol_w);
+          tma_load_2d(sB(stage), &tmH, kb * kElems, nt * N, full_bar(stage), pol_h);
+          outstanding |= 1u << stage;
+          out_par = (out_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(p.err, ERR_TIMEOUT);
+        // let this thread's loads still in flight land before the CTA exits
+        const int zero = 0;
+        for (int s = 0; s < S; ++s)
+          if ((outstanding >> s) & 1u)
+            mbar_wait(full_bar(s), (out_par >> s) & 1u, &zero, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      if (p.stall) ok = mbar_wait(never_bar, 0, abort_flag, p.timeout_ns);
+      uint32_t cc = 0;   // chunks issued so far (slot = cc & 1)
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        for (int c = 0; c < p.n_chunks && ok; ++c, ++cc) {
+          const uint32_t slot = cc & 1u, sph = (cc >> 1) & 1u;
+          if (!mbar_wait(acce_bar(slot), sph ^ 1u, abort_flag, p.timeout_ns)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + slot * static_cast<uint32_t>(N);
+          const int kb0 = c * kBlocksPerChunk;
+          const int kb1 = min(kb0 + kBlocksPerChunk, p.nk);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(full_bar(stage), phase, abort_flag, p.timeout_ns)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t da = sdesc_sw128(sA(stage));
+            const uint64_t db = sdesc_sw128(sB(stage));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)   // K = 16 per MMA: 32 bytes = 2 descriptor units
+              mma_f16(d_tmem, da + 2u * k, db + 2u * k, p.idesc, (kb != kb0) || (k != 0));
+            mma_commit(empty_bar(stage));
+            if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+          }
+          if (!ok) break;
+          mma_commit(accf_bar(slot));
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(p.err, ERR_TIMEOUT);
+      }
+      // every MMA this thread issued has finished before TMEM is released
+      mma_commit(drain_bar);
+      const int zero = 0;
+      mbar_wait(drain_bar, 0, &zero, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int q = warp & 3;                    // TMEM lane quadrant of this warp
+    const int et = threadIdx.x - 64;           // 0..127
+    const int row = q * 32 + lane;             // vocabulary row within the tile
+    const int nblk = N / 16;                   // 16-column blocks in this unit
+    const uint32_t tlane = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t cc = 0;
+    bool failed = false;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      const int vt = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
+      float acc[kMaxN / 16][16];
+      for (int c = 0; c < p.n_chunks; ++c, ++cc) {
+        const uint32_t slot = cc & 1u, sph = (cc >> 1) & 1u;
+        if (!failed && !mbar_wait(accf_bar(slot), sph, abort_flag, p.timeout_ns)) {
+          failed = true;
+          *abort_flag = 1;
+        }
+        if (failed) continue;
+        tc_fence_after();
+        const uint32_t sbase = tmem_base + tlane + slot * static_cast<uint32_t>(N);
+#pragma unroll
+        for (int bb = 0; bb < kMaxN / 16; ++bb) {
+          if (bb < nblk) {
+            uint32_t r[16];
+            tmem_ld16(sbase + bb * 16, r);
+            tmem_wait_ld();
+            if (c == 0) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) acc[bb][i] = __uint_as_float(r[i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) acc[bb][i] = __fadd_rn(acc[bb][i], __uint_as_float(r[i]));
+            }
+          }
+        }
+        tc_fence_before();   // slot fully read: hand it back to the MMA warp
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce_bar(slot));
+      }
+      if (epi_bar_or(failed || *abort_flag)) {
+        if (et == 0) { *abort_flag = 1; atomicOr(p.err, ERR_TIMEOUT); }
+        break;
+      }
+      const int v = vt * kBM + row;
+      const bool vok = v < p.V;
+      const int n0 = nt * N;
+#pragma unroll
+      for (int bb = 0; bb < kMaxN / 16; ++bb) {
+        if (bb >= nblk) continue;
+        const int c0 = bb * 16;
+        if (p.logits != nullptr && vok) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int n = n0 + c0 + i;
+            if (n < p.B) p.logits[static_cast<size_t>(n) * p.V + v] = acc[bb][i];
+          }
+        }
+        const int cw = c0 + brev4(lane & 15);   // column this lane ends up holding
+        if constexpr (MODE == MODE_GREEDY) {
+          Top2 g[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            g[i] = vok ? Top2{acc[bb][i], v, -INFINITY} : Top2{-INFINITY, INT32_MAX, -INFINITY};
+          const Top2 t = warp_reduce16(g, lane);
+          if (lane < 16) {
+            red_m[q * N + cw] = t.m;
+            red_i[q * N + cw] = t.i;
+            red_s[q * N + cw] = t.s;
+          }
+        } else {
+          if (vok) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int n = n0 + c0 + i;
+              if (n < p.B && p.targets[n] == v) p.zt[n] = acc[bb][i];
+            }
+          }
+          Lse g[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) g[i] = vok ? Lse{acc[bb][i], 1.0f} : Lse{-INFINITY, 0.0f};
+          const Lse t = warp_reduce16(g, lane);
+          if (lane < 16) {
+            red_m[q * N + cw] = t.m;
+            red_s[q * N + cw] = t.S;
+          }
+        }
+      }
+      named_bar_sync(1, kEpiThreads);
+      // fixed combination of the four 32-row quadrants: (q0 . q1) . (q2 . q3)
+      for (int c = et; c < N; c += kEpiThreads) {
+        const int n = n0 + c;
+        if (n >= p.B) continue;
+        const size_t o = static_cast<size_t>(vt) * p.B + n;
+        if constexpr (MODE == MODE_GREEDY) {
+          Top2 t[4];
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq)
+            t[qq] = Top2{red_m[qq * N + c], red_i[qq * N + c], red_s[qq * N + c]};
+          const Top2 r = top2_merge(top2_merge(t[0], t[1]), top2_merge(t[2], t[3]));
+          p.rec_m[o] = r.m;
+          p.rec_i[o] = r.i;
+          p.rec_s[o] = r.s;
+        } else {
+          Lse t[4];
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) t[qq] = Lse{red_m[qq * N + c], red_s[qq * N + c]};
+          const Lse r = lse_merge(lse_merge(t[0], t[1]), lse_merge(t[2], t[3]));
+          p.rec_m[o] = r.m;
+          p.rec_s[o] = r.S;
+        }
+      }
+      named_bar_sync(1, kEpiThreads);
+    }
+    if (failed && et == 0) atomicOr(p.err, ERR_TIMEOUT);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  grid_dep_launch();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+// ----------------------------------------------------------------- kernel 2
+// gap in bf16 ulps of the winner: (m - s) * 2^(7 - E), E = floor(log2|m|)
+// clamped at -126, evaluated in double (exact difference of two floats,
+// exact power-of-two scaling) and rounded once to float.
+__device__ __forceinline__ float gap_ulp_bf16(float m, float s) {
+  const uint32_t eb = (__float_as_uint(m) >> 23) & 0xFFu;
+  const int E = static_cast<int>(eb > 1u ? eb : 1u) - 127;
+  const double scale = __longlong_as_double(static_cast<long long>(1023 + 7 - E) << 52);
+  return static_cast<float>((static_cast<double>(m) - static_cast<double>(s)) * scale);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
+  grid_dep_wait();   // records of kernel 1 are complete and visible
+  const int lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (n >= p.B) return;
+  if constexpr (MODE == MODE_GREEDY) {
+    Top2 acc{-INFINITY, INT32_MAX, -INFINITY};
+    for (int t = lane; t < p.n_vt; t += 32) {
+      const size_t o = static_cast<size_t>(t) * p.B + n;
+      acc = top2_merge(acc, Top2{p.rec_m[o], p.rec_i[o], p.rec_s[o]});
+    }
+#pragma unroll
+    for (int b = 1; b < 32; b <<= 1) acc = top2_merge(acc, shfl_xor(acc, b));
+    if (lane == 0) {
+      p.token[n] = acc.i;
+      p.gap[n] = gap_ulp_bf16(acc.m, acc.s);
+    }
+  } else {
+    Lse acc{-INFINITY, 0.0f};
+    for (int t = lane; t < p.n_vt; t += 32) {
+      const size_t o = static_cast<size_t>(t) * p.B + n;
+      acc = lse_merge(acc, Lse{p.rec_m[o], p.rec_s[o]});
+    }
+#pragma unroll
+    for (int b = 1; b < 32; b <<= 1) acc = lse_merge(acc, shfl_xor(acc, b));
+    if (lane == 0) {
+      const int tg = p.targets[n];
+      if (tg < 0 || tg >= p.V) {
+        p.logp[n] = __int_as_float(0x7fc00000);
+        atomicOr(p.err, ERR_TARGET);
+      } else {
+        p.logp[n] = p.zt[n] - (acc.m + logf(acc.S));
+      }
+    }
+  }
+}
+
+}  // namespace detlm

@@ -1,0 +1,408 @@
+// int8_kernels.cuh -- the exact integer head (int8 x int8 -> int32) on sm_103a.
+//
+// "Eliminating Nondeterminism in LLM Inference with Integer-Only Arithmetic",
+// section "DetLLM": the only hardware-dispatched operation is the int8 x int8
+// -> int32 matmul, and argmax breaks ties toward the lowest token id; section
+// "What if we don't use floats at all?": integer sums are exact in any order
+// while they cannot overflow, and the overflow can be bounded in advance.
+//
+// sm_103a has no tcgen05 integer MMA (kind::i8 does not assemble for this
+// target), so the integer product runs on the kind::f16 tensor-core path with
+// exact arithmetic:
+//   * every int8 value is converted to IEEE fp16, where -128..127 are exact;
+//   * each product of two such values is an integer of magnitude <= 2^14,
+//     exact in the fp32 accumulator;
+//   * the K axis is cut into chunks of 1024 elements, each accumulated in its
+//     own TMEM accumulator, so every partial sum is an integer of magnitude
+//     <= 1024 * 2^14 = 2^24 and exact in fp32 (footnote 3 of the same page:
+//     2^24 is where fp32 runs out of integer precision);
+//   * the chunk sums are converted to int32 and added in int32; with
+//     d <= 16384 every logit is bounded by 16384 * 2^14 = 2^28 < 2^31.
+//
+// The conversion int8 -> fp16 is exact bit arithmetic: flipping the sign bit
+// gives u = x + 128 in 0..255; the half with bits 0x6400 | u is 1024 + u;
+// subtracting 1152 (exact) leaves x.
+//
+// Warp roles (320 threads): warp 0 TMA of int8 tiles, warp 1 MMA issuer,
+// warps 2..5 epilogue, warps 6..9 converters (int8 ring -> fp16 ring in the
+// 128-byte swizzle layout the MMA descriptors expect).
+#pragma once
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+#include "ptx.cuh"
+#include "head_kernels.cuh"
+
+namespace detlm {
+
+constexpr int kI8Chunk = 1024;            // K elements per exact fp32 chunk
+constexpr int kI8Threads = 320;
+constexpr int kI8MaxD = 16384;            // 16 chunks; keeps |logit| <= 2^28
+constexpr int kI8MaxStages8 = 8;
+constexpr int kI8MaxN = 64;               // keeps >= 5 int8 stages in shared memory
+
+__host__ __device__ inline int int8_chunks(int64_t d) {
+  return static_cast<int>((d + kI8Chunk - 1) / kI8Chunk);
+}
+
+// Hidden rows per MMA for the integer head: two TMEM buffers of n_chunks
+// accumulators each must fit 512 columns, and the int8 and fp16 rings must
+// fit shared memory.
+__host__ __device__ inline int int8_cols_for(int64_t B, int64_t d) {
+  const int nc = int8_chunks(d);
+  int cap = (256 / nc) / 16 * 16;
+  if (cap < 16) cap = 16;
+  if (cap > kI8MaxN) cap = kI8MaxN;
+  int n = static_cast<int>((B + 15) / 16) * 16;
+  if (n < 16) n = 16;
+  return n < cap ? n : cap;
+}
+
+struct Int8Params {
+  int32_t V, d, B;
+  int32_t N, n_vt, n_nt, nk, n_chunks;
+  int32_t s8, s16;           // int8 ring and fp16 ring depths
+  uint32_t tmem_cols;
+  uint32_t idesc;
+  int32_t* logits;           // optional int32 [B, V]
+  int32_t* rec_m;            // [n_vt, B]
+  int32_t* rec_i;
+  int32_t* rec_s;
+  int* err;
+  int32_t stall;
+  uint64_t timeout_ns;
+};
+
+struct Int8Layout {
+  uint32_t a8, b8, st8, a16, b16, st16, off16, ctrl, red, total;
+};
+
+__host__ __device__ inline Int8Layout int8_layout(int N, int s8, int s16) {
+  Int8Layout L;
+  L.a8 = kBM * kRowBytes;                       // int8 W tile: 128 rows x 128 B
+  L.b8 = static_cast<uint32_t>(N) * kRowBytes;  // int8 h tile
+  L.st8 = L.a8 + L.b8;
+  L.a16 = 2u * kBM * kRowBytes;                 // fp16 W: two 64-element sub-tiles
+  L.b16 = 2u * static_cast<uint32_t>(N) * kRowBytes;
+  L.st16 = L.a16 + L.b16;
+  L.off16 = static_cast<uint32_t>(s8) * L.st8;
+  L.ctrl = L.off16 + static_cast<uint32_t>(s16) * L.st16;
+  // f8full[s8], f8empty[s8], f16full[s16], f16empty[s16], accf[2], acce[2],
+  // never, drain; then TMEM holder and abort flag
+  L.red = L.ctrl + (2u * s8 + 2u * s16 + 6u) * 8u + 16u;
+  L.total = L.red + 3u * 4u * static_cast<uint32_t>(N) * 4u;
+  return L;
+}
+
+struct ITop2 { int32_t m; int32_t i; int32_t s; };
+
+__device__ __forceinline__ ITop2 itop2_merge(const ITop2& a, const ITop2& b) {
+  const bool aw = (a.m > b.m) || (a.m == b.m && a.i < b.i);
+  ITop2 r;
+  r.m = aw ? a.m : b.m;
+  r.i = aw ? a.i : b.i;
+  r.s = max(aw ? a.s : b.s, aw ? b.m : a.m);
+  return r;
+}
+__device__ __forceinline__ ITop2 shfl_xor(const ITop2& x, int b) {
+  return ITop2{__shfl_xor_sync(0xffffffffu, x.m, b), __shfl_xor_sync(0xffffffffu, x.i, b),
+               __shfl_xor_sync(0xffffffffu, x.s, b)};
+}
+__device__ __forceinline__ ITop2 merge(const ITop2& a, const ITop2& b) { return itop2_merge(a, b); }
+
+// four int8 in one word -> two half2 holding the same integers exactly
+__device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;             // bytes x + 128
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+  const __half2 k = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+  const __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), k);
+  const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), k);
+  lo = *reinterpret_cast<const uint32_t*>(&ha);
+  hi = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
+// Convert `rows` rows of a swizzled int8 tile (128 B per row) into the two
+// swizzled fp16 sub-tiles (each 128 B per row) at dst (sub-tile 1 at
+// dst + rows * 128). Threads ct = 0..nthreads-1 share the 16-byte chunks.
+__device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int rows,
+                                             int ct, int nthreads) {
+  const int chunks = rows * 8;
+  for (int q = ct; q < chunks; q += nthreads) {
+    const int r = q >> 3, c = q & 7;                       // row, logical 16-byte chunk
+    const uint4 w = *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ (r & 7)) << 4));
+    uint4 o0, o1;
+    i8x4_to_h2x2(w.x, o0.x, o0.y);
+    i8x4_to_h2x2(w.y, o0.z, o0.w);
+    i8x4_to_h2x2(w.z, o1.x, o1.y);
+    i8x4_to_h2x2(w.w, o1.z, o1.w);
+    // int8 elements 16c .. 16c+15 -> fp16 sub-tile c/4, chunks 2(c%4), 2(c%4)+1
+    uint8_t* sub = dst + (c >> 2) * rows * 128 + r * 128;
+    const int cc = (c & 3) * 2;
+    *reinterpret_cast<uint4*>(sub + ((cc ^ (r & 7)) << 4)) = o0;
+    *reinterpret_cast<uint4*>(sub + (((cc + 1) ^ (r & 7)) << 4)) = o1;
+  }
+}
+
+__global__ void __launch_bounds__(kI8Threads, 1)
+int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
+                 const Int8Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S8 = p.s8, S16 = p.s16, N = p.N;
+  const Int8Layout L = int8_layout(N, S8, S16);
+
+  const uint32_t bar0 = smem_u32(smem + L.ctrl);
+  auto f8full = [&](int s) { return bar0 + 8u * s; };
+  auto f8empty = [&](int s) { return bar0 + 8u * (S8 + s); };
+  auto f16full = [&](int s) { return bar0 + 8u * (2 * S8 + s); };
+  auto f16empty = [&](int s) { return bar0 + 8u * (2 * S8 + S16 + s); };
+  auto accf = [&](int b) { return bar0 + 8u * (2 * S8 + 2 * S16 + b); };
+  auto acce = [&](int b) { return bar0 + 8u * (2 * S8 + 2 * S16 + 2 + b); };
+  const uint32_t never_bar = bar0 + 8u * (2 * S8 + 2 * S16 + 4);
+  const uint32_t drain_bar = bar0 + 8u * (2 * S8 + 2 * S16 + 5);
+  uint32_t* tmem_holder =
+      reinterpret_cast<uint32_t*>(smem + L.ctrl + (2 * S8 + 2 * S16 + 6) * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int32_t* red_m = reinterpret_cast<int32_t*>(smem + L.red);
+  int32_t* red_i = red_m + 4 * N;
+  int32_t* red_s = red_i + 4 * N;
+  const uint32_t base = smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S8; ++s) { mbar_init(f8full(s), 1); mbar_init(f8empty(s), 4); }
+    for (int s = 0; s < S16; ++s) { mbar_init(f16full(s), 4); mbar_init(f16empty(s), 1); }
+    for (int b = 0; b < 2; ++b) { mbar_init(accf(b), 1); mbar_init(acce(b), 4); }
+    mbar_init(never_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmH);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int n_units = p.n_vt * p.n_nt;
+  const int kb_per_chunk = kI8Chunk / kRowBytes;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_h = policy_evict_last();
+      uint32_t stage = 0, phase = 0, outstanding = 0, out_par = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const int vt = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
+        for (int kb = 0; kb < p.nk; ++kb) {
+          if (!mbar_wait(f8empty(stage), phase ^ 1u, abort_flag, p.timeout_ns)) { ok = false; break; }
+          outstanding &= ~(1u << stage);
+          mbar_arrive_expect_tx(f8full(stage), L.st8);
+          const uint32_t a = base + stage * L.st8;
+          tma_load_2d(a, &tmW, kb * kRowBytes, vt * kBM, f8full(stage), pol_w);
+          tma_load_2d(a + L.a8, &tmH, kb * kRowBytes, nt * N, f8full(stage), pol_h);
+          outstanding |= 1u << stage;
+          out_par = (out_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == static_cast<uint32_t>(S8)) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(p.err, ERR_TIMEOUT);
+        const int zero = 0;
+        for (int s = 0; s < S8; ++s)
+          if ((outstanding >> s) & 1u) mbar_wait(f8full(s), (out_par >> s) & 1u, &zero, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      if (p.stall) ok = mbar_wait(never_bar, 0, abort_flag, p.timeout_ns);
+      int j = 0;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++j) {
+        const uint32_t buf = j & 1, aph = (j >> 1) & 1;
+        if (!mbar_wait(acce(buf), aph ^ 1u, abort_flag, p.timeout_ns)) { ok = false; break; }
+        tc_fence_after();
+        for (int kb = 0; kb < p.nk; ++kb) {
+          if (!mbar_wait(f16full(stage), phase, abort_flag, p.timeout_ns)) { ok = false; break; }
+          tc_fence_after();
+          const int ch = kb / kb_per_chunk;
+          const uint32_t d_tmem =
+              tmem_base + (buf * static_cast<uint32_t>(p.n_chunks) + ch) * static_cast<uint32_t>(N);
+          const uint32_t a16 = base + L.off16 + stage * L.st16;
+          const uint32_t b16 = a16 + L.a16;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const uint64_t da = sdesc_sw128(a16 + t * (kBM * kRowBytes));
+            const uint64_t db = sdesc_sw128(b16 + t * (N * kRowBytes));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_f16(d_tmem, da + 2u * k, db + 2u * k, p.idesc,
+                      ((kb % kb_per_chunk) | t | k) != 0);
+          }
+          mma_commit(f16empty(stage));
+          if (++stage == static_cast<uint32_t>(S16)) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(accf(buf));
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(p.err, ERR_TIMEOUT);
+      }
+      mma_commit(drain_bar);
+      const int zero = 0;
+      mbar_wait(drain_bar, 0, &zero, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp >= 6) {
+    // ------------------------------------------------------- converters
+    const int ct = threadIdx.x - 192;   // 0..127
+    uint32_t s8 = 0, ph8 = 0, s16 = 0, ph16 = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int kb = 0; kb < p.nk; ++kb) {
+        const bool g1 = mbar_wait(f8full(s8), ph8, abort_flag, p.timeout_ns);
+        const bool g2 = g1 && mbar_wait(f16empty(s16), ph16 ^ 1u, abort_flag, p.timeout_ns);
+        if (!g2) { ok = false; break; }
+        const uint8_t* src = smem + s8 * L.st8;
+        uint8_t* dst = smem + L.off16 + s16 * L.st16;
+        convert_tile(src, dst, kBM, ct, 128);
+        convert_tile(src + L.a8, dst + L.a16, N, ct, 128);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(f8empty(s8));
+          mbar_arrive(f16full(s16));
+        }
+        if (++s8 == static_cast<uint32_t>(S8)) { s8 = 0; ph8 ^= 1u; }
+        if (++s16 == static_cast<uint32_t>(S16)) { s16 = 0; ph16 ^= 1u; }
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      atomicOr(p.err, ERR_TIMEOUT);
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int et = threadIdx.x - 64;
+    const int row = q * 32 + lane;
+    int j = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++j) {
+      const int vt = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
+      const uint32_t buf = j & 1, aph = (j >> 1) & 1;
+      const bool got = mbar_wait(accf(buf), aph, abort_flag, p.timeout_ns);
+      if (epi_bar_or(!got || *abort_flag)) {
+        if (et == 0) { *abort_flag = 1; atomicOr(p.err, ERR_TIMEOUT); }
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tlane = static_cast<uint32_t>(q * 32) << 16;
+      const int v = vt * kBM + row;
+      const bool vok = v < p.V;
+      const int n0 = nt * N;
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        int32_t x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = 0;
+        for (int ch = 0; ch < p.n_chunks; ++ch) {
+          uint32_t r[16];
+          tmem_ld16(tmem_base + tlane +
+                        (buf * static_cast<uint32_t>(p.n_chunks) + ch) * static_cast<uint32_t>(N) + c0,
+                    r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[i] += __float2int_rn(__uint_as_float(r[i]));
+        }
+        if (c0 + 16 >= N) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acce(buf));
+        }
+        if (p.logits != nullptr && vok) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int n = n0 + c0 + i;
+            if (n < p.B) p.logits[static_cast<size_t>(n) * p.V + v] = x[i];
+          }
+        }
+        ITop2 g[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          g[i] = vok ? ITop2{x[i], v, INT32_MIN} : ITop2{INT32_MIN, INT32_MAX, INT32_MIN};
+        const ITop2 t = warp_reduce16(g, lane);
+        const int cw = c0 + brev4(lane & 15);
+        if (lane < 16) {
+          red_m[q * N + cw] = t.m;
+          red_i[q * N + cw] = t.i;
+          red_s[q * N + cw] = t.s;
+        }
+      }
+      named_bar_sync(1, kEpiThreads);
+      for (int c = et; c < N; c += kEpiThreads) {
+        const int n = n0 + c;
+        if (n >= p.B) continue;
+        ITop2 t[4];
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) t[qq] = ITop2{red_m[qq * N + c], red_i[qq * N + c], red_s[qq * N + c]};
+        const ITop2 r = itop2_merge(itop2_merge(t[0], t[1]), itop2_merge(t[2], t[3]));
+        const size_t o = static_cast<size_t>(vt) * p.B + n;
+        p.rec_m[o] = r.m;
+        p.rec_i[o] = r.i;
+        p.rec_s[o] = r.s;
+      }
+      named_bar_sync(1, kEpiThreads);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  grid_dep_launch();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+struct Int8MergeParams {
+  int32_t B, n_vt;
+  const int32_t* rec_m;
+  const int32_t* rec_i;
+  const int32_t* rec_s;
+  int32_t* token;
+  int32_t* gap;
+};
+
+__global__ void __launch_bounds__(128) int8_merge_kernel(const Int8MergeParams p) {
+  grid_dep_wait();
+  const int lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (n >= p.B) return;
+  ITop2 acc{INT32_MIN, INT32_MAX, INT32_MIN};
+  for (int t = lane; t < p.n_vt; t += 32) {
+    const size_t o = static_cast<size_t>(t) * p.B + n;
+    acc = itop2_merge(acc, ITop2{p.rec_m[o], p.rec_i[o], p.rec_s[o]});
+  }
+#pragma unroll
+  for (int b = 1; b < 32; b <<= 1) acc = itop2_merge(acc, shfl_xor(acc, b));
+  if (lane == 0) {
+    p.token[n] = acc.i;
+    p.gap[n] = acc.s == INT32_MIN ? INT32_MAX : acc.m - acc.s;
+  }
+}
+
+}  // namespace detlm

@@ -216,7 +216,7 @@ def small_float(seed: int, V: int, d: int, B: int, fmt: str = "bf16",
     conv = bf16_bits_from_f32 if fmt == "bf16" else f16_bits_from_f32
     W = conv(Wf)
     h = conv(hf)
-    for k in range(min(n_ties, B)):
+    for k in range(min(n_ties, B) if V >= 2 else 0):
         a, b = (int(x) for x in rng.choice(V, size=2, replace=False))
         W[b] = W[a]
         wa = (W[a].astype(np.uint32) << 16).view(np.float32) if fmt == "bf16" \
@@ -232,7 +232,7 @@ def small_int8(seed: int, V: int, d: int, B: int, n_ties: int = 0,
     rng = _rng(seed)
     W = rng.integers(lo, hi + 1, size=(V, d), dtype=np.int8)
     h = rng.integers(lo, hi + 1, size=(B, d), dtype=np.int8)
-    for k in range(min(n_ties, B)):
+    for k in range(min(n_ties, B) if V >= 2 else 0):
         a, b = (int(x) for x in rng.choice(V, size=2, replace=False))
         W[b] = W[a]
         h[k] = W[a]

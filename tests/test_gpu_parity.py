@@ -1,0 +1,101 @@
+"""GPU parity against the oracle at sizes the oracle finishes in seconds:
+several vocabulary tiles with a ragged tail, several K blocks with a ragged
+tail, one and several column tiles, all three dtypes."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.gpu_helpers import (check_float_greedy, dev, host, logprob_tol,
+                               oracle_float_rows)
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [  # (V, d): tiles of 128 vocabulary rows, K blocks of 128 bytes
+    (1000, 520),   # 7 full tiles + 104-row tail; 8 K blocks of bf16 + 8-element tail
+    (16, 64),      # one partial tile, one K block
+    (129, 8),      # one full tile + 1 row; K shorter than a block
+    (1, 32),       # a single vocabulary entry
+]
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import invariant_output_head_gb300 as ioh
+    ioh.load_library()
+    return torch
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "fp16"])
+@pytest.mark.parametrize("V,d", SHAPES)
+@pytest.mark.parametrize("B", [1, 5, 17, 64, 300])
+def test_float_greedy_parity(torch_cuda, fmt, V, d, B):
+    from invariant_output_head_gb300 import Head
+    case = synth.small_float(100 + V + d + B, V, d, B, fmt=fmt, n_ties=min(2, B))
+    Wt = dev(case["W"], fmt)
+    head = Head(Wt, fmt)
+    tok, gap, z = head.greedy(dev(case["h"], fmt), with_logits=True)
+    torch_cuda.cuda.synchronize()
+    assert head.check() == 0
+    z_ref, A = oracle_float_rows(case["W"], case["h"], fmt)
+    check_float_greedy(z_ref, A, host(tok), host(gap), host(z), label=f"{fmt} {V}x{d} B={B}")
+    # the same call without the logits store gives the same decision bits
+    tok2, gap2, _ = head.greedy(dev(case["h"], fmt), with_logits=False)
+    assert (host(tok2) == host(tok)).all()
+    assert (host(gap2).view(np.uint32) == host(gap).view(np.uint32)).all()
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "fp16"])
+@pytest.mark.parametrize("V,d", SHAPES[:3])
+@pytest.mark.parametrize("B", [1, 17, 300])
+def test_float_logprob_parity(torch_cuda, fmt, V, d, B):
+    from invariant_output_head_gb300 import Head
+    case = synth.small_float(200 + V + d + B, V, d, B, fmt=fmt)
+    head = Head(dev(case["W"], fmt), fmt)
+    t = case["targets"]
+    lp = host(head.logprob(dev(case["h"], fmt), dev(t, "int32")))
+    assert head.check() == 0
+    z_ref, A = oracle_float_rows(case["W"], case["h"], fmt)
+    lse = oracle.logsumexp(z_ref)
+    lp_ref = oracle.logprob(z_ref, t)
+    tol = logprob_tol(A, lse, t)
+    err = np.abs(lp.astype(np.float64) - lp_ref)
+    assert (err <= tol).all(), (err.max(), tol[np.argmax(err - tol)])
+    assert (lp <= 0).all()
+
+
+@pytest.mark.parametrize("V,d", [(1000, 1040), (16, 16), (130, 2064), (1, 32)])
+@pytest.mark.parametrize("B", [1, 5, 33, 100])
+def test_int8_greedy_exact(torch_cuda, V, d, B):
+    from invariant_output_head_gb300 import Head
+    case = synth.small_int8(300 + V + d + B, V, d, B, n_ties=min(2, B), lo=-128, hi=127)
+    head = Head(dev(case["W"], "int8"), "int8")
+    tok, gap, z = head.greedy(dev(case["h"], "int8"), with_logits=True)
+    assert head.check() == 0
+    ref = oracle.head_greedy(case["W"], case["h"], "int8")
+    assert (host(z).astype(np.int64) == ref["logits"]).all()
+    assert (host(tok) == ref["token"]).all()
+    assert (host(gap).astype(np.int64) == np.minimum(ref["gap"], 2**31 - 1)).all()
+
+
+def test_int8_extreme_values_exact(torch_cuda):
+    """Partial sums at the edge of fp32's exact-integer range: 1024 products
+    of (-128)(-128) = 2^24 per K chunk, mixed with +-1 products."""
+    from invariant_output_head_gb300 import Head
+    V, d = 256, 4096
+    W = np.full((V, d), -128, np.int8)
+    W[1::2] = 127
+    W[5, ::3] = 1
+    W[7, 1024:2048] = -1
+    h = np.full((4, d), -128, np.int8)
+    h[1] = 127
+    h[2, ::2] = 1
+    h[3] = np.where(np.arange(d) % 1024 == 1023, 1, -128).astype(np.int8)
+    head = Head(dev(W, "int8"), "int8")
+    tok, gap, z = head.greedy(dev(h, "int8"), with_logits=True)
+    ref = oracle.head_greedy(W, h, "int8")
+    assert (host(z).astype(np.int64) == ref["logits"]).all()
+    assert (host(tok) == ref["token"]).all()
