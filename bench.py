@@ -1,0 +1,528 @@
+"""Benchmark of the batch-invariant output head on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload pr1|sweep|spec|logprob|int8]
+                    [--impl ours|reference]
+
+Prints ONE JSON line. A step is one pass of the whole hot path over one batch
+of synthetic input:
+
+* pr1 (default): the greedy-decode workload -- 16 independent hidden rows,
+  each a B=1 call on the bf16 head d=2048, V=32000 (TinyLlama-1.1B shape),
+  returning fp32 logits, the token and the top-2 gap;
+* sweep: the same head with 8 planted near-tie rows, 64 rows evaluated at
+  B = 1, 2, 3, 8, 17, 64;
+* spec: speculative-verify block, bf16 d=3584, V=152064, B=256, with logits;
+* logprob: trainer scoring, bf16 d=1536, V=151936, 8192 rows, target logp;
+* int8: the integer head d=4096, V=128256 at --batch rows (default 512).
+
+value = rows/s for the whole job (all ranks); inputs resident in HBM. Several
+copies of W rotate so that every call streams W from HBM (their total is
+larger than L2). The projection kernel of every call is bracketed by CUDA
+events on the call's stream for the roofline figure. `e2e` is the same metric
+through the host-buffer entry point (pinned host memory, copies inside the
+timed region). `cpu_baseline` times the CPU oracle on a bounded sample.
+Under torchrun each rank runs the same per-GPU workload (weak scaling, no
+collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("lm-head rows/s & HBM GB/s (B=1) or TFLOP/s (B≥256) vs roofline, "
+          "bit-stable")
+
+WORKLOADS = {
+    "pr1": dict(desc="PR1 greedy decode: bf16 head d=2048 V=32000, 16 independent B=1 "
+                     "rows, fp32 logits + token + top-2 gap",
+                fmt="bf16", V=32000, d=2048, mode="greedy", bound="hbm"),
+    "sweep": dict(desc="batch-invariance sweep: bf16 head d=2048 V=32000, 64 rows (8 planted "
+                       "near ties) at B in {1,2,3,8,17,64}, logits + token + gap",
+                  fmt="bf16", V=32000, d=2048, mode="greedy", bound="hbm"),
+    "spec": dict(desc="speculative verify: bf16 head d=3584 V=152064, B=256 (16x16), "
+                      "logits + token + gap", fmt="bf16", V=152064, d=3584, B=256,
+                 mode="greedy", bound="tensor"),
+    "logprob": dict(desc="trainer log-prob scoring: bf16 head d=1536 V=151936, 8x1024 rows, "
+                         "target logp", fmt="bf16", V=151936, d=1536, B=8192,
+                    mode="logprob", bound="tensor"),
+    "int8": dict(desc="integer-only head: int8 d=4096 V=128256, exact int32 logits + token",
+                 fmt="int8", V=128256, d=4096, mode="greedy", bound="hbm"),
+}
+
+
+# ------------------------------------------------------------------ helpers
+
+def env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained",
+                                                     d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    src = os.path.join(ROOT, "invariant_output_head_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(src)):
+        with open(os.path.join(src, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the projection kernel from a committed ncu
+    summary (profiles/<kernel>_<workload>.md), only while the kernel sources
+    still hash to the value recorded with the capture."""
+    path = os.path.join(ROOT, "profiles", f"head_gemm_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- ") and ":" in line:
+                k, v = line[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                n += 1
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ------------------------------------------------------------- workloads
+
+def make_inputs(name: str, batch: int):
+    import synth
+    if name == "pr1":
+        c = synth.pr1()
+        c["calls"] = [(r, 1) for r in range(c["h"].shape[0])]
+    elif name == "sweep":
+        c = synth.sweep()
+        calls = []
+        for B in (1, 2, 3, 8, 17, 64):
+            for r0 in range(0, 64, B):
+                calls.append((r0, min(B, 64 - r0)))
+        c["calls"] = calls
+    elif name == "spec":
+        c = synth.spec_verify()
+        c["calls"] = [(0, 256)]
+    elif name == "logprob":
+        c = synth.logprob()
+        c["calls"] = [(0, c["h"].shape[0])]
+    elif name == "int8":
+        c = synth.int8_head(B=batch)
+        c["calls"] = [(0, batch)]
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    return c
+
+
+def algorithmic(name, c, B):
+    """Algorithmic bytes and flops of one call with B rows."""
+    V, d = c["V"], c["d"]
+    eb = 1 if c["dtype"] == "int8" else 2
+    by = V * d * eb + B * d * eb
+    if WORKLOADS[name]["mode"] == "greedy":
+        by += B * V * 4 + B * 8          # logits + token + gap
+    else:
+        by += B * 8                      # targets + logp
+    return by, 2.0 * B * V * d
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import invariant_output_head_gb300 as ioh
+    from invariant_output_head_gb300 import binding as bd
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    spec = WORKLOADS[args.workload]
+    c = make_inputs(args.workload, args.batch)
+    fmt, V, d = c["dtype"], c["V"], c["d"]
+    tdt = {"bf16": torch.bfloat16, "fp16": torch.float16, "int8": torch.int8}[fmt]
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a.view(np.int16) if fmt != "int8" else a)
+        return t.to(dev).view(tdt) if fmt != "int8" else t.to(dev)
+
+    W0 = to_dev(c["W"])
+    wbytes = W0.numel() * W0.element_size()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_copies = max(2, int(np.ceil(2 * l2 / wbytes)) + 1)
+    Ws = [W0] + [W0.clone() for _ in range(n_copies - 1)]
+    heads = [ioh.Head(W, fmt) for W in Ws]
+    h_all = to_dev(c["h"])
+    rows = h_all.shape[0]
+    calls = c["calls"]
+    maxB = max(B for _, B in calls)
+    for hd in heads:
+        bd.detlm_head_reserve(hd.handle, maxB)
+    greedy = spec["mode"] == "greedy"
+    gdt = torch.int32 if fmt == "int8" else torch.float32
+    outs = []
+    for r0, B in calls:
+        if greedy:
+            outs.append((torch.empty(B, dtype=torch.int32, device=dev),
+                         torch.empty(B, dtype=gdt, device=dev),
+                         torch.empty((B, V), dtype=gdt, device=dev)))
+        else:
+            outs.append(torch.empty(B, dtype=torch.float32, device=dev))
+    targets = torch.from_numpy(c["targets"]).to(dev) if not greedy else None
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    n_calls = len(calls)
+    k = [0]
+
+    def step(ev=None):
+        for j, (r0, B) in enumerate(calls):
+            hd = heads[k[0] % n_copies]
+            k[0] += 1
+            if ev is not None:
+                bd.detlm_head_time_next(hd.handle, ev[j][0].cuda_event, ev[j][1].cuda_event)
+            hv = h_all[r0:r0 + B]
+            if greedy:
+                tok, gap, lg = outs[j]
+                bd.detlm_head_greedy(hd.handle, hv.data_ptr(), B, tok.data_ptr(),
+                                     gap.data_ptr(), lg.data_ptr(), sp)
+            else:
+                bd.detlm_head_logprob(hd.handle, hv.data_ptr(), targets[r0:r0 + B].data_ptr(),
+                                      B, outs[j].data_ptr(), sp)
+
+    def snapshot():
+        if greedy:
+            return [tuple(t.clone() for t in o) for o in outs]
+        return [o.clone() for o in outs]
+
+    # warm-up, and the reference outputs for the bit-stability check
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    first = snapshot()
+    for hd in heads:
+        assert hd.check() == 0, "device error after warm-up"
+
+    # kernel events for the projection kernel of every call in the timed region
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_calls)] for _ in range(args.steps)]
+    for row in ev:          # torch creates an event at its first record
+        for e0, e1 in row:
+            e0.record(stream)
+            e1.record(stream)
+    sampler = ClockSampler(local_rank)
+    if rank == 0:
+        sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(args.steps):
+        step(ev[s])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+    elapsed_ms = t0.elapsed_time(t1)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    for hd in heads:
+        assert hd.check() == 0, "device error in the timed region"
+
+    # bit stability: last step's outputs equal the warm-up outputs bit for bit
+    last = snapshot()
+    stable = all(
+        all(torch.equal(a.view(torch.int32) if a.dtype != torch.int32 else a,
+                        b.view(torch.int32) if b.dtype != torch.int32 else b)
+            for a, b in zip(x, y)) if greedy else torch.equal(x.view(torch.int32),
+                                                                y.view(torch.int32))
+        for x, y in zip(first, last))
+
+    # per-launch duration of the projection kernel, averaged over the timed region
+    kms = np.array([[e0.elapsed_time(e1) for e0, e1 in row] for row in ev])
+    rows_per_step = sum(B for _, B in calls)
+    by, fl = 0.0, 0.0
+    for _, B in calls:
+        b_, f_ = algorithmic(args.workload, c, B)
+        by += b_
+        fl += f_
+    by_launch, fl_launch = by / n_calls, fl / n_calls
+    avg_kernel_s = kms.mean() / 1e3
+    peaks = measured_peaks()
+    if spec["bound"] == "hbm":
+        achieved = by_launch / avg_kernel_s / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved = fl_launch / avg_kernel_s / 1e12
+        peak, unit = peaks["bf16_tflops_sustained"], "TFLOP/s"
+    traffic = profiled_traffic(args.workload)
+
+    value = rows_per_step * args.steps * world / (elapsed_ms / 1e3)
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8" if fmt == "int8" else fmt, "data": "synthetic",
+        "config": {"workload": spec["desc"], "name": args.workload, "V": V, "d": d,
+                   "rows_per_step": rows_per_step, "calls_per_step": n_calls,
+                   "l2": f"{n_copies} rotating copies of W ({n_copies * wbytes / 1e6:.0f} MB) "
+                         f"> 2x L2 ({l2 / 1e6:.0f} MB); inputs larger than L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": spec["bound"], "achieved": round(achieved, 1),
+                     "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "kernel": "head_gemm_kernel",
+                     "kernel_us_per_launch": round(avg_kernel_s * 1e6, 2),
+                     "algorithmic_bytes_per_launch": int(by_launch),
+                     "algorithmic_flops_per_launch": fl_launch,
+                     "peak_source": f"MEASURED_PEAKS.json ({peaks['source']}, "
+                                    f"{'hbm_gbs' if unit == 'GB/s' else 'bf16_tflops_sustained'})"},
+        "bit_stable": bool(stable),
+        "gpu_launches": 2 * n_calls * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        res["e2e"] = run_e2e(args, c, heads, calls, greedy, rows_per_step, dev, stream)
+        res["cpu_baseline"] = cpu_baseline(args.workload, c, budget_s=args.cpu_seconds)
+    return res
+
+
+def run_e2e(args, c, heads, calls, greedy, rows_per_step, dev, stream):
+    """Same metric through the host-buffer entry points: pinned host inputs are
+    copied in and the results copied out on every call."""
+    import torch
+    from invariant_output_head_gb300 import binding as bd
+    fmt, V = c["dtype"], c["V"]
+    h_host = torch.from_numpy(np.ascontiguousarray(
+        c["h"].view(np.int16) if fmt != "int8" else c["h"])).pin_memory()
+    esz = h_host.element_size()
+    d = c["d"]
+    maxB = max(B for _, B in calls)
+    tok = torch.empty(maxB, dtype=torch.int32).pin_memory()
+    gap = torch.empty(maxB, dtype=torch.int32).pin_memory()
+    lg = torch.empty((maxB, V), dtype=torch.int32).pin_memory() if greedy else None
+    lp = torch.empty(maxB, dtype=torch.float32).pin_memory()
+    tg = torch.from_numpy(c["targets"]).pin_memory() if not greedy else None
+    sp = stream.cuda_stream
+    steps = max(3, min(args.steps, int(args.e2e_seconds / 0.002)))
+
+    def one_step(i):
+        for j, (r0, B) in enumerate(calls):
+            hd = heads[(i * len(calls) + j) % len(heads)]
+            hp = h_host.data_ptr() + r0 * d * esz
+            if greedy:
+                bd.detlm_head_greedy_host(hd.handle, hp, B, tok.data_ptr(), gap.data_ptr(),
+                                          lg.data_ptr(), sp)
+            else:
+                bd.detlm_head_logprob_host(hd.handle, hp, tg.data_ptr() + r0 * 4, B,
+                                           lp.data_ptr(), sp)
+    for i in range(3):
+        one_step(i)
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for i in range(steps):
+        one_step(i)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t
+    h2d = sum(B * d * esz + (0 if greedy else 4 * B) for _, B in calls)
+    d2h = sum((8 * B + 4 * B * V) if greedy else 4 * B for _, B in calls)
+    return {"value": round(rows_per_step * steps / dt, 2), "unit": "rows/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "api": "detlm_head_greedy_host" if greedy else "detlm_head_logprob_host"}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_rows_per_s(name, c, budget_s, max_rows=None):
+    """Time the oracle as it stands on rows of the workload, one call at a time
+    (each call decodes W and computes every logit and the decision)."""
+    import oracle
+    fmt = c["dtype"]
+    h = c["h"]
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        r = n % h.shape[0]
+        if WORKLOADS[name]["mode"] == "greedy":
+            oracle.head_greedy(c["W"], h[r:r + 1], fmt)
+        else:
+            oracle.head_logprob(c["W"], h[r:r + 1], c["targets"][r:r + 1], fmt)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or (max_rows is not None and n >= max_rows):
+            return n / dt, n, dt
+
+
+def cpu_baseline(name, c, budget_s):
+    v, n, dt = oracle_rows_per_s(name, c, budget_s)
+    return {"value": round(v, 4), "unit": "rows/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{n} hidden rows of the {name} workload, one oracle call per row "
+                      f"(exact decode of W, float64/int64 logits, decision), {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step one row of the workload."""
+    if rank != 0:
+        return None
+    c = make_inputs(args.workload, args.batch)
+    import oracle
+    fmt = c["dtype"]
+    greedy = WORKLOADS[args.workload]["mode"] == "greedy"
+    h = c["h"]
+
+    def one(i):
+        r = i % h.shape[0]
+        if greedy:
+            oracle.head_greedy(c["W"], h[r:r + 1], fmt)
+        else:
+            oracle.head_logprob(c["W"], h[r:r + 1], c["targets"][r:r + 1], fmt)
+    for i in range(args.warmup):
+        one(i)
+    # bound the timed work to a few minutes of CPU time
+    t0 = time.perf_counter()
+    one(0)
+    per = time.perf_counter() - t0
+    steps = max(1, min(args.steps, int(args.ref_seconds / max(per, 1e-6))))
+    t0 = time.perf_counter()
+    for i in range(steps):
+        one(i)
+    dt = time.perf_counter() - t0
+    value = steps / dt
+    sample = (f"{steps} of {args.steps} requested steps, each one hidden row of the "
+              f"{args.workload} workload through the CPU oracle (B=1 call)")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "rows/s",
+            "n_gpus": world, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64" if fmt != "int8" else "int64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOADS[args.workload]["desc"], "name": args.workload},
+            "cpu_baseline": {"value": round(value, 4), "unit": "rows/s", "cores": cpu_cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="pr1", choices=sorted(WORKLOADS))
+    ap.add_argument("--batch", type=int, default=512, help="rows per call (int8 workload)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--e2e-seconds", type=float, default=3.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local_rank = env_rank()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
