@@ -145,6 +145,39 @@ int detlm_head_debug(detlm_head_t* head, int flags, uint64_t timeout_ns);
 int detlm_head_tiles(const detlm_head_t* head, int64_t B, int32_t* n_vtiles,
                      int32_t* n_cols);
 
+/* Greedy call that allocates no device memory at all (no counterpart in the
+ * source pages; this is a deployment convenience).
+ *
+ * Meant for callers that may not call cudaMalloc or any other allocator:
+ * code living inside a framework that has already reserved all of the GPU's
+ * memory for itself (an inference server that pre-reserves HBM for its KV
+ * cache), plugin interfaces whose execute step must not allocate, and hot
+ * paths that cannot afford the device-wide synchronisation an allocation
+ * implies. It needs no handle: pass the weight directly.
+ *
+ * Same computation and outputs as detlm_head_greedy on a BF16 or FP16 head
+ * (same kernels, bit-identical results); INT8 returns DETLM_EUNSUPPORTED.
+ * The split-V records live in one static device array of
+ * DETLM_NOALLOC_SCRATCH_BYTES bytes, compiled into this library: every GPU
+ * that loads the library holds it until the process exits. A call needs
+ * 256 + 3 * 4 * ceil(V / 128) * B bytes of it (rounded up to 256-byte
+ * parts); larger B returns DETLM_EINVAL before any GPU work.
+ * err_dev: optional int on the device, set to 0 by the call and then to a
+ * non-zero error bit if a bounded wait in the kernel ran out (the outputs
+ * are then undefined). NULL: the error word lives in the static array and is
+ * not reported.
+ * The first call on each device looks up the array's device address with
+ * that device current (a one-time runtime query, no allocation); make that
+ * first call before capturing any stream. All calls share the array and it
+ * keeps the last call's contents (each call clears what must start at zero):
+ * calls that may run at the same time on the GPU (other streams, other host
+ * threads) race on it and must be serialised by the caller. */
+#define DETLM_NOALLOC_SCRATCH_BYTES (8u << 20)
+int detlm_greedy_noalloc(const void* W_dev, int64_t V, int64_t d, int dtype,
+                         const void* h_dev, int64_t B, int32_t* token_dev,
+                         float* gap_dev, float* logits_dev, int* err_dev,
+                         cudaStream_t stream);
+
 void detlm_head_destroy(detlm_head_t* head);
 
 const char* detlm_status_string(int status);

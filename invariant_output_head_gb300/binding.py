@@ -34,6 +34,7 @@ _SIGS = {
                                 ctypes.POINTER(ctypes.c_int32)]),
     "detlm_head_destroy": (None, [_vp]),
     "detlm_status_string": (ctypes.c_char_p, [_i32]),
+    "detlm_greedy_noalloc": (_i32, [_vp, _i64, _i64, _i32, _vp, _i64, _vp, _vp, _vp, _vp, _vp]),
 }
 
 _lib = None
@@ -138,6 +139,15 @@ def detlm_head_destroy(handle) -> None:
 
 def detlm_status_string(status: int) -> str:
     return status_string(status)
+
+
+def detlm_greedy_noalloc(W_ptr, V, d, dtype, h_ptr, B, token_ptr, gap_ptr, logits_ptr,
+                         err_ptr, stream) -> None:
+    """Greedy call that allocates no device memory (its workspace is a static
+    device array inside the library); for callers that may not allocate."""
+    _check(load_library().detlm_greedy_noalloc(W_ptr, V, d, dtype, h_ptr, B, token_ptr,
+                                               gap_ptr, logits_ptr, err_ptr, stream),
+           "detlm_greedy_noalloc")
 
 
 # ---- torch convenience wrapper ------------------------------------------

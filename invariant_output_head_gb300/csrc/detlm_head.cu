@@ -512,3 +512,133 @@ void detlm_head_destroy(detlm_head_t* h) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Greedy call without any device allocation (see the header for who needs
+// it). Its split-V records and error word live in this file-scope device
+// array; host code obtains the array's device address once per device with
+// cudaGetSymbolAddress (the host-side name is only a stand-in and must never
+// be handed to a kernel).
+static __device__ __align__(256) unsigned char detlm_noalloc_scratch[DETLM_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up on
+// the first call per device, with that device current).
+int noalloc_scratch(int dev, void** out) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return DETLM_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, detlm_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) return DETLM_ECUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return DETLM_OK;
+}
+
+}  // namespace
+
+extern "C" int detlm_greedy_noalloc(const void* W_dev, int64_t V, int64_t d, int dtype,
+                                    const void* h_dev, int64_t B, int32_t* token_dev,
+                                    float* gap_dev, float* logits_dev, int* err_dev,
+                                    cudaStream_t stream) {
+  if (dtype == DETLM_INT8) return DETLM_EUNSUPPORTED;
+  if (dtype != DETLM_BF16 && dtype != DETLM_FP16) return DETLM_EINVAL;
+  if (W_dev == nullptr || !aligned(W_dev, 16)) return DETLM_EINVAL;
+  if (V < 1 || V >= (int64_t{1} << 31) || d < 1 || d >= (int64_t{1} << 31)) return DETLM_EINVAL;
+  if ((d * 2) % 16 != 0) return DETLM_EINVAL;
+  if (bad_B(B)) return DETLM_EINVAL;
+  if (B == 0) return DETLM_OK;
+  if (h_dev == nullptr || !aligned(h_dev, 16)) return DETLM_EINVAL;
+  if (token_dev == nullptr || !aligned(token_dev, 4)) return DETLM_EINVAL;
+  if (gap_dev == nullptr || !aligned(gap_dev, 4)) return DETLM_EINVAL;
+  if (logits_dev != nullptr && !aligned(logits_dev, 4)) return DETLM_EINVAL;
+  if (err_dev != nullptr && !aligned(err_dev, 4)) return DETLM_EINVAL;
+  // scratch: error word (256 B), then rec_m, rec_i, rec_s [n_vt, B]
+  const int n_vt = static_cast<int>((V + kBM - 1) / kBM);
+  const size_t part = ws_part(static_cast<int64_t>(n_vt) * B);
+  if (256 + 3 * part > DETLM_NOALLOC_SCRATCH_BYTES) return DETLM_EINVAL;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DETLM_ECUDA;
+  int major = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (major != 10 || sms <= 0) return DETLM_ECUDA;
+  if (!load_encode()) return DETLM_ECUDA;
+  void* scratch = nullptr;
+  int st = noalloc_scratch(dev, &scratch);
+  if (st != DETLM_OK) return st;
+  uint8_t* sb = static_cast<uint8_t*>(scratch);
+  int* err = err_dev != nullptr ? err_dev : reinterpret_cast<int*>(sb);
+  float* rec_m = reinterpret_cast<float*>(sb + 256);
+  int32_t* rec_i = reinterpret_cast<int32_t*>(sb + 256 + part);
+  float* rec_s = reinterpret_cast<float*>(sb + 256 + 2 * part);
+
+  const int N = cols_for(B);
+  CUtensorMap tmW, tmH;
+  if (!encode_2d(&tmW, dtype, W_dev, d, V, kBM)) return DETLM_EINVAL;
+  if (!encode_2d(&tmH, dtype, h_dev, d, B, static_cast<uint32_t>(N))) return DETLM_EINVAL;
+
+  HeadParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.V = static_cast<int32_t>(V);
+  p.d = static_cast<int32_t>(d);
+  p.B = static_cast<int32_t>(B);
+  p.N = N;
+  p.n_vt = n_vt;
+  p.n_nt = static_cast<int32_t>((B + N - 1) / N);
+  p.nk = static_cast<int32_t>((d * 2 + kRowBytes - 1) / kRowBytes);
+  p.n_chunks = static_cast<int32_t>((d + kChunkK - 1) / kChunkK);
+  p.stages = stages_for(N);
+  p.tmem_cols = tmem_cols_for(2 * N);
+  p.idesc = idesc_f16(dtype == DETLM_BF16 ? 1u : 0u, kBM, static_cast<uint32_t>(N));
+  p.logits = logits_dev;
+  p.rec_m = rec_m;
+  p.rec_i = rec_i;
+  p.rec_s = rec_s;
+  p.err = err;
+  p.timeout_ns = kDefaultTimeoutNs;
+
+  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), stream);   // must start at zero
+  if (e != cudaSuccess) return status_from_cuda(e);
+  const size_t smem = smem_layout(N, p.stages).total + 1024;
+  e = cudaFuncSetAttribute(head_gemm_kernel<MODE_GREEDY>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return status_from_cuda(e);
+  const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
+  const int grid = static_cast<int>(units < sms ? units : sms);
+  head_gemm_kernel<MODE_GREEDY><<<grid, kThreads, smem, stream>>>(tmW, tmH, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return status_from_cuda(e);
+
+  MergeParams mp;
+  std::memset(&mp, 0, sizeof(mp));
+  mp.V = p.V;
+  mp.B = p.B;
+  mp.n_vt = p.n_vt;
+  mp.rec_m = rec_m;
+  mp.rec_i = rec_i;
+  mp.rec_s = rec_s;
+  mp.token = token_dev;
+  mp.gap = gap_dev;
+  mp.err = err;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>((B + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, merge_kernel<MODE_GREEDY>, mp);
+  return status_from_cuda(e);
+}
