@@ -227,7 +227,7 @@ def run_ours(args, rank, world, local_rank):
     W0 = to_dev(c["W"])
     wbytes = W0.numel() * W0.element_size()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    n_copies = max(2, int(np.ceil(2 * l2 / wbytes)) + 1)
+    n_copies = args.copies or max(2, int(np.ceil(2 * l2 / wbytes)) + 1)
     Ws = [W0] + [W0.clone() for _ in range(n_copies - 1)]
     heads = [ioh.Head(W, fmt) for W in Ws]
     h_all = to_dev(c["h"])
@@ -256,7 +256,7 @@ def run_ours(args, rank, world, local_rank):
         for j, (r0, B) in enumerate(calls):
             hd = heads[k[0] % n_copies]
             k[0] += 1
-            if ev is not None:
+            if ev is not None and ev[j] is not None:
                 bd.detlm_head_time_next(hd.handle, ev[j][0].cuda_event, ev[j][1].cuda_event)
             hv = h_all[r0:r0 + B]
             if greedy:
@@ -280,13 +280,22 @@ def run_ours(args, rank, world, local_rank):
     for hd in heads:
         assert hd.check() == 0, "device error after warm-up"
 
-    # kernel events for the projection kernel of every call in the timed region
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n_calls)] for _ in range(args.steps)]
-    for row in ev:          # torch creates an event at its first record
-        for e0, e1 in row:
-            e0.record(stream)
-            e1.record(stream)
+    # CUDA events around the projection kernel of every `event_every`-th call of
+    # the timed region (an event between two kernels stops the next call's
+    # kernel from starting early, so not every call is bracketed)
+    ev, idx = [], 0
+    for _ in range(args.steps):
+        row = []
+        for _ in range(n_calls):
+            if idx % args.event_every == 0:
+                pair = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                pair[0].record(stream)      # torch creates an event at its first record
+                pair[1].record(stream)
+                row.append(pair)
+            else:
+                row.append(None)
+            idx += 1
+        ev.append(row)
     sampler = ClockSampler(local_rank)
     if rank == 0:
         sampler.start()
@@ -321,7 +330,7 @@ def run_ours(args, rank, world, local_rank):
         for x, y in zip(first, last))
 
     # per-launch duration of the projection kernel, averaged over the timed region
-    kms = np.array([[e0.elapsed_time(e1) for e0, e1 in row] for row in ev])
+    kms = np.array([e[0].elapsed_time(e[1]) for row in ev for e in row if e is not None])
     rows_per_step = sum(B for _, B in calls)
     by, fl = 0.0, 0.0
     for _, B in calls:
@@ -355,6 +364,7 @@ def run_ours(args, rank, world, local_rank):
                      "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
                      "traffic": traffic, "kernel": "head_gemm_kernel",
                      "kernel_us_per_launch": round(avg_kernel_s * 1e6, 2),
+                     "timed_launches": int(kms.size),
                      "algorithmic_bytes_per_launch": int(by_launch),
                      "algorithmic_flops_per_launch": fl_launch,
                      "peak_source": f"MEASURED_PEAKS.json ({peaks['source']}, "
@@ -363,9 +373,11 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": 2 * n_calls * args.steps,
         "clocks": clocks,
     }
-    if rank == 0:
+    if rank == 0 and not args.profile:
         res["e2e"] = run_e2e(args, c, heads, calls, greedy, rows_per_step, dev, stream)
         res["cpu_baseline"] = cpu_baseline(args.workload, c, budget_s=args.cpu_seconds)
+    if args.profile:
+        res["profile_run"] = "e2e and cpu_baseline legs skipped (--profile)"
     return res
 
 
@@ -502,6 +514,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--e2e-seconds", type=float, default=3.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--event-every", type=int, default=4,
+                    help="bracket every n-th call's projection kernel with CUDA events")
+    ap.add_argument("--copies", type=int, default=0,
+                    help="copies of W to rotate (default: enough to exceed 2x L2)")
+    ap.add_argument("--profile", action="store_true",
+                    help="GPU leg only (no e2e, no CPU baseline): for profiler runs")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -96,6 +96,13 @@ uint32_t tmem_cols_for(int ncols) {
   return c;
 }
 
+// Chunk slots: as many as fit 512 TMEM columns, at most kMaxSlots. The
+// slot count changes no arithmetic (every chunk starts from zero).
+int slots_for(int N) {
+  int s = 512 / N;
+  return s > kMaxSlots ? kMaxSlots : s;
+}
+
 int stages_for(int N) {
   const SmemLayout L1 = smem_layout(N, 1);
   const uint32_t fixed = L1.total - L1.stage_bytes + 2u * kMaxStages * 8u + 1024u;
@@ -145,6 +152,45 @@ WsView ws_view(const detlm_head* h, int64_t B) {
   return w;
 }
 
+// Launch kernel 1 for N = 16 * nblk as a programmatic dependent of the
+// previous kernel on the stream (its prologue overlaps that kernel's tail).
+template <int MODE, int NBLK>
+cudaError_t launch_gemm_n(const CUtensorMap& tmW, const CUtensorMap& tmH, const HeadParams& p,
+                          int grid, size_t smem, cudaStream_t stream) {
+  auto kern = head_gemm_kernel<MODE, NBLK>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmW, tmH, p);
+}
+
+template <int MODE>
+cudaError_t launch_gemm(const CUtensorMap& tmW, const CUtensorMap& tmH, const HeadParams& p,
+                        int grid, size_t smem, cudaStream_t stream) {
+  switch (p.N / 16) {
+    case 1: return launch_gemm_n<MODE, 1>(tmW, tmH, p, grid, smem, stream);
+    case 2: return launch_gemm_n<MODE, 2>(tmW, tmH, p, grid, smem, stream);
+    case 3: return launch_gemm_n<MODE, 3>(tmW, tmH, p, grid, smem, stream);
+    case 4: return launch_gemm_n<MODE, 4>(tmW, tmH, p, grid, smem, stream);
+    case 5: return launch_gemm_n<MODE, 5>(tmW, tmH, p, grid, smem, stream);
+    case 6: return launch_gemm_n<MODE, 6>(tmW, tmH, p, grid, smem, stream);
+    case 7: return launch_gemm_n<MODE, 7>(tmW, tmH, p, grid, smem, stream);
+    case 8: return launch_gemm_n<MODE, 8>(tmW, tmH, p, grid, smem, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <int MODE>
 int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* targets,
                  int32_t* token, float* gap, float* logits, float* logp, cudaStream_t stream) {
@@ -165,8 +211,9 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   p.n_nt = static_cast<int32_t>((B + N - 1) / N);
   p.nk = h->nk;
   p.n_chunks = static_cast<int32_t>((h->d + kChunkK - 1) / kChunkK);
+  p.n_slots = slots_for(N);
   p.stages = stages_for(N);
-  p.tmem_cols = tmem_cols_for(2 * N);
+  p.tmem_cols = tmem_cols_for(p.n_slots * N);
   p.idesc = idesc_f16(h->dtype == DETLM_BF16 ? 1u : 0u, kBM, static_cast<uint32_t>(N));
   p.logits = logits;
   p.targets = targets;
@@ -180,16 +227,11 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
 
   const SmemLayout L = smem_layout(N, p.stages);
   const size_t smem = L.total + 1024;
-  auto kern = head_gemm_kernel<MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return status_from_cuda(e);
   const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
   const int grid = static_cast<int>(units < h->num_sms ? units : h->num_sms);
 
   if (h->t_start) cudaEventRecord(h->t_start, stream);
-  kern<<<grid, kThreads, smem, stream>>>(h->tmW, tmH, p);
-  e = cudaGetLastError();
+  cudaError_t e = launch_gemm<MODE>(h->tmW, tmH, p, grid, smem, stream);
   if (h->t_stop) {
     cudaEventRecord(h->t_stop, stream);
     h->t_start = h->t_stop = nullptr;
@@ -596,8 +638,9 @@ extern "C" int detlm_greedy_noalloc(const void* W_dev, int64_t V, int64_t d, int
   p.n_nt = static_cast<int32_t>((B + N - 1) / N);
   p.nk = static_cast<int32_t>((d * 2 + kRowBytes - 1) / kRowBytes);
   p.n_chunks = static_cast<int32_t>((d + kChunkK - 1) / kChunkK);
+  p.n_slots = slots_for(N);
   p.stages = stages_for(N);
-  p.tmem_cols = tmem_cols_for(2 * N);
+  p.tmem_cols = tmem_cols_for(p.n_slots * N);
   p.idesc = idesc_f16(dtype == DETLM_BF16 ? 1u : 0u, kBM, static_cast<uint32_t>(N));
   p.logits = logits_dev;
   p.rec_m = rec_m;
@@ -609,13 +652,9 @@ extern "C" int detlm_greedy_noalloc(const void* W_dev, int64_t V, int64_t d, int
   cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), stream);   // must start at zero
   if (e != cudaSuccess) return status_from_cuda(e);
   const size_t smem = smem_layout(N, p.stages).total + 1024;
-  e = cudaFuncSetAttribute(head_gemm_kernel<MODE_GREEDY>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return status_from_cuda(e);
   const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
   const int grid = static_cast<int>(units < sms ? units : sms);
-  head_gemm_kernel<MODE_GREEDY><<<grid, kThreads, smem, stream>>>(tmW, tmH, p);
-  e = cudaGetLastError();
+  e = launch_gemm<MODE_GREEDY>(tmW, tmH, p, grid, smem, stream);
   if (e != cudaSuccess) return status_from_cuda(e);
 
   MergeParams mp;

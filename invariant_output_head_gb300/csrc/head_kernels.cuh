@@ -15,13 +15,13 @@
 // K=16 step toward zero-ish, so a long K loop in one accumulator drifts by
 // about half an ulp per step when all products share a sign. K is therefore
 // cut into chunks of kChunkK elements (a function of d only); each chunk is
-// accumulated from zero in one of two TMEM slots (ping-pong), and the
+// accumulated from zero in one of up to kMaxSlots TMEM slots (a ring), and the
 // epilogue adds the chunk sums in fp32 registers with round-to-nearest, in
 // ascending chunk order. This keeps every logit within 1e-6 * sum|w h| and
 // is the same arithmetic for every B.
 //
 // Warp 0 issues TMA loads into an S-stage ring, warp 1 issues the MMAs into
-// the two chunk slots, warps 2..5 drain each slot into running sums (one
+// the chunk slot ring, warps 2..5 drain each slot into running sums (one
 // thread per vocabulary row, up to 128 hidden rows per thread), then write
 // the optional fp32 logits and the per-tile decision record of each hidden
 // row:
@@ -54,6 +54,7 @@ constexpr int kMaxN = 128;        // largest MMA N (running sums live in registe
 constexpr int kChunkK = 128;      // K elements per accumulation chunk
 constexpr int kBlocksPerChunk = kChunkK / 64;   // 128-byte K blocks of 16-bit data
 constexpr int kMaxStages = 12;
+constexpr int kMaxSlots = 8;
 constexpr int kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
 
 enum : int { MODE_GREEDY = 0, MODE_LOGPROB = 1 };
@@ -64,7 +65,8 @@ struct HeadParams {
   int32_t N;            // hidden rows per unit (MMA N), multiple of 16, <= kMaxN
   int32_t n_vt, n_nt;   // vocabulary tiles, hidden-row tiles
   int32_t nk;           // K blocks of 128 bytes
-  int32_t n_chunks;     // K chunks of kChunkK elements
+  int32_t n_chunks;     // K chunks of kChunkK elements (= pipeline stages per unit)
+  int32_t n_slots;      // TMEM chunk slots (ring), N columns each
   int32_t stages;
   uint32_t tmem_cols;
   uint32_t idesc;
@@ -174,32 +176,36 @@ struct SmemLayout {
   uint32_t a_bytes, b_bytes, stage_bytes, ctrl_off, red_off, total;
 };
 
+// One pipeline stage holds one K chunk: kBlocksPerChunk 128-byte K boxes of
+// the W tile (each [128 rows x 128 B], swizzled) followed by as many boxes of
+// the hidden-row tile ([N rows x 128 B] each).
 __host__ __device__ inline SmemLayout smem_layout(int N, int stages) {
   SmemLayout L;
-  L.a_bytes = kBM * kRowBytes;
-  L.b_bytes = static_cast<uint32_t>(N) * kRowBytes;
+  L.a_bytes = kBlocksPerChunk * kBM * kRowBytes;
+  L.b_bytes = kBlocksPerChunk * static_cast<uint32_t>(N) * kRowBytes;
   L.stage_bytes = L.a_bytes + L.b_bytes;
   L.ctrl_off = static_cast<uint32_t>(stages) * L.stage_bytes;
-  // barriers: full[S], empty[S], slot_full[2], slot_empty[2], never, drain;
-  // then the TMEM address holder and the abort flag
-  L.red_off = L.ctrl_off + (2u * stages + 6u) * 8u + 16u;
+  // barriers: full[S], empty[S], slot_full[kMaxSlots], slot_empty[kMaxSlots],
+  // never, drain; then the TMEM address holder and the abort flag
+  L.red_off = L.ctrl_off + (2u * stages + 2u * kMaxSlots + 2u) * 8u + 16u;
   // per-quadrant column results: 3 words x 4 quadrants x N columns
   L.total = L.red_off + 3u * 4u * static_cast<uint32_t>(N) * 4u;
   return L;
 }
 
 // ----------------------------------------------------------------- kernel 1
-template <int MODE>
+template <int MODE, int NBLK>
 __global__ void __launch_bounds__(kThreads, 1)
 head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                  const __grid_constant__ CUtensorMap tmH, const HeadParams p) {
+  static_assert(NBLK >= 1 && NBLK * 16 <= kMaxN, "N = 16 * NBLK");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = p.stages;
-  const int N = p.N;
+  constexpr int N = 16 * NBLK;
   const SmemLayout L = smem_layout(N, S);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.ctrl_off);
@@ -207,10 +213,11 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
   auto accf_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
-  const uint32_t never_bar = bar0 + 8u * (2 * S + 4);
-  const uint32_t drain_bar = bar0 + 8u * (2 * S + 5);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.ctrl_off + (2 * S + 6) * 8);
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * S + kMaxSlots + b); };
+  const uint32_t never_bar = bar0 + 8u * (2 * S + 2 * kMaxSlots);
+  const uint32_t drain_bar = bar0 + 8u * (2 * S + 2 * kMaxSlots + 1);
+  uint32_t* tmem_holder =
+      reinterpret_cast<uint32_t*>(smem + L.ctrl_off + (2 * S + 2 * kMaxSlots + 2) * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   float* red_m = reinterpret_cast<float*>(smem + L.red_off);
   int32_t* red_i = reinterpret_cast<int32_t*>(red_m + 4 * N);
@@ -224,7 +231,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < p.n_slots; ++b) {
       mbar_init(accf_bar(b), 1);
       mbar_init(acce_bar(b), 4);
     }
@@ -244,6 +251,10 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // launched as a dependent grid: everything above overlapped the previous
+  // kernel on the stream; inputs are read and outputs written only after it
+  // has completed
+  grid_dep_wait();
   const uint32_t tmem_base = *tmem_holder;
   const int n_units = p.n_vt * p.n_nt;
   const int kElems = kRowBytes / 2;     // 16-bit elements per 128-byte row
@@ -257,15 +268,22 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const int vt = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
-        for (int kb = 0; kb < p.nk; ++kb) {
+        for (int c = 0; c < p.n_chunks; ++c) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
             ok = false;
             break;
           }
           outstanding &= ~(1u << stage);
-          mbar_arrive_expect_tx(full_bar(stage), L.stage_bytes);
-          tma_load_2d(sA(stage), &tmW, kb * kElems, vt * kBM, full_bar(stage), pol_w);
-          tma_load_2d(sB(stage), &tmH, kb * kElems, nt * N, full_bar(stage), pol_h);
+          const int kb0 = c * kBlocksPerChunk;
+          const int nb = min(kBlocksPerChunk, p.nk - kb0);
+          mbar_arrive_expect_tx(full_bar(stage), static_cast<uint32_t>(nb) *
+                                                     (kBM + N) * kRowBytes);
+          for (int b = 0; b < nb; ++b) {
+            tma_load_2d(sA(stage) + b * kBM * kRowBytes, &tmW, (kb0 + b) * kElems, vt * kBM,
+                        full_bar(stage), pol_w);
+            tma_load_2d(sB(stage) + b * N * kRowBytes, &tmH, (kb0 + b) * kElems, nt * N,
+                        full_bar(stage), pol_h);
+          }
           outstanding |= 1u << stage;
           out_par = (out_par & ~(1u << stage)) | (phase << stage);
           if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
@@ -288,28 +306,27 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       if (p.stall) ok = mbar_wait(never_bar, 0, abort_flag, p.timeout_ns);
-      uint32_t cc = 0;   // chunks issued so far (slot = cc & 1)
+      uint32_t slot = 0, sph = 0;   // chunk slot ring position and phase
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        for (int c = 0; c < p.n_chunks && ok; ++c, ++cc) {
-          const uint32_t slot = cc & 1u, sph = (cc >> 1) & 1u;
+        for (int c = 0; c < p.n_chunks && ok; ++c) {
           if (!mbar_wait(acce_bar(slot), sph ^ 1u, abort_flag, p.timeout_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + slot * static_cast<uint32_t>(N);
-          const int kb0 = c * kBlocksPerChunk;
-          const int kb1 = min(kb0 + kBlocksPerChunk, p.nk);
-          for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(full_bar(stage), phase, abort_flag, p.timeout_ns)) { ok = false; break; }
-            tc_fence_after();
-            const uint64_t da = sdesc_sw128(sA(stage));
-            const uint64_t db = sdesc_sw128(sB(stage));
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.timeout_ns)) { ok = false; break; }
+          tc_fence_after();
+          const int nb = min(kBlocksPerChunk, p.nk - c * kBlocksPerChunk);
+          for (int b = 0; b < nb; ++b) {
+            const uint64_t da = sdesc_sw128(sA(stage) + b * kBM * kRowBytes);
+            const uint64_t db = sdesc_sw128(sB(stage) + b * N * kRowBytes);
 #pragma unroll
             for (int k = 0; k < 4; ++k)   // K = 16 per MMA: 32 bytes = 2 descriptor units
-              mma_f16(d_tmem, da + 2u * k, db + 2u * k, p.idesc, (kb != kb0) || (k != 0));
-            mma_commit(empty_bar(stage));
-            if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+              mma_f16(d_tmem, da + 2u * k, db + 2u * k, p.idesc, (b != 0) || (k != 0));
           }
+          mma_commit(empty_bar(stage));
+          if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
           if (!ok) break;
           mma_commit(accf_bar(slot));
+          if (++slot == static_cast<uint32_t>(p.n_slots)) { slot = 0; sph ^= 1u; }
         }
       }
       if (!ok) {
@@ -327,40 +344,38 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
     const int q = warp & 3;                    // TMEM lane quadrant of this warp
     const int et = threadIdx.x - 64;           // 0..127
     const int row = q * 32 + lane;             // vocabulary row within the tile
-    const int nblk = N / 16;                   // 16-column blocks in this unit
     const uint32_t tlane = static_cast<uint32_t>(q * 32) << 16;
-    uint32_t cc = 0;
+    uint32_t slot = 0, sph = 0;
     bool failed = false;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       const int vt = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
-      float acc[kMaxN / 16][16];
-      for (int c = 0; c < p.n_chunks; ++c, ++cc) {
-        const uint32_t slot = cc & 1u, sph = (cc >> 1) & 1u;
-        if (!failed && !mbar_wait(accf_bar(slot), sph, abort_flag, p.timeout_ns)) {
+      float acc[NBLK][16];
+      for (int c = 0; c < p.n_chunks; ++c) {
+        const uint32_t cur = slot, cph = sph;
+        if (++slot == static_cast<uint32_t>(p.n_slots)) { slot = 0; sph ^= 1u; }
+        if (!failed && !mbar_wait(accf_bar(cur), cph, abort_flag, p.timeout_ns)) {
           failed = true;
           *abort_flag = 1;
         }
         if (failed) continue;
         tc_fence_after();
-        const uint32_t sbase = tmem_base + tlane + slot * static_cast<uint32_t>(N);
+        const uint32_t sbase = tmem_base + tlane + cur * static_cast<uint32_t>(N);
 #pragma unroll
-        for (int bb = 0; bb < kMaxN / 16; ++bb) {
-          if (bb < nblk) {
-            uint32_t r[16];
-            tmem_ld16(sbase + bb * 16, r);
-            tmem_wait_ld();
-            if (c == 0) {
+        for (int bb = 0; bb < NBLK; ++bb) {
+          uint32_t r[16];
+          tmem_ld16(sbase + bb * 16, r);
+          tmem_wait_ld();
+          if (c == 0) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) acc[bb][i] = __uint_as_float(r[i]);
-            } else {
+            for (int i = 0; i < 16; ++i) acc[bb][i] = __uint_as_float(r[i]);
+          } else {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) acc[bb][i] = __fadd_rn(acc[bb][i], __uint_as_float(r[i]));
-            }
+            for (int i = 0; i < 16; ++i) acc[bb][i] = __fadd_rn(acc[bb][i], __uint_as_float(r[i]));
           }
         }
         tc_fence_before();   // slot fully read: hand it back to the MMA warp
         __syncwarp();
-        if (lane == 0) mbar_arrive(acce_bar(slot));
+        if (lane == 0) mbar_arrive(acce_bar(cur));
       }
       if (epi_bar_or(failed || *abort_flag)) {
         if (et == 0) { *abort_flag = 1; atomicOr(p.err, ERR_TIMEOUT); }
@@ -370,8 +385,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       const bool vok = v < p.V;
       const int n0 = nt * N;
 #pragma unroll
-      for (int bb = 0; bb < kMaxN / 16; ++bb) {
-        if (bb >= nblk) continue;
+      for (int bb = 0; bb < NBLK; ++bb) {
         const int c0 = bb * 16;
         if (p.logits != nullptr && vok) {
 #pragma unroll
@@ -462,6 +476,7 @@ __device__ __forceinline__ float gap_ulp_bf16(float m, float s) {
 template <int MODE>
 __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
   grid_dep_wait();   // records of kernel 1 are complete and visible
+  grid_dep_launch(); // the next call's kernel 1 may start its prologue
   const int lane = threadIdx.x & 31;
   const int n = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (n >= p.B) return;
