@@ -1,0 +1,128 @@
+"""Failure detection without faulting the GPU.
+
+A device-side wait that runs out is provoked on purpose: the test hook makes
+the MMA issuer wait on a barrier nothing arrives on, with a 20 ms limit. The
+kernel gives up, records the timeout in the handle's error word and returns;
+the host reads DETLM_ETIMEOUT, and the next call on the same context
+succeeds. Bad arguments are refused on the host before any GPU work; an
+out-of-range target id yields NaN and DETLM_ETARGET.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.gpu_helpers import check_float_greedy, dev, host, oracle_float_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from invariant_output_head_gb300 import binding
+    binding.load_library()
+    return torch, binding
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "int8"])
+def test_stalled_wait_reports_timeout_and_context_survives(env, fmt):
+    torch, b = env
+    if fmt == "int8":
+        case = synth.small_int8(3, 700, 256, 9)
+    else:
+        case = synth.small_float(3, 700, 256, 9)
+    head = b.Head(dev(case["W"], fmt), fmt)
+    h = dev(case["h"], fmt)
+    b.detlm_head_debug(head.handle, b.DETLM_DEBUG_STALL, 20_000_000)
+    head.greedy(h, with_logits=True)
+    torch.cuda.synchronize()
+    assert head.check() == b.DETLM_ETIMEOUT
+    b.detlm_head_debug(head.handle, 0, 0)
+    t, g, z = head.greedy(h, with_logits=True)
+    assert head.check() == b.DETLM_OK
+    ref = oracle.head_greedy(case["W"], case["h"], fmt)
+    assert (host(t) == ref["token"]).all()
+
+
+def test_out_of_range_target_gives_nan_and_status(env):
+    torch, b = env
+    case = synth.small_float(4, 500, 128, 6)
+    head = b.Head(dev(case["W"], "bf16"), "bf16")
+    tg = case["targets"].copy()
+    tg[1], tg[4] = -1, 500
+    lp = host(head.logprob(dev(case["h"], "bf16"), dev(tg, "int32")))
+    assert head.check() == b.DETLM_ETARGET
+    assert np.isnan(lp[[1, 4]]).all() and np.isfinite(lp[[0, 2, 3, 5]]).all()
+    assert head.check() == b.DETLM_OK        # the error word was cleared
+
+
+def test_host_side_argument_errors(env):
+    torch, b = env
+    lib = b.load_library()
+    case = synth.small_float(5, 300, 64, 4)
+    W = dev(case["W"], "bf16")
+    head = b.Head(W, "bf16")
+    h = dev(case["h"], "bf16")
+    tok = torch.empty(4, dtype=torch.int32, device="cuda")
+    gap = torch.empty(4, dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    # misaligned hidden rows, null outputs, negative B
+    assert lib.detlm_head_greedy(head.handle, h.data_ptr() + 2, 4, tok.data_ptr(),
+                                 gap.data_ptr(), None, s) == b.DETLM_EINVAL
+    assert lib.detlm_head_greedy(head.handle, h.data_ptr(), 4, None, gap.data_ptr(),
+                                 None, s) == b.DETLM_EINVAL
+    assert lib.detlm_head_greedy(head.handle, h.data_ptr(), -1, tok.data_ptr(),
+                                 gap.data_ptr(), None, s) == b.DETLM_EINVAL
+    # B = 0 is a no-op
+    assert lib.detlm_head_greedy(head.handle, h.data_ptr(), 0, tok.data_ptr(),
+                                 gap.data_ptr(), None, s) == b.DETLM_OK
+    # log-prob is not defined for the integer head
+    Wi = dev(synth.small_int8(5, 300, 64, 1)["W"], "int8")
+    hi = b.Head(Wi, "int8")
+    assert lib.detlm_head_logprob(hi.handle, h.data_ptr(), tok.data_ptr(), 4,
+                                  gap.data_ptr(), s) == b.DETLM_EUNSUPPORTED
+    # misaligned weight at create
+    out = ctypes.c_void_p()
+    assert lib.detlm_head_create(ctypes.byref(out), W.data_ptr() + 8, 300, 64,
+                                 b.DETLM_BF16) == b.DETLM_EINVAL
+
+
+def test_host_buffer_calls_match_device_calls(env):
+    torch, b = env
+    case = synth.small_float(6, 900, 256, 7)
+    head = b.Head(dev(case["W"], "bf16"), "bf16")
+    t, g, z = head.greedy(dev(case["h"], "bf16"), with_logits=True)
+    lp = head.logprob(dev(case["h"], "bf16"), dev(case["targets"], "int32"))
+    B, V = 7, 900
+    th = np.empty(B, np.int32)
+    gh = np.empty(B, np.float32)
+    zh = np.empty((B, V), np.float32)
+    lh = np.empty(B, np.float32)
+    hb = np.ascontiguousarray(case["h"])
+    s = torch.cuda.current_stream().cuda_stream
+    b.detlm_head_greedy_host(head.handle, hb.ctypes.data, B, th.ctypes.data, gh.ctypes.data,
+                             zh.ctypes.data, s)
+    b.detlm_head_logprob_host(head.handle, hb.ctypes.data, case["targets"].ctypes.data, B,
+                              lh.ctypes.data, s)
+    assert (th == host(t)).all()
+    assert (gh.view(np.uint32) == host(g).view(np.uint32)).all()
+    assert (zh.view(np.uint32) == host(z).view(np.uint32)).all()
+    assert (lh.view(np.uint32) == host(lp).view(np.uint32)).all()
+
+
+def test_reserved_workspace_and_tiles(env):
+    torch, b = env
+    case = synth.small_float(7, 1000, 128, 300)
+    head = b.Head(dev(case["W"], "bf16"), "bf16")
+    b.detlm_head_reserve(head.handle, 300)
+    assert head.tiles(1) == (8, 16)
+    assert head.tiles(17) == (8, 32)
+    assert head.tiles(300) == (8, 128)
+    t, g, _ = head.greedy(dev(case["h"], "bf16"))
+    z_ref, A = oracle_float_rows(case["W"], case["h"], "bf16")
+    check_float_greedy(z_ref, A, host(t), host(g), label="reserved")
