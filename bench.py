@@ -164,6 +164,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": n}
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """Max of a host scalar over all ranks (NCCL on GPUs, gloo on CPUs)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = (torch.device("cuda", torch.cuda.current_device())
+           if dist.get_backend() == "nccl" else torch.device("cpu"))
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(rows_per_step: int, steps: int, world: int, elapsed_ms: float) -> float:
+    """Whole-job throughput: every rank runs the same per-GPU workload (weak
+    scaling), timed by the slowest rank."""
+    return rows_per_step * steps * world / (elapsed_ms / 1e3)
+
+
 # ------------------------------------------------------------- workloads
 
 def make_inputs(name: str, batch: int):
@@ -312,11 +331,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop() if rank == 0 else None
-    elapsed_ms = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world)
     for hd in heads:
         assert hd.check() == 0, "device error in the timed region"
 
@@ -348,7 +363,7 @@ def run_ours(args, rank, world, local_rank):
         peak, unit = peaks["bf16_tflops_sustained"], "TFLOP/s"
     traffic = profiled_traffic(args.workload)
 
-    value = rows_per_step * args.steps * world / (elapsed_ms / 1e3)
+    value = job_rows_per_s(rows_per_step, args.steps, world, elapsed_ms)
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
