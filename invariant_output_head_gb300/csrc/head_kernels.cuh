@@ -27,7 +27,10 @@
 // row:
 //   greedy : (m, i, s) = tile maximum, lowest index attaining it, runner-up
 //            value of the tile's multiset;
-//   logprob: (m, S) = tile maximum and sum_v exp(z_v - m), plus z[target].
+//   logprob: (m, S) = tile maximum and sum_v exp(z_v - m), plus z[target];
+//            within a warp the exact maximum comes first and the 32 terms
+//            exp(z - m_warp) are added in a fixed tree, then the four warps'
+//            (m, S) pairs merge in a fixed order.
 //
 // Kernel 2 (merge_kernel): one warp per hidden row folds the n_vt tile
 // records in a fixed order (lane l takes tiles l, l+32, ... in ascending
@@ -35,9 +38,10 @@
 // No atomics take part in any result.
 //
 // Both reductions are written so that a row's bits do not depend on its
-// column position in the tile or on B: the within-tile tree over the 128
-// vocabulary rows has the same shape for every column, and both merge
-// operators are commutative bit for bit.
+// column position in the tile or on B: the greedy record is exact (a
+// function of the multiset of values), and every floating-point sum of the
+// log-sum-exp runs in a tree whose shape is the same for every column, with
+// operators that are commutative bit for bit.
 #pragma once
 #include <cuda.h>
 #include <cstdint>
@@ -125,33 +129,58 @@ __device__ __forceinline__ Top2 shfl_xor(const Top2& x, int b) {
 __device__ __forceinline__ Lse shfl_xor(const Lse& x, int b) {
   return Lse{__shfl_xor_sync(0xffffffffu, x.m, b), __shfl_xor_sync(0xffffffffu, x.S, b)};
 }
-__device__ __forceinline__ Top2 merge(const Top2& a, const Top2& b) { return top2_merge(a, b); }
-__device__ __forceinline__ Lse merge(const Lse& a, const Lse& b) { return lse_merge(a, b); }
-
-// One halving step of the transposed reduction over 16 columns held by each
-// lane: the lane keeps one half of its columns, sends the other half to the
-// partner lane ^ b and merges what it receives into the kept half.
-template <int H, typename T>
-__device__ __forceinline__ void transpose_step(T (&g)[16], int lane, int b) {
-  const bool up = (lane & b) != 0;
-#pragma unroll
-  for (int j = 0; j < H; ++j) {
-    const T keep = up ? g[j + H] : g[j];
-    const T send = up ? g[j] : g[j + H];
-    g[j] = merge(keep, shfl_xor(send, b));
-  }
+// Order-preserving 32-bit keys of finite floats (larger float, larger
+// unsigned key); key 0 is below every finite value and marks "no value".
+__device__ __forceinline__ uint32_t fkey(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float funkey(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Reduce 16 columns over the warp's 32 lanes (vocabulary rows). Afterwards
-// lanes l and l ^ 16 hold column brev4(l & 15). The tree is the same for
-// every column: pairs (l, l^1), then ^2, ^4, ^8, ^16.
-template <typename T>
-__device__ __forceinline__ T warp_reduce16(T (&g)[16], int lane) {
-  transpose_step<8>(g, lane, 1);
-  transpose_step<4>(g, lane, 2);
-  transpose_step<2>(g, lane, 4);
-  transpose_step<1>(g, lane, 8);
-  return merge(g[0], shfl_xor(g[0], 16));
+// Per-column reduction of one 16-column block over a warp's 32 vocabulary
+// rows, through a shared-memory transpose (warp-collective shuffles and
+// reductions serialise on this part, a 16-element fold from shared memory
+// does not). Lane l ends with column (l & 15) folded over rows 16*(l >> 4) ..
+// 16*(l >> 4) + 15 in ascending order; one exchange with lane l ^ 16 then
+// covers all 32 rows. The fold order is the same for every column.
+constexpr int kXpStride = 17;             // padded row stride (no bank conflicts)
+constexpr int kXpWords = 32 * kXpStride;  // per warp
+
+// greedy: exact (max, lowest row index of it, runner-up); invalid rows are -inf
+__device__ __forceinline__ Top2 xp_top2(const float* xp, int lane, int v_row0) {
+  const int c = lane & 15, h = lane >> 4;
+  Top2 t{-INFINITY, INT32_MAX, -INFINITY};
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int r = h * 16 + j;
+    const float x = xp[r * kXpStride + c];
+    if (x > t.m) {              // strictly greater: on a tie the lower row stays
+      t.s = t.m;
+      t.m = x;
+      t.i = v_row0 + r;
+    } else {
+      t.s = fmaxf(t.s, x);
+    }
+  }
+  return top2_merge(t, shfl_xor(t, 16));
+}
+
+// log-prob: exact maximum M of the 16 rows, then sum of exp(z - M) in
+// ascending row order; the two halves merge commutatively
+__device__ __forceinline__ Lse xp_lse(const float* xp, int lane) {
+  const int c = lane & 15, h = lane >> 4;
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) m = fmaxf(m, xp[(h * 16 + j) * kXpStride + c]);
+  float sum = 0.0f;
+  if (m != -INFINITY) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      sum = __fadd_rn(sum, __expf(xp[(h * 16 + j) * kXpStride + c] - m));
+  }
+  return lse_merge(Lse{m, sum}, shfl_xor(Lse{m, sum}, 16));
 }
 
 __device__ __forceinline__ int brev4(int l) {
@@ -173,7 +202,7 @@ __device__ __forceinline__ bool epi_bar_or(bool pred) {
 
 // ----------------------------------------------------------- shared layout
 struct SmemLayout {
-  uint32_t a_bytes, b_bytes, stage_bytes, ctrl_off, red_off, total;
+  uint32_t a_bytes, b_bytes, stage_bytes, ctrl_off, red_off, xp_off, total;
 };
 
 // One pipeline stage holds one K chunk: kBlocksPerChunk 128-byte K boxes of
@@ -188,8 +217,10 @@ __host__ __device__ inline SmemLayout smem_layout(int N, int stages) {
   // barriers: full[S], empty[S], slot_full[kMaxSlots], slot_empty[kMaxSlots],
   // never, drain; then the TMEM address holder and the abort flag
   L.red_off = L.ctrl_off + (2u * stages + 2u * kMaxSlots + 2u) * 8u + 16u;
-  // per-quadrant column results: 3 words x 4 quadrants x N columns
-  L.total = L.red_off + 3u * 4u * static_cast<uint32_t>(N) * 4u;
+  // per-quadrant column results: 3 words x 4 quadrants x N columns, then
+  // the four epilogue warps' transpose areas
+  L.xp_off = L.red_off + 3u * 4u * static_cast<uint32_t>(N) * 4u;
+  L.total = L.xp_off + 4u * kXpWords * 4u;
   return L;
 }
 
@@ -222,6 +253,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   float* red_m = reinterpret_cast<float*>(smem + L.red_off);
   int32_t* red_i = reinterpret_cast<int32_t*>(red_m + 4 * N);
   float* red_s = reinterpret_cast<float*>(red_i + 4 * N);
+  float* xpose = reinterpret_cast<float*>(smem + L.xp_off);
   const uint32_t smem_base = smem_u32(smem);
   auto sA = [&](int s) { return smem_base + static_cast<uint32_t>(s) * L.stage_bytes; };
   auto sB = [&](int s) { return sA(s) + L.a_bytes; };
@@ -394,17 +426,16 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
             if (n < p.B) p.logits[static_cast<size_t>(n) * p.V + v] = acc[bb][i];
           }
         }
-        const int cw = c0 + brev4(lane & 15);   // column this lane ends up holding
-        if constexpr (MODE == MODE_GREEDY) {
-          Top2 g[16];
+        float* xp = xpose + q * kXpWords;
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            g[i] = vok ? Top2{acc[bb][i], v, -INFINITY} : Top2{-INFINITY, INT32_MAX, -INFINITY};
-          const Top2 t = warp_reduce16(g, lane);
+        for (int i = 0; i < 16; ++i) xp[lane * kXpStride + i] = vok ? acc[bb][i] : -INFINITY;
+        __syncwarp();
+        if constexpr (MODE == MODE_GREEDY) {
+          const Top2 t = xp_top2(xp, lane, vt * kBM + q * 32);
           if (lane < 16) {
-            red_m[q * N + cw] = t.m;
-            red_i[q * N + cw] = t.i;
-            red_s[q * N + cw] = t.s;
+            red_m[q * N + c0 + lane] = t.m;
+            red_i[q * N + c0 + lane] = t.i;
+            red_s[q * N + c0 + lane] = t.s;
           }
         } else {
           if (vok) {
@@ -414,15 +445,13 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
               if (n < p.B && p.targets[n] == v) p.zt[n] = acc[bb][i];
             }
           }
-          Lse g[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) g[i] = vok ? Lse{acc[bb][i], 1.0f} : Lse{-INFINITY, 0.0f};
-          const Lse t = warp_reduce16(g, lane);
+          const Lse t = xp_lse(xp, lane);
           if (lane < 16) {
-            red_m[q * N + cw] = t.m;
-            red_s[q * N + cw] = t.S;
+            red_m[q * N + c0 + lane] = t.m;
+            red_s[q * N + c0 + lane] = t.S;
           }
         }
+        __syncwarp();
       }
       named_bar_sync(1, kEpiThreads);
       // fixed combination of the four 32-row quadrants: (q0 . q1) . (q2 . q3)

@@ -74,7 +74,7 @@ struct Int8Params {
 };
 
 struct Int8Layout {
-  uint32_t a8, b8, st8, a16, b16, st16, off16, ctrl, red, total;
+  uint32_t a8, b8, st8, a16, b16, st16, off16, ctrl, red, xp, total;
 };
 
 __host__ __device__ inline Int8Layout int8_layout(int N, int s8, int s16) {
@@ -90,7 +90,8 @@ __host__ __device__ inline Int8Layout int8_layout(int N, int s8, int s16) {
   // f8full[s8], f8empty[s8], f16full[s16], f16empty[s16], accf[2], acce[2],
   // never, drain; then TMEM holder and abort flag
   L.red = L.ctrl + (2u * s8 + 2u * s16 + 6u) * 8u + 16u;
-  L.total = L.red + 3u * 4u * static_cast<uint32_t>(N) * 4u;
+  L.xp = L.red + 3u * 4u * static_cast<uint32_t>(N) * 4u;
+  L.total = L.xp + 4u * kXpWords * 4u;
   return L;
 }
 
@@ -108,7 +109,27 @@ __device__ __forceinline__ ITop2 shfl_xor(const ITop2& x, int b) {
   return ITop2{__shfl_xor_sync(0xffffffffu, x.m, b), __shfl_xor_sync(0xffffffffu, x.i, b),
                __shfl_xor_sync(0xffffffffu, x.s, b)};
 }
-__device__ __forceinline__ ITop2 merge(const ITop2& a, const ITop2& b) { return itop2_merge(a, b); }
+
+// Exact top-2 of one 16-column block of int32 logits over a warp's 32 rows
+// through the warp's shared-memory transpose area (INT32_MIN marks rows
+// outside the vocabulary; |z| is far below 2^31).
+__device__ __forceinline__ ITop2 xp_itop2(const int32_t* xp, int lane, int v_row0) {
+  const int c = lane & 15, h = lane >> 4;
+  ITop2 t{INT32_MIN, INT32_MAX, INT32_MIN};
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int r = h * 16 + j;
+    const int32_t x = xp[r * kXpStride + c];
+    if (x > t.m) {
+      t.s = t.m;
+      t.m = x;
+      t.i = v_row0 + r;
+    } else {
+      t.s = max(t.s, x);
+    }
+  }
+  return itop2_merge(t, shfl_xor(t, 16));
+}
 
 // four int8 in one word -> two half2 holding the same integers exactly
 __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
@@ -171,6 +192,7 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   int32_t* red_m = reinterpret_cast<int32_t*>(smem + L.red);
   int32_t* red_i = red_m + 4 * N;
   int32_t* red_s = red_i + 4 * N;
+  int32_t* xpose = reinterpret_cast<int32_t*>(smem + L.xp);
   const uint32_t base = smem_u32(smem);
 
   if (threadIdx.x == 0) {
@@ -340,17 +362,17 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             if (n < p.B) p.logits[static_cast<size_t>(n) * p.V + v] = x[i];
           }
         }
-        ITop2 g[16];
+        int32_t* xp = xpose + q * kXpWords;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          g[i] = vok ? ITop2{x[i], v, INT32_MIN} : ITop2{INT32_MIN, INT32_MAX, INT32_MIN};
-        const ITop2 t = warp_reduce16(g, lane);
-        const int cw = c0 + brev4(lane & 15);
+        for (int i = 0; i < 16; ++i) xp[lane * kXpStride + i] = vok ? x[i] : INT32_MIN;
+        __syncwarp();
+        const ITop2 t = xp_itop2(xp, lane, vt * kBM + q * 32);
         if (lane < 16) {
-          red_m[q * N + cw] = t.m;
-          red_i[q * N + cw] = t.i;
-          red_s[q * N + cw] = t.s;
+          red_m[q * N + c0 + lane] = t.m;
+          red_i[q * N + c0 + lane] = t.i;
+          red_s[q * N + c0 + lane] = t.s;
         }
+        __syncwarp();
       }
       named_bar_sync(1, kEpiThreads);
       for (int c = et; c < N; c += kEpiThreads) {
