@@ -283,10 +283,10 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // launched as a dependent grid: everything above overlapped the previous
-  // kernel on the stream; inputs are read and outputs written only after it
-  // has completed
-  grid_dep_wait();
+  // Launched as a dependent grid: the set-up above overlapped the previous
+  // kernels on the stream. The merge kernel may be scheduled at once (it
+  // waits for this grid to complete before reading anything).
+  grid_dep_launch();
   const uint32_t tmem_base = *tmem_holder;
   const int n_units = p.n_vt * p.n_nt;
   const int kElems = kRowBytes / 2;     // 16-bit elements per 128-byte row
@@ -296,27 +296,51 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_h = policy_evict_last();
+      // W is read-only for the life of the head, so the W boxes of the first
+      // S chunks are requested before waiting for the previous kernels; the
+      // hidden rows (which a previous kernel may write) only after.
+      const int n_my = (n_units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                       static_cast<int>(gridDim.x);
+      const int pre = min(S, n_my > 0 ? n_my * p.n_chunks : 0);
+      for (int j = 0; j < pre; ++j) {
+        const int u = blockIdx.x + (j / p.n_chunks) * gridDim.x;
+        const int vt = u / p.n_nt, c = j - (j / p.n_chunks) * p.n_chunks;
+        const int kb0 = c * kBlocksPerChunk;
+        const int nb = min(kBlocksPerChunk, p.nk - kb0);
+        mbar_expect_tx(full_bar(j), static_cast<uint32_t>(nb) * (kBM + N) * kRowBytes);
+        for (int b = 0; b < nb; ++b)
+          tma_load_2d(sA(j) + b * kBM * kRowBytes, &tmW, (kb0 + b) * kElems, vt * kBM,
+                      full_bar(j), pol_w);
+      }
+      grid_dep_wait();
       uint32_t stage = 0, phase = 0, outstanding = 0, out_par = 0;
       bool ok = true;
+      int j = 0;                     // chunks issued by this CTA
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const int vt = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
-        for (int c = 0; c < p.n_chunks; ++c) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          outstanding &= ~(1u << stage);
+        for (int c = 0; c < p.n_chunks; ++c, ++j) {
           const int kb0 = c * kBlocksPerChunk;
           const int nb = min(kBlocksPerChunk, p.nk - kb0);
-          mbar_arrive_expect_tx(full_bar(stage), static_cast<uint32_t>(nb) *
-                                                     (kBM + N) * kRowBytes);
-          for (int b = 0; b < nb; ++b) {
-            tma_load_2d(sA(stage) + b * kBM * kRowBytes, &tmW, (kb0 + b) * kElems, vt * kBM,
-                        full_bar(stage), pol_w);
-            tma_load_2d(sB(stage) + b * N * kRowBytes, &tmH, (kb0 + b) * kElems, nt * N,
-                        full_bar(stage), pol_h);
+          if (j < pre) {             // W already requested: add the hidden rows
+            for (int b = 0; b < nb; ++b)
+              tma_load_2d(sB(stage) + b * N * kRowBytes, &tmH, (kb0 + b) * kElems, nt * N,
+                          full_bar(stage), pol_h);
+            mbar_arrive(full_bar(stage));
+          } else {
+            if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(full_bar(stage), static_cast<uint32_t>(nb) *
+                                                       (kBM + N) * kRowBytes);
+            for (int b = 0; b < nb; ++b) {
+              tma_load_2d(sA(stage) + b * kBM * kRowBytes, &tmW, (kb0 + b) * kElems, vt * kBM,
+                          full_bar(stage), pol_w);
+              tma_load_2d(sB(stage) + b * N * kRowBytes, &tmH, (kb0 + b) * kElems, nt * N,
+                          full_bar(stage), pol_h);
+            }
           }
-          outstanding |= 1u << stage;
+          outstanding = (outstanding & ~(1u << stage)) | (1u << stage);
           out_par = (out_par & ~(1u << stage)) | (phase << stage);
           if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
         }
@@ -373,6 +397,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
     __syncwarp();
   } else {
     // --------------------------------------------------------- epilogue
+    grid_dep_wait();          // outputs and records: only after the previous kernels
     const int q = warp & 3;                    // TMEM lane quadrant of this warp
     const int et = threadIdx.x - 64;           // 0..127
     const int row = q * 32 + lane;             // vocabulary row within the tile
@@ -484,7 +509,6 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
 
   tc_fence_before();
   __syncthreads();
-  grid_dep_launch();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, p.tmem_cols);
@@ -504,8 +528,8 @@ __device__ __forceinline__ float gap_ulp_bf16(float m, float s) {
 
 template <int MODE>
 __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
+  grid_dep_launch(); // the next call's kernel 1 may start (it prefetches only W)
   grid_dep_wait();   // records of kernel 1 are complete and visible
-  grid_dep_launch(); // the next call's kernel 1 may start its prologue
   const int lane = threadIdx.x & 31;
   const int n = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (n >= p.B) return;
