@@ -233,7 +233,9 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    spec = WORKLOADS[args.workload]
+    spec = dict(WORKLOADS[args.workload])
+    if args.workload == "int8" and args.batch >= 256:
+        spec["bound"] = "tensor"     # fp16-rate tensor-core path, compute-bound
     c = make_inputs(args.workload, args.batch)
     fmt, V, d = c["dtype"], c["V"], c["d"]
     tdt = {"bf16": torch.bfloat16, "fp16": torch.float16, "int8": torch.int8}[fmt]
@@ -380,6 +382,14 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": traffic, "kernel": "head_gemm_kernel",
                      "kernel_us_per_launch": round(avg_kernel_s * 1e6, 2),
                      "timed_launches": int(kms.size),
+                     "steady_us_per_call": round(elapsed_ms * 1e3 / (args.steps * n_calls), 2),
+                     "steady_frac": round((by_launch if spec["bound"] == "hbm" else fl_launch) /
+                                          (elapsed_ms / 1e3 / (args.steps * n_calls)) /
+                                          (1e9 if spec["bound"] == "hbm" else 1e12) / peak, 4),
+                     "note": "achieved/frac: the projection kernel alone, bracketed by events on "
+                             "every event_every-th call (a bracketed call cannot overlap the "
+                             "previous call); steady_*: all calls of the timed region, both "
+                             "kernels, back to back",
                      "algorithmic_bytes_per_launch": int(by_launch),
                      "algorithmic_flops_per_launch": fl_launch,
                      "peak_source": f"MEASURED_PEAKS.json ({peaks['source']}, "
