@@ -82,10 +82,10 @@ bool encode_2d(CUtensorMap* m, int dtype, const void* base, int64_t d, int64_t r
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Hidden rows per MMA (N): B rounded up to 16, at most 128. Larger B is
-// covered by several column tiles. The result of a row does not depend on N.
+// Hidden rows per MMA (N): B rounded up to 16 up to 128; above that 256
+// (several column tiles past 256). The result of a row does not depend on N.
 int cols_for(int64_t B) {
-  if (B >= kMaxN) return kMaxN;
+  if (B > 128) return 256;
   const int n = static_cast<int>((B + 15) / 16) * 16;
   return n < 16 ? 16 : n;
 }
@@ -158,13 +158,20 @@ template <int MODE, int NBLK>
 cudaError_t launch_gemm_n(const CUtensorMap& tmW, const CUtensorMap& tmH, const HeadParams& p,
                           int grid, size_t smem, cudaStream_t stream) {
   auto kern = head_gemm_kernel<MODE, NBLK>;
+  if constexpr (threads_for(16 * NBLK) == 384) {
+    // the kernel's register split assumes exactly this launch budget
+    cudaFuncAttributes fa;
+    cudaError_t e0 = cudaFuncGetAttributes(&fa, kern);
+    if (e0 != cudaSuccess) return e0;
+    if (fa.numRegs != kRegsLaunchWide) return cudaErrorInvalidConfiguration;
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_for(16 * NBLK));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -187,6 +194,7 @@ cudaError_t launch_gemm(const CUtensorMap& tmW, const CUtensorMap& tmH, const He
     case 6: return launch_gemm_n<MODE, 6>(tmW, tmH, p, grid, smem, stream);
     case 7: return launch_gemm_n<MODE, 7>(tmW, tmH, p, grid, smem, stream);
     case 8: return launch_gemm_n<MODE, 8>(tmW, tmH, p, grid, smem, stream);
+    case 16: return launch_gemm_n<MODE, 16>(tmW, tmH, p, grid, smem, stream);
     default: return cudaErrorInvalidValue;
   }
 }

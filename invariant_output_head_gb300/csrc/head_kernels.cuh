@@ -52,9 +52,7 @@ namespace detlm {
 
 constexpr int kBM = 128;          // vocabulary rows per tile = MMA M = TMEM lanes
 constexpr int kRowBytes = 128;    // bytes of K per stage and tile row (one swizzle row)
-constexpr int kThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kEpiThreads = 128;
-constexpr int kMaxN = 128;        // largest MMA N (running sums live in registers)
+constexpr int kMaxN = 256;        // largest MMA N
 constexpr int kChunkK = 128;      // K elements per accumulation chunk
 constexpr int kBlocksPerChunk = kChunkK / 64;   // 128-byte K blocks of 16-bit data
 constexpr int kMaxStages = 12;
@@ -187,56 +185,80 @@ __device__ __forceinline__ int brev4(int l) {
   return ((l & 1) << 3) | ((l & 2) << 1) | ((l & 4) >> 1) | ((l & 8) >> 3);
 }
 
-// Barrier over the 128 epilogue threads that also ORs a predicate, so every
-// thread takes the same branch afterwards.
-__device__ __forceinline__ bool epi_bar_or(bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, 128, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r) : "r"(static_cast<uint32_t>(pred)) : "memory");
-  return r != 0;
-}
-
 // ----------------------------------------------------------- shared layout
+// Up to N = 128 a pipeline stage holds one whole K chunk (two 128-byte K
+// boxes) and four epilogue warps (warps 2..5) hold the running sums. At
+// N = 256 a stage holds one K box (so that four stages still fit) and eight
+// epilogue warps (warpgroups 1 and 2, two warps per TMEM lane quadrant) hold
+// 128 columns each; warpgroup 0 (producer, MMA issuer, two idle warps) gives
+// registers to them: launched at 168 per thread, 40 for warpgroup 0 and 232
+// for the epilogue (128 * 40 + 256 * 232 = 384 * 168).
+__host__ __device__ constexpr int epi_warps_for(int N) { return N > 128 ? 8 : 4; }
+__host__ __device__ constexpr int epi_first_warp(int N) { return N > 128 ? 4 : 2; }
+__host__ __device__ constexpr int kblocks_per_stage(int N) { return N > 128 ? 1 : 2; }
+__host__ __device__ constexpr int threads_for(int N) { return N > 128 ? 384 : 192; }
+constexpr int kRegsLaunchWide = 168;   // registers per thread at launch, N = 256
+constexpr int kRegsWg0Wide = 40;
+constexpr int kRegsEpiWide = 232;
+static_assert(128 * kRegsWg0Wide + 256 * kRegsEpiWide == 384 * kRegsLaunchWide,
+              "register split must equal the launch budget");
+
 struct SmemLayout {
   uint32_t a_bytes, b_bytes, stage_bytes, ctrl_off, red_off, xp_off, total;
 };
 
-// One pipeline stage holds one K chunk: kBlocksPerChunk 128-byte K boxes of
-// the W tile (each [128 rows x 128 B], swizzled) followed by as many boxes of
-// the hidden-row tile ([N rows x 128 B] each).
+// Stage s: kblocks_per_stage 128-byte K boxes of the W tile (each [128 rows x
+// 128 B], swizzled) followed by as many boxes of the hidden-row tile
+// ([N rows x 128 B] each).
 __host__ __device__ inline SmemLayout smem_layout(int N, int stages) {
   SmemLayout L;
-  L.a_bytes = kBlocksPerChunk * kBM * kRowBytes;
-  L.b_bytes = kBlocksPerChunk * static_cast<uint32_t>(N) * kRowBytes;
+  const uint32_t kps = static_cast<uint32_t>(kblocks_per_stage(N));
+  L.a_bytes = kps * kBM * kRowBytes;
+  L.b_bytes = kps * static_cast<uint32_t>(N) * kRowBytes;
   L.stage_bytes = L.a_bytes + L.b_bytes;
   L.ctrl_off = static_cast<uint32_t>(stages) * L.stage_bytes;
   // barriers: full[S], empty[S], slot_full[kMaxSlots], slot_empty[kMaxSlots],
   // never, drain; then the TMEM address holder and the abort flag
   L.red_off = L.ctrl_off + (2u * stages + 2u * kMaxSlots + 2u) * 8u + 16u;
   // per-quadrant column results: 3 words x 4 quadrants x N columns, then
-  // the four epilogue warps' transpose areas
+  // the epilogue warps' transpose areas
   L.xp_off = L.red_off + 3u * 4u * static_cast<uint32_t>(N) * 4u;
-  L.total = L.xp_off + 4u * kXpWords * 4u;
+  L.total = L.xp_off + static_cast<uint32_t>(epi_warps_for(N)) * kXpWords * 4u;
   return L;
+}
+
+// Barrier over the epilogue threads (barrier 1) that also ORs a predicate, so
+// every thread takes the same branch afterwards.
+template <int COUNT>
+__device__ __forceinline__ bool epi_bar_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r) : "r"(static_cast<uint32_t>(pred)), "n"(COUNT) : "memory");
+  return r != 0;
 }
 
 // ----------------------------------------------------------------- kernel 1
 template <int MODE, int NBLK>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(16 * NBLK), 1)
 head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                  const __grid_constant__ CUtensorMap tmH, const HeadParams p) {
-  static_assert(NBLK >= 1 && NBLK * 16 <= kMaxN, "N = 16 * NBLK");
+  constexpr int N = 16 * NBLK;
+  constexpr int EW = epi_warps_for(N);          // epilogue warps
+  constexpr int ET = 32 * EW;                   // epilogue threads
+  constexpr int KPS = kblocks_per_stage(N);     // K boxes per stage
+  constexpr int WBLK = NBLK / (EW / 4);         // 16-column blocks per epilogue warp
+  constexpr int E0 = epi_first_warp(N);         // first epilogue warp
+  static_assert(N <= kMaxN && NBLK % (EW / 4) == 0 && kBlocksPerChunk % KPS == 0, "shape");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = p.stages;
-  constexpr int N = 16 * NBLK;
   const SmemLayout L = smem_layout(N, S);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.ctrl_off);
@@ -265,7 +287,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
     }
     for (int b = 0; b < p.n_slots; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 4);
+      mbar_init(acce_bar(b), EW);
     }
     mbar_init(never_bar, 1);
     mbar_init(drain_bar, 1);
@@ -290,23 +312,25 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   const uint32_t tmem_base = *tmem_holder;
   const int n_units = p.n_vt * p.n_nt;
   const int kElems = kRowBytes / 2;     // 16-bit elements per 128-byte row
+  const int spu = (p.nk + KPS - 1) / KPS;   // stages per unit
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
+    if constexpr (EW == 8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegsWg0Wide));
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_h = policy_evict_last();
       // W is read-only for the life of the head, so the W boxes of the first
-      // S chunks are requested before waiting for the previous kernels; the
+      // S stages are requested before waiting for the previous kernels; the
       // hidden rows (which a previous kernel may write) only after.
       const int n_my = (n_units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                        static_cast<int>(gridDim.x);
-      const int pre = min(S, n_my > 0 ? n_my * p.n_chunks : 0);
+      const int pre = min(S, n_my > 0 ? n_my * spu : 0);
       for (int j = 0; j < pre; ++j) {
-        const int u = blockIdx.x + (j / p.n_chunks) * gridDim.x;
-        const int vt = u / p.n_nt, c = j - (j / p.n_chunks) * p.n_chunks;
-        const int kb0 = c * kBlocksPerChunk;
-        const int nb = min(kBlocksPerChunk, p.nk - kb0);
+        const int u = blockIdx.x + (j / spu) * gridDim.x;
+        const int vt = u / p.n_nt, st = j - (j / spu) * spu;
+        const int kb0 = st * KPS;
+        const int nb = min(KPS, p.nk - kb0);
         mbar_expect_tx(full_bar(j), static_cast<uint32_t>(nb) * (kBM + N) * kRowBytes);
         for (int b = 0; b < nb; ++b)
           tma_load_2d(sA(j) + b * kBM * kRowBytes, &tmW, (kb0 + b) * kElems, vt * kBM,
@@ -315,12 +339,12 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       grid_dep_wait();
       uint32_t stage = 0, phase = 0, outstanding = 0, out_par = 0;
       bool ok = true;
-      int j = 0;                     // chunks issued by this CTA
+      int j = 0;                     // stages issued by this CTA
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const int vt = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
-        for (int c = 0; c < p.n_chunks; ++c, ++j) {
-          const int kb0 = c * kBlocksPerChunk;
-          const int nb = min(kBlocksPerChunk, p.nk - kb0);
+        for (int st = 0; st < spu; ++st, ++j) {
+          const int kb0 = st * KPS;
+          const int nb = min(KPS, p.nk - kb0);
           if (j < pre) {             // W already requested: add the hidden rows
             for (int b = 0; b < nb; ++b)
               tma_load_2d(sB(stage) + b * N * kRowBytes, &tmH, (kb0 + b) * kElems, nt * N,
@@ -340,7 +364,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                           full_bar(stage), pol_h);
             }
           }
-          outstanding = (outstanding & ~(1u << stage)) | (1u << stage);
+          outstanding |= 1u << stage;
           out_par = (out_par & ~(1u << stage)) | (phase << stage);
           if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
         }
@@ -358,6 +382,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
+    if constexpr (EW == 8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegsWg0Wide));
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
@@ -368,18 +393,24 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           if (!mbar_wait(acce_bar(slot), sph ^ 1u, abort_flag, p.timeout_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + slot * static_cast<uint32_t>(N);
-          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.timeout_ns)) { ok = false; break; }
-          tc_fence_after();
-          const int nb = min(kBlocksPerChunk, p.nk - c * kBlocksPerChunk);
-          for (int b = 0; b < nb; ++b) {
-            const uint64_t da = sdesc_sw128(sA(stage) + b * kBM * kRowBytes);
-            const uint64_t db = sdesc_sw128(sB(stage) + b * N * kRowBytes);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)   // K = 16 per MMA: 32 bytes = 2 descriptor units
-              mma_f16(d_tmem, da + 2u * k, db + 2u * k, p.idesc, (b != 0) || (k != 0));
+          for (int sc = 0; sc < kBlocksPerChunk / KPS; ++sc) {
+            const int kb0 = c * kBlocksPerChunk + sc * KPS;
+            if (kb0 >= p.nk) break;
+            if (!mbar_wait(full_bar(stage), phase, abort_flag, p.timeout_ns)) { ok = false; break; }
+            tc_fence_after();
+            const int nb = min(KPS, p.nk - kb0);
+            for (int b = 0; b < nb; ++b) {
+              const uint64_t da = sdesc_sw128(sA(stage) + b * kBM * kRowBytes);
+              const uint64_t db = sdesc_sw128(sB(stage) + b * N * kRowBytes);
+              const bool first = (kb0 + b) == c * kBlocksPerChunk;
+#pragma unroll
+              for (int k = 0; k < 4; ++k)   // K = 16 per MMA: 32 bytes = 2 descriptor units
+                mma_f16(d_tmem, da + 2u * k, db + 2u * k, p.idesc, !(first && k == 0));
+            }
+            mma_commit(empty_bar(stage));
+            if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
           }
-          mma_commit(empty_bar(stage));
-          if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
           if (!ok) break;
           mma_commit(accf_bar(slot));
           if (++slot == static_cast<uint32_t>(p.n_slots)) { slot = 0; sph ^= 1u; }
@@ -395,18 +426,21 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       mbar_wait(drain_bar, 0, &zero, p.timeout_ns);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= E0) {
     // --------------------------------------------------------- epilogue
+    if constexpr (EW == 8) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(kRegsEpiWide));
     grid_dep_wait();          // outputs and records: only after the previous kernels
     const int q = warp & 3;                    // TMEM lane quadrant of this warp
-    const int et = threadIdx.x - 64;           // 0..127
+    const int g = (warp - E0) >> 2;            // column half (eight epilogue warps)
+    const int et = threadIdx.x - 32 * E0;      // 0 .. ET-1
     const int row = q * 32 + lane;             // vocabulary row within the tile
     const uint32_t tlane = static_cast<uint32_t>(q * 32) << 16;
+    float* xp = xpose + (warp - E0) * kXpWords;
     uint32_t slot = 0, sph = 0;
     bool failed = false;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       const int vt = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
-      float acc[NBLK][16];
+      float acc[WBLK][16];
       for (int c = 0; c < p.n_chunks; ++c) {
         const uint32_t cur = slot, cph = sph;
         if (++slot == static_cast<uint32_t>(p.n_slots)) { slot = 0; sph ^= 1u; }
@@ -416,9 +450,10 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
         }
         if (failed) continue;
         tc_fence_after();
-        const uint32_t sbase = tmem_base + tlane + cur * static_cast<uint32_t>(N);
+        const uint32_t sbase = tmem_base + tlane + cur * static_cast<uint32_t>(N) +
+                               static_cast<uint32_t>(g * WBLK * 16);
 #pragma unroll
-        for (int bb = 0; bb < NBLK; ++bb) {
+        for (int bb = 0; bb < WBLK; ++bb) {
           uint32_t r[16];
           tmem_ld16(sbase + bb * 16, r);
           tmem_wait_ld();
@@ -434,7 +469,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
         __syncwarp();
         if (lane == 0) mbar_arrive(acce_bar(cur));
       }
-      if (epi_bar_or(failed || *abort_flag)) {
+      if (epi_bar_or<ET>(failed || *abort_flag)) {
         if (et == 0) { *abort_flag = 1; atomicOr(p.err, ERR_TIMEOUT); }
         break;
       }
@@ -442,8 +477,8 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       const bool vok = v < p.V;
       const int n0 = nt * N;
 #pragma unroll
-      for (int bb = 0; bb < NBLK; ++bb) {
-        const int c0 = bb * 16;
+      for (int bb = 0; bb < WBLK; ++bb) {
+        const int c0 = (g * WBLK + bb) * 16;
         if (p.logits != nullptr && vok) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -451,7 +486,6 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
             if (n < p.B) p.logits[static_cast<size_t>(n) * p.V + v] = acc[bb][i];
           }
         }
-        float* xp = xpose + q * kXpWords;
 #pragma unroll
         for (int i = 0; i < 16; ++i) xp[lane * kXpStride + i] = vok ? acc[bb][i] : -INFINITY;
         __syncwarp();
@@ -478,9 +512,9 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
         }
         __syncwarp();
       }
-      named_bar_sync(1, kEpiThreads);
+      named_bar_sync(1, ET);
       // fixed combination of the four 32-row quadrants: (q0 . q1) . (q2 . q3)
-      for (int c = et; c < N; c += kEpiThreads) {
+      for (int c = et; c < N; c += ET) {
         const int n = n0 + c;
         if (n >= p.B) continue;
         const size_t o = static_cast<size_t>(vt) * p.B + n;
@@ -502,9 +536,12 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           p.rec_s[o] = r.S;
         }
       }
-      named_bar_sync(1, kEpiThreads);
+      named_bar_sync(1, ET);
     }
     if (failed && et == 0) atomicOr(p.err, ERR_TIMEOUT);
+  } else {
+    // warps 2 and 3 of warpgroup 0 (N = 256 only): no role, fewer registers
+    if constexpr (EW == 8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegsWg0Wide));
   }
 
   tc_fence_before();

@@ -328,7 +328,7 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
       const int vt = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
       const uint32_t buf = j & 1, aph = (j >> 1) & 1;
       const bool got = mbar_wait(accf(buf), aph, abort_flag, p.timeout_ns);
-      if (epi_bar_or(!got || *abort_flag)) {
+      if (epi_bar_or<128>(!got || *abort_flag)) {
         if (et == 0) { *abort_flag = 1; atomicOr(p.err, ERR_TIMEOUT); }
         break;
       }
@@ -374,8 +374,8 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         }
         __syncwarp();
       }
-      named_bar_sync(1, kEpiThreads);
-      for (int c = et; c < N; c += kEpiThreads) {
+      named_bar_sync(1, 128);
+      for (int c = et; c < N; c += 128) {
         const int n = n0 + c;
         if (n >= p.B) continue;
         ITop2 t[4];
@@ -387,7 +387,7 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         p.rec_i[o] = r.i;
         p.rec_s[o] = r.s;
       }
-      named_bar_sync(1, kEpiThreads);
+      named_bar_sync(1, 128);
     }
   }
 

@@ -122,7 +122,8 @@ def test_reserved_workspace_and_tiles(env):
     b.detlm_head_reserve(head.handle, 300)
     assert head.tiles(1) == (8, 16)
     assert head.tiles(17) == (8, 32)
-    assert head.tiles(300) == (8, 128)
+    assert head.tiles(128) == (8, 128)
+    assert head.tiles(300) == (8, 256)
     t, g, _ = head.greedy(dev(case["h"], "bf16"))
     z_ref, A = oracle_float_rows(case["W"], case["h"], "bf16")
     check_float_greedy(z_ref, A, host(t), host(g), label="reserved")
