@@ -220,9 +220,9 @@ __host__ __device__ inline SmemLayout smem_layout(int N, int stages) {
   // barriers: full[S], empty[S], slot_full[kMaxSlots], slot_empty[kMaxSlots],
   // never, drain; then the TMEM address holder and the abort flag
   L.red_off = L.ctrl_off + (2u * stages + 2u * kMaxSlots + 2u) * 8u + 16u;
-  // per-quadrant column results: 3 words x 4 quadrants x N columns, then
-  // the epilogue warps' transpose areas
-  L.xp_off = L.red_off + 3u * 4u * static_cast<uint32_t>(N) * 4u;
+  // per-quadrant column results: 3 words x 4 quadrants x N columns, the
+  // unit's target rows (N words), then the epilogue warps' transpose areas
+  L.xp_off = L.red_off + 3u * 4u * static_cast<uint32_t>(N) * 4u + static_cast<uint32_t>(N) * 4u;
   L.total = L.xp_off + static_cast<uint32_t>(epi_warps_for(N)) * kXpWords * 4u;
   return L;
 }
@@ -275,6 +275,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   float* red_m = reinterpret_cast<float*>(smem + L.red_off);
   int32_t* red_i = reinterpret_cast<int32_t*>(red_m + 4 * N);
   float* red_s = reinterpret_cast<float*>(red_i + 4 * N);
+  int* tgt_row = reinterpret_cast<int*>(red_s + 4 * N);   // log-prob: target row in tile, or -1
   float* xpose = reinterpret_cast<float*>(smem + L.xp_off);
   const uint32_t smem_base = smem_u32(smem);
   auto sA = [&](int s) { return smem_base + static_cast<uint32_t>(s) * L.stage_bytes; };
@@ -476,6 +477,16 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       const int v = vt * kBM + row;
       const bool vok = v < p.V;
       const int n0 = nt * N;
+      if constexpr (MODE == MODE_LOGPROB) {
+        // stage each column's target row within this tile once (the barrier
+        // after the folds below orders these writes before the reads)
+        for (int c = et; c < N; c += ET) {
+          const int n = n0 + c;
+          const int t = n < p.B ? p.targets[n] - vt * kBM : -1;
+          tgt_row[c] = (t >= 0 && t < kBM) ? t : -1;
+        }
+        named_bar_sync(1, ET);
+      }
 #pragma unroll
       for (int bb = 0; bb < WBLK; ++bb) {
         const int c0 = (g * WBLK + bb) * 16;
@@ -497,13 +508,9 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
             red_s[q * N + c0 + lane] = t.s;
           }
         } else {
-          if (vok) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int n = n0 + c0 + i;
-              if (n < p.B && p.targets[n] == v) p.zt[n] = acc[bb][i];
-            }
-          }
+          for (int i = 0; i < 16; ++i)
+            if (tgt_row[c0 + i] == row) p.zt[n0 + c0 + i] = acc[bb][i];
           const Lse t = xp_lse(xp, lane);
           if (lane < 16) {
             red_m[q * N + c0 + lane] = t.m;
