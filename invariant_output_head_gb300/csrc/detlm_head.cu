@@ -35,6 +35,12 @@ struct detlm_head {
   // device staging for the *_host calls
   void* stage = nullptr;
   size_t stage_bytes = 0;
+  // integer head, wide batches: fp16 copy of W (made at the first such call)
+  // and the call's hidden rows in fp16
+  void* W16 = nullptr;
+  CUtensorMap tmW16;
+  void* h16 = nullptr;
+  size_t h16_bytes = 0;
   // test hook and timing hook
   int stall = 0;
   uint64_t timeout_ns = 2000000000ull;
@@ -274,8 +280,116 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   return status_from_cuda(e);
 }
 
+// Integer head, B >= kI8WideB: the projection kernel of the float heads on
+// exact fp16 copies of the int8 values (MODE_INT), which is compute-bound
+// there; the int8-streaming kernel serves smaller batches. Both are exact,
+// so every B gives the same bits.
+constexpr int64_t kI8WideB = 256;
+
+cudaError_t i8_to_f16(const void* in, void* out, size_t n, cudaStream_t stream) {
+  const size_t n16 = n / 16;
+  size_t blocks = (n16 + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks == 0) blocks = 1;
+  i8_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const uint4*>(in), static_cast<uint4*>(out), n16);
+  return cudaGetLastError();
+}
+
+int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token, int32_t* gap,
+                     int32_t* logits, cudaStream_t stream) {
+  cudaError_t e;
+  if (h->W16 == nullptr) {
+    const size_t n = static_cast<size_t>(h->V) * h->d;
+    void* w16 = nullptr;
+    e = cudaMalloc(&w16, n * 2);
+    if (e != cudaSuccess) return status_from_cuda(e);
+    e = i8_to_f16(h->W, w16, n, stream);
+    if (e != cudaSuccess || !encode_2d(&h->tmW16, DETLM_FP16, w16, h->d, h->V, kBM)) {
+      cudaFree(w16);
+      return e != cudaSuccess ? status_from_cuda(e) : DETLM_EINVAL;
+    }
+    h->W16 = w16;
+  }
+  const size_t hb = static_cast<size_t>(B) * h->d * 2;
+  if (hb > h->h16_bytes) {
+    if (h->h16 != nullptr) {
+      e = cudaStreamSynchronize(stream);
+      if (e != cudaSuccess) return status_from_cuda(e);
+      cudaFree(h->h16);
+      h->h16 = nullptr;
+      h->h16_bytes = 0;
+    }
+    e = cudaMalloc(&h->h16, hb);
+    if (e != cudaSuccess) return status_from_cuda(e);
+    h->h16_bytes = hb;
+  }
+  e = i8_to_f16(h_dev, h->h16, static_cast<size_t>(B) * h->d, stream);
+  if (e != cudaSuccess) return status_from_cuda(e);
+  const int N = cols_for(B);
+  CUtensorMap tmH;
+  if (!encode_2d(&tmH, DETLM_FP16, h->h16, h->d, B, static_cast<uint32_t>(N))) return DETLM_EINVAL;
+  int st = ensure_ws(h, B, stream);
+  if (st != DETLM_OK) return st;
+  const WsView w = ws_view(h, B);
+
+  HeadParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.V = static_cast<int32_t>(h->V);
+  p.d = static_cast<int32_t>(h->d);
+  p.B = static_cast<int32_t>(B);
+  p.N = N;
+  p.n_vt = h->n_vt;
+  p.n_nt = static_cast<int32_t>((B + N - 1) / N);
+  p.nk = static_cast<int32_t>((h->d * 2 + kRowBytes - 1) / kRowBytes);
+  p.n_chunks = static_cast<int32_t>((h->d + kChunkK - 1) / kChunkK);
+  p.n_slots = slots_for(N);
+  p.stages = stages_for(N);
+  p.tmem_cols = tmem_cols_for(p.n_slots * N);
+  p.idesc = idesc_f16(0u, kBM, static_cast<uint32_t>(N));
+  p.logits = reinterpret_cast<float*>(logits);
+  p.rec_m = w.m;
+  p.rec_i = w.i;
+  p.rec_s = w.s;
+  p.err = h->d_err;
+  p.stall = h->stall;
+  p.timeout_ns = h->timeout_ns;
+  const size_t smem = smem_layout(N, p.stages).total + 1024;
+  const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
+  const int grid = static_cast<int>(units < h->num_sms ? units : h->num_sms);
+  if (h->t_start) cudaEventRecord(h->t_start, stream);
+  e = launch_gemm<MODE_INT>(h->tmW16, tmH, p, grid, smem, stream);
+  if (h->t_stop) {
+    cudaEventRecord(h->t_stop, stream);
+    h->t_start = h->t_stop = nullptr;
+  }
+  if (e != cudaSuccess) return status_from_cuda(e);
+
+  Int8MergeParams mp;
+  mp.B = p.B;
+  mp.n_vt = p.n_vt;
+  mp.rec_m = reinterpret_cast<const int32_t*>(w.m);
+  mp.rec_i = w.i;
+  mp.rec_s = reinterpret_cast<const int32_t*>(w.s);
+  mp.token = token;
+  mp.gap = gap;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>((B + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, int8_merge_kernel, mp);
+  return status_from_cuda(e);
+}
+
 int launch_int8(detlm_head* h, const void* h_dev, int64_t B, int32_t* token, int32_t* gap,
                 int32_t* logits, cudaStream_t stream) {
+  if (B >= kI8WideB) return launch_int8_wide(h, h_dev, B, token, gap, logits, stream);
   const int N = int8_cols_for(B, h->d);
   CUtensorMap tmH;
   if (!encode_2d(&tmH, DETLM_INT8, h_dev, h->d, B, static_cast<uint32_t>(N))) return DETLM_EINVAL;
@@ -549,13 +663,15 @@ int detlm_head_debug(detlm_head_t* h, int flags, uint64_t timeout_ns) {
 int detlm_head_tiles(const detlm_head_t* h, int64_t B, int32_t* n_vtiles, int32_t* n_cols) {
   if (h == nullptr || bad_B(B) || n_vtiles == nullptr || n_cols == nullptr) return DETLM_EINVAL;
   *n_vtiles = h->n_vt;
-  *n_cols = h->dtype == DETLM_INT8 ? int8_cols_for(B, h->d) : cols_for(B);
+  *n_cols = (h->dtype == DETLM_INT8 && B < kI8WideB) ? int8_cols_for(B, h->d) : cols_for(B);
   return DETLM_OK;
 }
 
 void detlm_head_destroy(detlm_head_t* h) {
   if (h == nullptr) return;
   if (h->ws) cudaFree(h->ws);
+  if (h->W16) cudaFree(h->W16);
+  if (h->h16) cudaFree(h->h16);
   if (h->stage) cudaFree(h->stage);
   if (h->d_err) cudaFree(h->d_err);
   delete h;

@@ -46,6 +46,7 @@
 #include <cuda.h>
 #include <cstdint>
 #include <cmath>
+#include <type_traits>
 #include "ptx.cuh"
 
 namespace detlm {
@@ -59,7 +60,11 @@ constexpr int kMaxStages = 12;
 constexpr int kMaxSlots = 8;
 constexpr int kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
 
-enum : int { MODE_GREEDY = 0, MODE_LOGPROB = 1 };
+// MODE_INT: the integer head's wide-batch path. The int8 values of W and h
+// are held as fp16 (exact), every 128-element chunk sum is an integer below
+// 2^21 (exact in the fp32 accumulator) and the chunk sums are added in
+// int32; logits, records and the decision are int32.
+enum : int { MODE_GREEDY = 0, MODE_LOGPROB = 1, MODE_INT = 2 };
 enum : int { ERR_TIMEOUT = 1, ERR_TARGET = 2 };
 
 struct HeadParams {
@@ -98,6 +103,7 @@ struct MergeParams {
 
 // ------------------------------------------------------------ merge rules
 struct Top2 { float m; int32_t i; float s; };   // max, its lowest index, runner-up
+struct ITop2 { int32_t m; int32_t i; int32_t s; };  // the same for int32 logits
 struct Lse { float m; float S; };               // max, sum exp(z - max)
 
 // Top-2 of a multiset with index tie-break: exact, associative, commutative.
@@ -107,6 +113,15 @@ __device__ __forceinline__ Top2 top2_merge(const Top2& a, const Top2& b) {
   r.m = aw ? a.m : b.m;
   r.i = aw ? a.i : b.i;
   r.s = fmaxf(aw ? a.s : b.s, aw ? b.m : a.m);
+  return r;
+}
+
+__device__ __forceinline__ ITop2 itop2_merge(const ITop2& a, const ITop2& b) {
+  const bool aw = (a.m > b.m) || (a.m == b.m && a.i < b.i);
+  ITop2 r;
+  r.m = aw ? a.m : b.m;
+  r.i = aw ? a.i : b.i;
+  r.s = max(aw ? a.s : b.s, aw ? b.m : a.m);
   return r;
 }
 
@@ -123,6 +138,10 @@ __device__ __forceinline__ Lse lse_merge(const Lse& a, const Lse& b) {
 __device__ __forceinline__ Top2 shfl_xor(const Top2& x, int b) {
   return Top2{__shfl_xor_sync(0xffffffffu, x.m, b), __shfl_xor_sync(0xffffffffu, x.i, b),
               __shfl_xor_sync(0xffffffffu, x.s, b)};
+}
+__device__ __forceinline__ ITop2 shfl_xor(const ITop2& x, int b) {
+  return ITop2{__shfl_xor_sync(0xffffffffu, x.m, b), __shfl_xor_sync(0xffffffffu, x.i, b),
+               __shfl_xor_sync(0xffffffffu, x.s, b)};
 }
 __device__ __forceinline__ Lse shfl_xor(const Lse& x, int b) {
   return Lse{__shfl_xor_sync(0xffffffffu, x.m, b), __shfl_xor_sync(0xffffffffu, x.S, b)};
@@ -179,6 +198,26 @@ __device__ __forceinline__ Lse xp_lse(const float* xp, int lane) {
       sum = __fadd_rn(sum, __expf(xp[(h * 16 + j) * kXpStride + c] - m));
   }
   return lse_merge(Lse{m, sum}, shfl_xor(Lse{m, sum}, 16));
+}
+
+// integer head: exact (max, lowest row, runner-up); INT32_MIN marks rows
+// outside the vocabulary (|z| is far below 2^31)
+__device__ __forceinline__ ITop2 xp_itop2(const int32_t* xp, int lane, int v_row0) {
+  const int c = lane & 15, h = lane >> 4;
+  ITop2 t{INT32_MIN, INT32_MAX, INT32_MIN};
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int r = h * 16 + j;
+    const int32_t x = xp[r * kXpStride + c];
+    if (x > t.m) {
+      t.s = t.m;
+      t.m = x;
+      t.i = v_row0 + r;
+    } else {
+      t.s = max(t.s, x);
+    }
+  }
+  return itop2_merge(t, shfl_xor(t, 16));
 }
 
 __device__ __forceinline__ int brev4(int l) {
@@ -441,7 +480,8 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
     bool failed = false;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       const int vt = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
-      float acc[WBLK][16];
+      using Acc = typename std::conditional<MODE == MODE_INT, int32_t, float>::type;
+      Acc acc[WBLK][16];
       for (int c = 0; c < p.n_chunks; ++c) {
         const uint32_t cur = slot, cph = sph;
         if (++slot == static_cast<uint32_t>(p.n_slots)) { slot = 0; sph ^= 1u; }
@@ -458,7 +498,13 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           uint32_t r[16];
           tmem_ld16(sbase + bb * 16, r);
           tmem_wait_ld();
-          if (c == 0) {
+          if constexpr (MODE == MODE_INT) {   // exact integer chunk sums, int32 fold
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int32_t x = __float2int_rn(__uint_as_float(r[i]));
+              acc[bb][i] = (c == 0) ? x : acc[bb][i] + x;
+            }
+          } else if (c == 0) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) acc[bb][i] = __uint_as_float(r[i]);
           } else {
@@ -491,16 +537,30 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       for (int bb = 0; bb < WBLK; ++bb) {
         const int c0 = (g * WBLK + bb) * 16;
         if (p.logits != nullptr && vok) {
+          Acc* lg = reinterpret_cast<Acc*>(p.logits);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int n = n0 + c0 + i;
-            if (n < p.B) p.logits[static_cast<size_t>(n) * p.V + v] = acc[bb][i];
+            if (n < p.B) lg[static_cast<size_t>(n) * p.V + v] = acc[bb][i];
           }
         }
+        if constexpr (MODE == MODE_INT) {
+          int32_t* xpi = reinterpret_cast<int32_t*>(xp);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) xp[lane * kXpStride + i] = vok ? acc[bb][i] : -INFINITY;
+          for (int i = 0; i < 16; ++i) xpi[lane * kXpStride + i] = vok ? acc[bb][i] : INT32_MIN;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) xp[lane * kXpStride + i] = vok ? acc[bb][i] : -INFINITY;
+        }
         __syncwarp();
-        if constexpr (MODE == MODE_GREEDY) {
+        if constexpr (MODE == MODE_INT) {
+          const ITop2 t = xp_itop2(reinterpret_cast<const int32_t*>(xp), lane, vt * kBM + q * 32);
+          if (lane < 16) {
+            reinterpret_cast<int32_t*>(red_m)[q * N + c0 + lane] = t.m;
+            red_i[q * N + c0 + lane] = t.i;
+            reinterpret_cast<int32_t*>(red_s)[q * N + c0 + lane] = t.s;
+          }
+        } else if constexpr (MODE == MODE_GREEDY) {
           const Top2 t = xp_top2(xp, lane, vt * kBM + q * 32);
           if (lane < 16) {
             red_m[q * N + c0 + lane] = t.m;
@@ -525,7 +585,17 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
         const int n = n0 + c;
         if (n >= p.B) continue;
         const size_t o = static_cast<size_t>(vt) * p.B + n;
-        if constexpr (MODE == MODE_GREEDY) {
+        if constexpr (MODE == MODE_INT) {
+          const int32_t* rm = reinterpret_cast<const int32_t*>(red_m);
+          const int32_t* rs = reinterpret_cast<const int32_t*>(red_s);
+          ITop2 t[4];
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) t[qq] = ITop2{rm[qq * N + c], red_i[qq * N + c], rs[qq * N + c]};
+          const ITop2 r = itop2_merge(itop2_merge(t[0], t[1]), itop2_merge(t[2], t[3]));
+          reinterpret_cast<int32_t*>(p.rec_m)[o] = r.m;
+          p.rec_i[o] = r.i;
+          reinterpret_cast<int32_t*>(p.rec_s)[o] = r.s;
+        } else if constexpr (MODE == MODE_GREEDY) {
           Top2 t[4];
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq)

@@ -95,42 +95,6 @@ __host__ __device__ inline Int8Layout int8_layout(int N, int s8, int s16) {
   return L;
 }
 
-struct ITop2 { int32_t m; int32_t i; int32_t s; };
-
-__device__ __forceinline__ ITop2 itop2_merge(const ITop2& a, const ITop2& b) {
-  const bool aw = (a.m > b.m) || (a.m == b.m && a.i < b.i);
-  ITop2 r;
-  r.m = aw ? a.m : b.m;
-  r.i = aw ? a.i : b.i;
-  r.s = max(aw ? a.s : b.s, aw ? b.m : a.m);
-  return r;
-}
-__device__ __forceinline__ ITop2 shfl_xor(const ITop2& x, int b) {
-  return ITop2{__shfl_xor_sync(0xffffffffu, x.m, b), __shfl_xor_sync(0xffffffffu, x.i, b),
-               __shfl_xor_sync(0xffffffffu, x.s, b)};
-}
-
-// Exact top-2 of one 16-column block of int32 logits over a warp's 32 rows
-// through the warp's shared-memory transpose area (INT32_MIN marks rows
-// outside the vocabulary; |z| is far below 2^31).
-__device__ __forceinline__ ITop2 xp_itop2(const int32_t* xp, int lane, int v_row0) {
-  const int c = lane & 15, h = lane >> 4;
-  ITop2 t{INT32_MIN, INT32_MAX, INT32_MIN};
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int r = h * 16 + j;
-    const int32_t x = xp[r * kXpStride + c];
-    if (x > t.m) {
-      t.s = t.m;
-      t.m = x;
-      t.i = v_row0 + r;
-    } else {
-      t.s = max(t.s, x);
-    }
-  }
-  return itop2_merge(t, shfl_xor(t, 16));
-}
-
 // four int8 in one word -> two half2 holding the same integers exactly
 __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t u = w ^ 0x80808080u;             // bytes x + 128
@@ -142,6 +106,22 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t&
   const __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), k);
   lo = *reinterpret_cast<const uint32_t*>(&ha);
   hi = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
+// Elementwise int8 -> fp16 (exact) for the wide-batch integer path: n is a
+// multiple of 16 (rows of d % 16 == 0 elements).
+__global__ void i8_to_f16_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, size_t n16) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 w = in[i];
+    uint4 o0, o1;
+    i8x4_to_h2x2(w.x, o0.x, o0.y);
+    i8x4_to_h2x2(w.y, o0.z, o0.w);
+    i8x4_to_h2x2(w.z, o1.x, o1.y);
+    i8x4_to_h2x2(w.w, o1.z, o1.w);
+    out[2 * i] = o0;
+    out[2 * i + 1] = o1;
+  }
 }
 
 // Convert `rows` rows of a swizzled int8 tile (128 B per row) into the two

@@ -99,3 +99,22 @@ def test_int8_extreme_values_exact(torch_cuda):
     ref = oracle.head_greedy(W, h, "int8")
     assert (host(z).astype(np.int64) == ref["logits"]).all()
     assert (host(tok) == ref["token"]).all()
+
+
+@pytest.mark.parametrize("V,d", [(1000, 1040), (300, 4096), (129, 16)])
+def test_int8_wide_batch_path_exact(torch_cuda, V, d):
+    """B >= 256 runs the integer head on fp16 copies through the float
+    projection kernel; exact, so it must agree bit for bit with the oracle
+    and with the int8-streaming path used for small B."""
+    from invariant_output_head_gb300 import Head
+    case = synth.small_int8(500 + V, V, d, 300, n_ties=3, lo=-128, hi=127)
+    head = Head(dev(case["W"], "int8"), "int8")
+    h = dev(case["h"], "int8")
+    tok, gap, z = head.greedy(h, with_logits=True)
+    assert head.check() == 0
+    ref = oracle.head_greedy(case["W"], case["h"], "int8")
+    assert (host(z).astype(np.int64) == ref["logits"]).all()
+    assert (host(tok) == ref["token"]).all()
+    assert (host(gap).astype(np.int64) == np.minimum(ref["gap"], 2**31 - 1)).all()
+    t2, g2, z2 = head.greedy(h[:40], with_logits=True)      # narrow path
+    assert (host(z2) == host(z)[:40]).all() and (host(t2) == host(tok)[:40]).all()
