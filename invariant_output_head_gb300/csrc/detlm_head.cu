@@ -280,6 +280,28 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   return status_from_cuda(e);
 }
 
+template <int N>
+cudaError_t launch_int8_t(const CUtensorMap& tmW, const CUtensorMap& tmH, const Int8Params& p,
+                          int grid, size_t smem, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(int8_gemm_kernel<N>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int8_gemm_kernel<N><<<grid, kI8Threads, smem, stream>>>(tmW, tmH, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_int8_n(int N, const CUtensorMap& tmW, const CUtensorMap& tmH,
+                          const Int8Params& p, int grid, size_t smem, cudaStream_t stream) {
+  switch (N) {
+    case 16: return launch_int8_t<16>(tmW, tmH, p, grid, smem, stream);
+    case 32: return launch_int8_t<32>(tmW, tmH, p, grid, smem, stream);
+    case 48: return launch_int8_t<48>(tmW, tmH, p, grid, smem, stream);
+    case 64: return launch_int8_t<64>(tmW, tmH, p, grid, smem, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 // Integer head, B >= kI8WideB: the projection kernel of the float heads on
 // exact fp16 copies of the int8 values (MODE_INT), which is compute-bound
 // there; the int8-streaming kernel serves smaller batches. Both are exact,
@@ -426,14 +448,10 @@ int launch_int8(detlm_head* h, const void* h_dev, int64_t B, int32_t* token, int
   p.timeout_ns = h->timeout_ns;
 
   const size_t smem = int8_layout(N, p.s8, p.s16).total + 1024;
-  cudaError_t e = cudaFuncSetAttribute(int8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return status_from_cuda(e);
   const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
   const int grid = static_cast<int>(units < h->num_sms ? units : h->num_sms);
   if (h->t_start) cudaEventRecord(h->t_start, stream);
-  int8_gemm_kernel<<<grid, kI8Threads, smem, stream>>>(h->tmW, tmH, p);
-  e = cudaGetLastError();
+  cudaError_t e = launch_int8_n(N, h->tmW, tmH, p, grid, smem, stream);
   if (h->t_stop) {
     cudaEventRecord(h->t_stop, stream);
     h->t_start = h->t_stop = nullptr;

@@ -23,8 +23,8 @@
 // gives u = x + 128 in 0..255; the half with bits 0x6400 | u is 1024 + u;
 // subtracting 1152 (exact) leaves x.
 //
-// Warp roles (320 threads): warp 0 TMA of int8 tiles, warp 1 MMA issuer,
-// warps 2..5 epilogue, warps 6..9 converters (int8 ring -> fp16 ring in the
+// Warp roles (448 threads): warp 0 TMA of int8 tiles, warp 1 MMA issuer,
+// warps 2..5 epilogue, warps 6..13 converters (int8 ring -> fp16 ring in the
 // 128-byte swizzle layout the MMA descriptors expect).
 #pragma once
 #include <cuda.h>
@@ -36,7 +36,8 @@
 namespace detlm {
 
 constexpr int kI8Chunk = 1024;            // K elements per exact fp32 chunk
-constexpr int kI8Threads = 320;
+constexpr int kI8ConvWarps = 8;            // converter warps (warps 6 .. 13)
+constexpr int kI8Threads = 192 + 32 * kI8ConvWarps;
 constexpr int kI8MaxD = 16384;            // 16 chunks; keeps |logit| <= 2^28
 constexpr int kI8MaxStages8 = 8;
 constexpr int kI8MaxN = 64;               // keeps >= 5 int8 stages in shared memory
@@ -124,28 +125,42 @@ __global__ void i8_to_f16_kernel(const uint4* __restrict__ in, uint4* __restrict
   }
 }
 
-// Convert `rows` rows of a swizzled int8 tile (128 B per row) into the two
+// Convert ROWS rows of a swizzled int8 tile (128 B per row) into the two
 // swizzled fp16 sub-tiles (each 128 B per row) at dst (sub-tile 1 at
-// dst + rows * 128). Threads ct = 0..nthreads-1 share the 16-byte chunks.
-__device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int rows,
-                                             int ct, int nthreads) {
-  const int chunks = rows * 8;
-  for (int q = ct; q < chunks; q += nthreads) {
+// dst + ROWS * 128). The converter threads share the 16-byte chunks; the
+// trip count is a compile-time constant so all loads are issued before the
+// conversions (the loop was latency-bound otherwise).
+template <int ROWS>
+__device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int ct) {
+  constexpr int kNT = 32 * kI8ConvWarps;
+  constexpr int kIters = (ROWS * 8 + kNT - 1) / kNT;
+  uint4 w[kIters];
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    const int q = ct + it * kNT;
     const int r = q >> 3, c = q & 7;                       // row, logical 16-byte chunk
-    const uint4 w = *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ (r & 7)) << 4));
+    if (q < ROWS * 8)
+      w[it] = *reinterpret_cast<const uint4*>(src + r * 128 + ((c ^ (r & 7)) << 4));
+  }
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    const int q = ct + it * kNT;
+    if (q >= ROWS * 8) continue;
+    const int r = q >> 3, c = q & 7;
     uint4 o0, o1;
-    i8x4_to_h2x2(w.x, o0.x, o0.y);
-    i8x4_to_h2x2(w.y, o0.z, o0.w);
-    i8x4_to_h2x2(w.z, o1.x, o1.y);
-    i8x4_to_h2x2(w.w, o1.z, o1.w);
+    i8x4_to_h2x2(w[it].x, o0.x, o0.y);
+    i8x4_to_h2x2(w[it].y, o0.z, o0.w);
+    i8x4_to_h2x2(w[it].z, o1.x, o1.y);
+    i8x4_to_h2x2(w[it].w, o1.z, o1.w);
     // int8 elements 16c .. 16c+15 -> fp16 sub-tile c/4, chunks 2(c%4), 2(c%4)+1
-    uint8_t* sub = dst + (c >> 2) * rows * 128 + r * 128;
+    uint8_t* sub = dst + (c >> 2) * ROWS * 128 + r * 128;
     const int cc = (c & 3) * 2;
     *reinterpret_cast<uint4*>(sub + ((cc ^ (r & 7)) << 4)) = o0;
     *reinterpret_cast<uint4*>(sub + (((cc + 1) ^ (r & 7)) << 4)) = o1;
   }
 }
 
+template <int N_>
 __global__ void __launch_bounds__(kI8Threads, 1)
 int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
                  const Int8Params p) {
@@ -154,7 +169,8 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int S8 = p.s8, S16 = p.s16, N = p.N;
+  const int S8 = p.s8, S16 = p.s16;
+  constexpr int N = N_;
   const Int8Layout L = int8_layout(N, S8, S16);
 
   const uint32_t bar0 = smem_u32(smem + L.ctrl);
@@ -176,8 +192,8 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   const uint32_t base = smem_u32(smem);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S8; ++s) { mbar_init(f8full(s), 1); mbar_init(f8empty(s), 4); }
-    for (int s = 0; s < S16; ++s) { mbar_init(f16full(s), 4); mbar_init(f16empty(s), 1); }
+    for (int s = 0; s < S8; ++s) { mbar_init(f8full(s), 1); mbar_init(f8empty(s), kI8ConvWarps); }
+    for (int s = 0; s < S16; ++s) { mbar_init(f16full(s), kI8ConvWarps); mbar_init(f16empty(s), 1); }
     for (int b = 0; b < 2; ++b) { mbar_init(accf(b), 1); mbar_init(acce(b), 4); }
     mbar_init(never_bar, 1);
     mbar_init(drain_bar, 1);
@@ -272,7 +288,7 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     __syncwarp();
   } else if (warp >= 6) {
     // ------------------------------------------------------- converters
-    const int ct = threadIdx.x - 192;   // 0..127
+    const int ct = threadIdx.x - 192;   // 0 .. 32 * kI8ConvWarps - 1
     uint32_t s8 = 0, ph8 = 0, s16 = 0, ph16 = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -282,8 +298,8 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         if (!g2) { ok = false; break; }
         const uint8_t* src = smem + s8 * L.st8;
         uint8_t* dst = smem + L.off16 + s16 * L.st16;
-        convert_tile(src, dst, kBM, ct, 128);
-        convert_tile(src + L.a8, dst + L.a16, N, ct, 128);
+        convert_tile<kBM>(src, dst, ct);
+        convert_tile<N>(src + L.a8, dst + L.a16, ct);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
