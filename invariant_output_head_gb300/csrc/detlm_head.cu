@@ -123,7 +123,7 @@ int status_from_cuda(cudaError_t e) {
   return DETLM_ECUDA;
 }
 
-// workspace: rec_m, rec_i, rec_s [n_vt, B] and zt [B], 256-byte aligned parts
+// workspace: rec_m, rec_i, rec_s [B, n_vt] and zt [B], 256-byte aligned parts
 size_t ws_part(int64_t n) { return (static_cast<size_t>(n) * 4 + 255) & ~static_cast<size_t>(255); }
 size_t ws_bytes_for(const detlm_head* h, int64_t B) {
   return 3 * ws_part(static_cast<int64_t>(h->n_vt) * B) + ws_part(B);
@@ -267,8 +267,8 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   mp.err = h->d_err;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(static_cast<unsigned>((B + 3) / 4));
-  cfg.blockDim = dim3(128);
+  cfg.gridDim = dim3(static_cast<unsigned>(B));
+  cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -397,8 +397,8 @@ int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token
   mp.gap = gap;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(static_cast<unsigned>((B + 3) / 4));
-  cfg.blockDim = dim3(128);
+  cfg.gridDim = dim3(static_cast<unsigned>(B));
+  cfg.blockDim = dim3(kMergeThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -468,8 +468,8 @@ int launch_int8(detlm_head* h, const void* h_dev, int64_t B, int32_t* token, int
   mp.gap = gap;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(static_cast<unsigned>((B + 3) / 4));
-  cfg.blockDim = dim3(128);
+  cfg.gridDim = dim3(static_cast<unsigned>(B));
+  cfg.blockDim = dim3(kMergeThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -812,8 +812,8 @@ extern "C" int detlm_greedy_noalloc(const void* W_dev, int64_t V, int64_t d, int
   mp.err = err;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(static_cast<unsigned>((B + 3) / 4));
-  cfg.blockDim = dim3(128);
+  cfg.gridDim = dim3(static_cast<unsigned>(B));
+  cfg.blockDim = dim3(kMergeThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

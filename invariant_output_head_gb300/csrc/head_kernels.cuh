@@ -32,10 +32,11 @@
 //            exp(z - m_warp) are added in a fixed tree, then the four warps'
 //            (m, S) pairs merge in a fixed order.
 //
-// Kernel 2 (merge_kernel): one warp per hidden row folds the n_vt tile
-// records in a fixed order (lane l takes tiles l, l+32, ... in ascending
-// order, then a butterfly over lanes 1, 2, 4, 8, 16) -- a function of V only.
-// No atomics take part in any result.
+// Kernel 2 (merge_kernel): one 128-thread block per hidden row folds the
+// n_vt tile records in a fixed order that depends on V only: thread g folds
+// tiles g, g+128, g+256, ... in ascending order, then the 128 partial
+// results combine in a balanced binary tree over g (pairs g^1, g^2, ...,
+// g^64). No atomics take part in any result.
 //
 // Both reductions are written so that a row's bits do not depend on its
 // column position in the tile or on B: the greedy record is exact (a
@@ -79,9 +80,9 @@ struct HeadParams {
   uint32_t idesc;
   float* logits;            // optional fp32 [B, V]
   const int32_t* targets;   // logprob: [B]
-  float* rec_m;             // [n_vt, B] tile maximum
-  int32_t* rec_i;           // [n_vt, B] greedy: lowest index of the maximum
-  float* rec_s;             // [n_vt, B] greedy: runner-up; logprob: sum exp
+  float* rec_m;             // [B, n_vt] tile maximum
+  int32_t* rec_i;           // [B, n_vt] greedy: lowest index of the maximum
+  float* rec_s;             // [B, n_vt] greedy: runner-up; logprob: sum exp
   float* zt;                // [B] logprob: target logit
   int* err;                 // device error word
   int32_t stall;            // test hook: MMA issuer waits on a dead barrier
@@ -584,7 +585,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       for (int c = et; c < N; c += ET) {
         const int n = n0 + c;
         if (n >= p.B) continue;
-        const size_t o = static_cast<size_t>(vt) * p.B + n;
+        const size_t o = static_cast<size_t>(n) * p.n_vt + vt;   // records [B][n_vt]
         if constexpr (MODE == MODE_INT) {
           const int32_t* rm = reinterpret_cast<const int32_t*>(red_m);
           const int32_t* rs = reinterpret_cast<const int32_t*>(red_s);
@@ -640,40 +641,68 @@ __device__ __forceinline__ float gap_ulp_bf16(float m, float s) {
   return static_cast<float>((static_cast<double>(m) - static_cast<double>(s)) * scale);
 }
 
+// Balanced-tree combination of one value per thread over a 128-thread block
+// (levels g^1 .. g^16 by shuffles, then (w0 . w1) . (w2 . w3) across warps);
+// the result is valid in thread 0.
+template <typename T, typename M>
+__device__ __forceinline__ T block_tree128(T x, M merge_fn, T* smem4) {
+#pragma unroll
+  for (int b = 1; b < 32; b <<= 1) x = merge_fn(x, shfl_xor(x, b));
+  if ((threadIdx.x & 31) == 0) smem4[threadIdx.x >> 5] = x;
+  __syncthreads();
+  return merge_fn(merge_fn(smem4[0], smem4[1]), merge_fn(smem4[2], smem4[3]));
+}
+
+constexpr int kMergeThreads = 128;
+constexpr int kMergeBatch = 8;     // records loaded per thread before folding
+
 template <int MODE>
-__global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
   grid_dep_launch(); // the next call's kernel 1 may start (it prefetches only W)
   grid_dep_wait();   // records of kernel 1 are complete and visible
-  const int lane = threadIdx.x & 31;
-  const int n = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (n >= p.B) return;
+  const int n = blockIdx.x;
+  const int g = threadIdx.x;
+  const size_t base = static_cast<size_t>(n) * p.n_vt;
   if constexpr (MODE == MODE_GREEDY) {
+    __shared__ Top2 part[4];
     Top2 acc{-INFINITY, INT32_MAX, -INFINITY};
-    for (int t = lane; t < p.n_vt; t += 32) {
-      const size_t o = static_cast<size_t>(t) * p.B + n;
-      acc = top2_merge(acc, Top2{p.rec_m[o], p.rec_i[o], p.rec_s[o]});
-    }
+    for (int t0 = g; t0 < p.n_vt; t0 += kMergeThreads * kMergeBatch) {
+      Top2 r[kMergeBatch];
 #pragma unroll
-    for (int b = 1; b < 32; b <<= 1) acc = top2_merge(acc, shfl_xor(acc, b));
-    if (lane == 0) {
-      p.token[n] = acc.i;
-      p.gap[n] = gap_ulp_bf16(acc.m, acc.s);
+      for (int j = 0; j < kMergeBatch; ++j) {
+        const int t = t0 + j * kMergeThreads;
+        r[j] = t < p.n_vt ? Top2{p.rec_m[base + t], p.rec_i[base + t], p.rec_s[base + t]}
+                          : Top2{-INFINITY, INT32_MAX, -INFINITY};
+      }
+#pragma unroll
+      for (int j = 0; j < kMergeBatch; ++j) acc = top2_merge(acc, r[j]);
+    }
+    const Top2 tot = block_tree128(acc, top2_merge, part);
+    if (g == 0) {
+      p.token[n] = tot.i;
+      p.gap[n] = gap_ulp_bf16(tot.m, tot.s);
     }
   } else {
+    __shared__ Lse part[4];
     Lse acc{-INFINITY, 0.0f};
-    for (int t = lane; t < p.n_vt; t += 32) {
-      const size_t o = static_cast<size_t>(t) * p.B + n;
-      acc = lse_merge(acc, Lse{p.rec_m[o], p.rec_s[o]});
-    }
+    for (int t0 = g; t0 < p.n_vt; t0 += kMergeThreads * kMergeBatch) {
+      Lse r[kMergeBatch];
 #pragma unroll
-    for (int b = 1; b < 32; b <<= 1) acc = lse_merge(acc, shfl_xor(acc, b));
-    if (lane == 0) {
+      for (int j = 0; j < kMergeBatch; ++j) {
+        const int t = t0 + j * kMergeThreads;
+        r[j] = t < p.n_vt ? Lse{p.rec_m[base + t], p.rec_s[base + t]} : Lse{-INFINITY, 0.0f};
+      }
+#pragma unroll
+      for (int j = 0; j < kMergeBatch; ++j) acc = lse_merge(acc, r[j]);
+    }
+    const Lse tot = block_tree128(acc, lse_merge, part);
+    if (g == 0) {
       const int tg = p.targets[n];
       if (tg < 0 || tg >= p.V) {
         p.logp[n] = __int_as_float(0x7fc00000);
         atomicOr(p.err, ERR_TARGET);
       } else {
-        p.logp[n] = p.zt[n] - (acc.m + logf(acc.S));
+        p.logp[n] = p.zt[n] - (tot.m + logf(tot.S));
       }
     }
   }

@@ -378,7 +378,7 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) t[qq] = ITop2{red_m[qq * N + c], red_i[qq * N + c], red_s[qq * N + c]};
         const ITop2 r = itop2_merge(itop2_merge(t[0], t[1]), itop2_merge(t[2], t[3]));
-        const size_t o = static_cast<size_t>(vt) * p.B + n;
+        const size_t o = static_cast<size_t>(n) * p.n_vt + vt;   // records [B][n_vt]
         p.rec_m[o] = r.m;
         p.rec_i[o] = r.i;
         p.rec_s[o] = r.s;
@@ -405,21 +405,28 @@ struct Int8MergeParams {
   int32_t* gap;
 };
 
-__global__ void __launch_bounds__(128) int8_merge_kernel(const Int8MergeParams p) {
+__global__ void __launch_bounds__(kMergeThreads) int8_merge_kernel(const Int8MergeParams p) {
   grid_dep_wait();
-  const int lane = threadIdx.x & 31;
-  const int n = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (n >= p.B) return;
+  const int n = blockIdx.x;
+  const int g = threadIdx.x;
+  const size_t base = static_cast<size_t>(n) * p.n_vt;
+  __shared__ ITop2 part[4];
   ITop2 acc{INT32_MIN, INT32_MAX, INT32_MIN};
-  for (int t = lane; t < p.n_vt; t += 32) {
-    const size_t o = static_cast<size_t>(t) * p.B + n;
-    acc = itop2_merge(acc, ITop2{p.rec_m[o], p.rec_i[o], p.rec_s[o]});
-  }
+  for (int t0 = g; t0 < p.n_vt; t0 += kMergeThreads * kMergeBatch) {
+    ITop2 r[kMergeBatch];
 #pragma unroll
-  for (int b = 1; b < 32; b <<= 1) acc = itop2_merge(acc, shfl_xor(acc, b));
-  if (lane == 0) {
-    p.token[n] = acc.i;
-    p.gap[n] = acc.s == INT32_MIN ? INT32_MAX : acc.m - acc.s;
+    for (int j = 0; j < kMergeBatch; ++j) {
+      const int t = t0 + j * kMergeThreads;
+      r[j] = t < p.n_vt ? ITop2{p.rec_m[base + t], p.rec_i[base + t], p.rec_s[base + t]}
+                        : ITop2{INT32_MIN, INT32_MAX, INT32_MIN};
+    }
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) acc = itop2_merge(acc, r[j]);
+  }
+  const ITop2 tot = block_tree128(acc, itop2_merge, part);
+  if (g == 0) {
+    p.token[n] = tot.i;
+    p.gap[n] = tot.s == INT32_MIN ? INT32_MAX : tot.m - tot.s;
   }
 }
 
