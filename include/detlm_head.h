@@ -111,6 +111,27 @@ int detlm_head_logprob(detlm_head_t* head, const void* h_dev,
                        const int32_t* targets_dev, int64_t B, float* logp_dev,
                        cudaStream_t stream);
 
+/* Greedy speculative verify: the greedy call on n_req * P hidden rows (the P
+ * verified positions of each request, request-major) that also returns the
+ * accepted draft length of each request. The acceptance is folded into the
+ * split-V merge kernel (no extra launch); the handle keeps 8 bytes of
+ * per-request workspace, grown on demand (growth synchronizes the stream).
+ *
+ * "Inference and Decoding", section 6 (Speculative decoding): the target
+ * scores every drafted position in one forward pass and keeps the drafted
+ * tokens while they agree with it; "TandemLLM docs, 12 Exactness", 12.1: at
+ * temperature 0 that is equality with the target's greedy token.
+ * drafts_dev int32 [n_req, P]: the token proposed for each position.
+ * accepted_dev int32 [n_req]: number of leading positions whose draft equals
+ * the greedy token (0 .. P); the caller keeps those drafts and takes
+ * token[r, accepted[r]] as the next token when accepted[r] < P.
+ * token_dev, gap_dev, logits_dev: as in detlm_head_greedy for B = n_req * P.
+ * Requirements: n_req >= 0, P >= 1, n_req * P < 2^31. */
+int detlm_head_verify(detlm_head_t* head, const void* h_dev, int64_t n_req,
+                      int64_t P, const int32_t* drafts_dev, int32_t* token_dev,
+                      void* gap_dev, void* logits_dev, int32_t* accepted_dev,
+                      cudaStream_t stream);
+
 /* Host-buffer forms of the two calls: copy h (and targets) from host memory,
  * run the call, copy the results back, wait for the stream, and report the
  * error word. Host buffers may be pageable; pinned buffers copy faster.

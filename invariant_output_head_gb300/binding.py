@@ -25,6 +25,7 @@ _SIGS = {
     "detlm_head_reserve": (_i32, [_vp, _i64]),
     "detlm_head_greedy": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp]),
     "detlm_head_logprob": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
+    "detlm_head_verify": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     "detlm_head_greedy_host": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp]),
     "detlm_head_logprob_host": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
     "detlm_head_check": (_i32, [_vp, _vp]),
@@ -98,6 +99,13 @@ def detlm_head_greedy(handle, h_ptr, B, token_ptr, gap_ptr, logits_ptr, stream) 
 def detlm_head_logprob(handle, h_ptr, targets_ptr, B, logp_ptr, stream) -> None:
     _check(load_library().detlm_head_logprob(handle, h_ptr, targets_ptr, B, logp_ptr,
                                              stream), "detlm_head_logprob")
+
+
+def detlm_head_verify(handle, h_ptr, n_req, P, drafts_ptr, token_ptr, gap_ptr, logits_ptr,
+                      accepted_ptr, stream) -> None:
+    _check(load_library().detlm_head_verify(handle, h_ptr, n_req, P, drafts_ptr, token_ptr,
+                                            gap_ptr, logits_ptr, accepted_ptr, stream),
+           "detlm_head_verify")
 
 
 def detlm_head_greedy_host(handle, h_ptr, B, token_ptr, gap_ptr, logits_ptr, stream) -> None:
@@ -217,6 +225,27 @@ class Head:
         detlm_head_logprob(self.handle, h.data_ptr(), targets.data_ptr(), B, logp.data_ptr(),
                            _stream_ptr(stream))
         return logp
+
+    def verify(self, h, drafts, with_logits: bool = False, stream=None):
+        """Greedy speculative verify. h [R*P, d] request-major, drafts int32
+        [R, P]. Returns (token [R*P], gap, logits or None, accepted [R])."""
+        import torch
+        self._check_h(h)
+        if drafts.dtype != torch.int32 or not drafts.is_cuda or drafts.dim() != 2:
+            raise ValueError("drafts must be an int32 CUDA tensor [R, P]")
+        R, P = int(drafts.shape[0]), int(drafts.shape[1])
+        if R * P != int(h.shape[0]):
+            raise ValueError("h must hold R * P rows")
+        gdt = torch.int32 if self.dtype == "int8" else torch.float32
+        token = torch.empty(R * P, dtype=torch.int32, device=h.device)
+        gap = torch.empty(R * P, dtype=gdt, device=h.device)
+        logits = torch.empty((R * P, self.V), dtype=gdt, device=h.device) if with_logits else None
+        accepted = torch.empty(R, dtype=torch.int32, device=h.device)
+        detlm_head_verify(self.handle, h.data_ptr(), R, P, drafts.contiguous().data_ptr(),
+                          token.data_ptr(), gap.data_ptr(),
+                          logits.data_ptr() if logits is not None else None,
+                          accepted.data_ptr(), _stream_ptr(stream))
+        return token, gap, logits, accepted
 
     def check(self, stream=None) -> int:
         return detlm_head_check(self.handle, _stream_ptr(stream))

@@ -41,6 +41,11 @@ struct detlm_head {
   CUtensorMap tmW16;
   void* h16 = nullptr;
   size_t h16_bytes = 0;
+  // verify: per-request workspace (first_miss, arrived) and the arguments of
+  // the call in progress (drafts == nullptr outside detlm_head_verify)
+  int32_t* vws = nullptr;
+  int64_t vws_R = 0;
+  AcceptArgs acc{};
   // test hook and timing hook
   int stall = 0;
   uint64_t timeout_ns = 2000000000ull;
@@ -158,6 +163,32 @@ WsView ws_view(const detlm_head* h, int64_t B) {
   return w;
 }
 
+// verify workspace for R requests: first_miss [R] filled with kMissNone
+// bytes, arrived [R] zero; the merge puts both back after every call
+int ensure_vws(detlm_head* h, int64_t R, cudaStream_t stream) {
+  if (R <= h->vws_R) return DETLM_OK;
+  if (h->vws != nullptr) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return status_from_cuda(e);
+    cudaFree(h->vws);
+    h->vws = nullptr;
+    h->vws_R = 0;
+  }
+  void* p = nullptr;
+  cudaError_t e = cudaMalloc(&p, static_cast<size_t>(R) * 8);
+  if (e != cudaSuccess) return status_from_cuda(e);
+  e = cudaMemsetAsync(p, 0x7f, static_cast<size_t>(R) * 4, stream);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(static_cast<int32_t*>(p) + R, 0, static_cast<size_t>(R) * 4, stream);
+  if (e != cudaSuccess) {
+    cudaFree(p);
+    return status_from_cuda(e);
+  }
+  h->vws = static_cast<int32_t*>(p);
+  h->vws_R = R;
+  return DETLM_OK;
+}
+
 // Launch kernel 1 for N = 16 * nblk as a programmatic dependent of the
 // previous kernel on the stream (its prologue overlaps that kernel's tail).
 template <int MODE, int NBLK>
@@ -265,6 +296,7 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   mp.gap = gap;
   mp.logp = logp;
   mp.err = h->d_err;
+  mp.acc = h->acc;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(static_cast<unsigned>(B));
@@ -395,6 +427,7 @@ int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token
   mp.rec_s = reinterpret_cast<const int32_t*>(w.s);
   mp.token = token;
   mp.gap = gap;
+  mp.acc = h->acc;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(static_cast<unsigned>(B));
@@ -466,6 +499,7 @@ int launch_int8(detlm_head* h, const void* h_dev, int64_t B, int32_t* token, int
   mp.rec_s = p.rec_s;
   mp.token = token;
   mp.gap = gap;
+  mp.acc = h->acc;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(static_cast<unsigned>(B));
@@ -608,6 +642,26 @@ int detlm_head_logprob(detlm_head_t* h, const void* h_dev, const int32_t* target
                                     stream);
 }
 
+int detlm_head_verify(detlm_head_t* h, const void* h_dev, int64_t n_req, int64_t P,
+                      const int32_t* drafts_dev, int32_t* token_dev, void* gap_dev,
+                      void* logits_dev, int32_t* accepted_dev, cudaStream_t stream) {
+  if (h == nullptr || n_req < 0 || P < 1) return DETLM_EINVAL;
+  if (n_req > 0 && P > (INT32_MAX - 1) / n_req) return DETLM_EINVAL;
+  if (n_req == 0) return DETLM_OK;
+  if (drafts_dev == nullptr || !aligned(drafts_dev, 4)) return DETLM_EINVAL;
+  if (accepted_dev == nullptr || !aligned(accepted_dev, 4)) return DETLM_EINVAL;
+  int st = ensure_vws(h, n_req, stream);
+  if (st != DETLM_OK) return st;
+  h->acc.P = static_cast<int32_t>(P);
+  h->acc.drafts = drafts_dev;
+  h->acc.first_miss = h->vws;
+  h->acc.arrived = h->vws + h->vws_R;
+  h->acc.accepted = accepted_dev;
+  st = detlm_head_greedy(h, h_dev, n_req * P, token_dev, gap_dev, logits_dev, stream);
+  h->acc = AcceptArgs{};
+  return st;
+}
+
 int detlm_head_greedy_host(detlm_head_t* h, const void* h_host, int64_t B, int32_t* token_host,
                            void* gap_host, void* logits_host, cudaStream_t stream) {
   if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
@@ -688,6 +742,7 @@ int detlm_head_tiles(const detlm_head_t* h, int64_t B, int32_t* n_vtiles, int32_
 void detlm_head_destroy(detlm_head_t* h) {
   if (h == nullptr) return;
   if (h->ws) cudaFree(h->ws);
+  if (h->vws) cudaFree(h->vws);
   if (h->W16) cudaFree(h->W16);
   if (h->h16) cudaFree(h->h16);
   if (h->stage) cudaFree(h->stage);

@@ -89,6 +89,38 @@ struct HeadParams {
   uint64_t timeout_ns;
 };
 
+// Greedy speculative verify, folded into the merge ("Inference and Decoding",
+// section 6: the target scores every drafted position in one pass and keeps
+// the drafts while they agree; "TandemLLM docs, 12 Exactness", 12.1: at
+// temperature 0 that means equality with the greedy token). Rows are
+// request-major, P per request. The block that merges row n = r*P + j lowers
+// first_miss[r] to j when its token differs from the draft; the last of the
+// request's P blocks to arrive writes accepted[r] = min(first_miss[r], P)
+// and puts both workspace words back to their idle values. atomicMin is
+// order-free, so the result does not depend on which block finishes last.
+struct AcceptArgs {
+  int32_t P;
+  const int32_t* drafts;    // [R, P]; nullptr: plain greedy call
+  int32_t* first_miss;      // [R] workspace, kMissNone between calls
+  int32_t* arrived;         // [R] workspace, 0 between calls
+  int32_t* accepted;        // [R] output
+};
+constexpr int32_t kMissNone = 0x7f7f7f7f;   // what a 0x7f byte fill leaves
+
+__device__ __forceinline__ void accept_fold(const AcceptArgs& a, int n, int32_t tok) {
+  if (a.drafts == nullptr) return;
+  const int r = n / a.P;
+  const int j = n - r * a.P;
+  if (tok != a.drafts[n]) atomicMin(a.first_miss + r, j);
+  __threadfence();
+  if (atomicAdd(a.arrived + r, 1) == a.P - 1) {
+    __threadfence();
+    const int32_t f = atomicExch(a.first_miss + r, kMissNone);
+    a.arrived[r] = 0;
+    a.accepted[r] = f < a.P ? f : a.P;
+  }
+}
+
 struct MergeParams {
   int32_t V, B, n_vt;
   const float* rec_m;
@@ -100,6 +132,7 @@ struct MergeParams {
   float* gap;
   float* logp;
   int* err;
+  AcceptArgs acc;
 };
 
 // ------------------------------------------------------------ merge rules
@@ -684,6 +717,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     if (g == 0) {
       p.token[n] = tot.i;
       p.gap[n] = gap_ulp_bf16(tot.m, tot.s);
+      accept_fold(p.acc, n, tot.i);
     }
   } else {
     __shared__ Lse part[4];

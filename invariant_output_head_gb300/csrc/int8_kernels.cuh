@@ -403,6 +403,7 @@ struct Int8MergeParams {
   const int32_t* rec_s;
   int32_t* token;
   int32_t* gap;
+  AcceptArgs acc;
 };
 
 __global__ void __launch_bounds__(kMergeThreads) int8_merge_kernel(const Int8MergeParams p) {
@@ -427,6 +428,7 @@ __global__ void __launch_bounds__(kMergeThreads) int8_merge_kernel(const Int8Mer
   if (g == 0) {
     p.token[n] = tot.i;
     p.gap[n] = tot.s == INT32_MIN ? INT32_MAX : tot.m - tot.s;
+    accept_fold(p.acc, n, tot.i);
   }
 }
 

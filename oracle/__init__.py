@@ -27,5 +27,5 @@ from .head import (  # noqa: F401
     logits_float, logits_int, bigint_dot,
     ulp_bf16, top2, greedy, greedy_int, gap_from_top2_f32,
     logsumexp, logprob,
-    head_greedy, head_logprob,
+    head_greedy, head_logprob, verify_accept,
 )

@@ -20,6 +20,10 @@ Sources, by page title:
   Temperature: p_i = exp(z_i / tau) / sum_j exp(z_j / tau); tau = 1 here.
 * [LogprobGap] "batch-logprob-gap" -- the trainer's per-token log-probability
   log p(target) and the ratio exp(logp_new - logp_old).
+* [Decoding] section 6 (Speculative decoding): the target scores all drafted
+  positions in one forward pass and keeps the drafted tokens while they agree
+  with it; [Exactness] 12.1: greedy speculative output equals plain greedy
+  decoding, so at temperature 0 "agree" means "equals the greedy token".
 
 Readings where the pages are silent (each also listed with the design notes):
 
@@ -225,3 +229,29 @@ def head_logprob(W_raw: np.ndarray, h_raw: np.ndarray, targets: np.ndarray,
     lse = logsumexp(z)
     lp = logprob(z, targets)
     return {"logits": z, "A": A, "lse": lse, "logp": lp}
+
+
+# --------------------------------------------------------------------------
+# Greedy speculative-verify acceptance
+# --------------------------------------------------------------------------
+
+def verify_accept(tokens: np.ndarray, drafts: np.ndarray) -> np.ndarray:
+    """Accepted draft length per request ([Decoding] section 6, [Exactness] 12.1).
+
+    tokens [R, P]: the target's greedy token at each of a request's P verified
+    positions; drafts [R, P]: the token the drafter proposed for each
+    position. Accepted = the number of leading positions whose draft equals
+    the target's token (0 .. P); the caller keeps those drafts and takes the
+    target's token at the first mismatch.
+    """
+    tokens = np.asarray(tokens)
+    drafts = np.asarray(drafts)
+    R, P = tokens.shape
+    out = np.empty(R, dtype=np.int64)
+    for r in range(R):
+        a = 0
+        while a < P and drafts[r, a] == tokens[r, a]:
+            a += 1
+        out[r] = a
+    return out
+

@@ -26,7 +26,7 @@ import numpy as np
 __all__ = [
     "bf16_bits_from_f32", "f16_bits_from_f32", "normal_bf16", "uniform_int8",
     "pr1", "sweep", "spec_verify", "logprob", "int8_head", "small_float",
-    "small_int8", "SEED_W", "SEED_H", "SEED_X",
+    "small_int8", "plant_drafts", "SEED_W", "SEED_H", "SEED_X",
 ]
 
 SEED_W, SEED_H, SEED_X = 1000, 2000, 3000
@@ -237,3 +237,24 @@ def small_int8(seed: int, V: int, d: int, B: int, n_ties: int = 0,
         W[b] = W[a]
         h[k] = W[a]
     return {"W": W, "h": h, "V": V, "d": d, "dtype": "int8"}
+
+
+def plant_drafts(tokens: np.ndarray, V: int, seed: int):
+    """Drafted tokens for a speculative-verify block with planted agreement.
+
+    ``tokens`` [R, P] are reference tokens supplied by the caller. Request r
+    copies its first ``cut[r]`` tokens (cut ~ U{0 .. P}, so some requests
+    agree everywhere), replaces position ``cut[r]`` by a different id and
+    draws the rest uniformly. Returns (drafts int32 [R, P], cut int64 [R]).
+    """
+    tokens = np.asarray(tokens, dtype=np.int64)
+    R, P = tokens.shape
+    rng = _rng(seed)
+    cut = rng.integers(0, P + 1, size=R)
+    drafts = tokens.copy()
+    for r in range(R):
+        c = int(cut[r])
+        if c < P:
+            drafts[r, c] = (tokens[r, c] + 1 + rng.integers(0, max(V - 1, 1))) % V
+            drafts[r, c + 1:] = rng.integers(0, V, size=P - c - 1)
+    return drafts.astype(np.int32), cut

@@ -353,9 +353,29 @@ def pin_gap_from_top2(o):
     assert g.tolist() == [0.5, 1.0, 0.0, 1.0, 6.0 / 2.0 ** -6]
 
 
+def pin_verify_accept(o):
+    """Accepted draft length: hand-worked cases and the defining property."""
+    toks = np.array([[5, 7, 9, 11],      # drafts all agree -> 4
+                     [5, 7, 9, 11],      # first position disagrees -> 0
+                     [5, 7, 9, 11],      # third disagrees -> 2
+                     [1, 1, 1, 1]])      # agrees, then disagrees, then agrees -> 1
+    drafts = np.array([[5, 7, 9, 11],
+                       [6, 7, 9, 11],
+                       [5, 7, 8, 11],
+                       [1, 2, 1, 1]])
+    assert o.verify_accept(toks, drafts).tolist() == [4, 0, 2, 1]
+    rng = np.random.default_rng(9)
+    t = rng.integers(0, 3, size=(200, 16))
+    d = np.where(rng.random((200, 16)) < 0.8, t, rng.integers(0, 3, size=(200, 16)))
+    a = o.verify_accept(t, d)
+    for r in range(200):
+        assert (d[r, :a[r]] == t[r, :a[r]]).all()
+        assert a[r] == 16 or d[r, a[r]] != t[r, a[r]]
+
+
 ALL_PINS = [pin_tiny_golden, pin_bruteforce_float, pin_logsumexp_mpmath,
             pin_closed_forms, pin_page_examples, pin_int_head, pin_invariants,
-            pin_gap_from_top2]
+            pin_gap_from_top2, pin_verify_accept]
 
 
 def failing_pins(o):

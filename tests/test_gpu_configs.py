@@ -118,3 +118,36 @@ def test_int8_head_exact(torch_cuda, B):
     assert (t == np.argmax(z, axis=1)).all()
     for k, (a, b) in enumerate(c["dup_pairs"][:min(B, len(c["dup_pairs"]))]):
         assert int(t[k]) == min(a, b) and int(g[k]) == 0
+
+
+def test_spec_verify_accept_b256(torch_cuda):
+    """The speculative-verify block through the verify call: 16 requests x 16
+    positions. Requests 0 and 9 get drafts planted from the oracle's tokens
+    and must match the oracle's accepted lengths; the rest get drafts planted
+    from a seeded random sequence and must follow the acceptance rule on the
+    call's own tokens. Tokens and gaps are bitwise those of the plain call."""
+    from invariant_output_head_gb300 import Head
+    torch = torch_cuda
+    c = synth.spec_verify()
+    R, P = 16, 16
+    head = Head(dev(c["W"], "bf16"), "bf16")
+    h = dev(c["h"], "bf16")
+    checked = [0, 9]
+    rows = np.concatenate([np.arange(r * P, (r + 1) * P) for r in checked])
+    z_ref, A = oracle_float_rows(c["W"], c["h"][rows], "bf16")
+    t_ref = np.argmax(z_ref, axis=1)
+    seq = np.random.default_rng(77).integers(0, c["V"], size=(R, P))
+    for k, r in enumerate(checked):
+        seq[r] = t_ref[k * P:(k + 1) * P]
+    drafts, _ = synth.plant_drafts(seq, c["V"], seed=78)
+    t_plain, g_plain, _ = head.greedy(h)
+    tok, gap, z, acc = head.verify(h, torch.from_numpy(drafts).cuda(), with_logits=True)
+    tok, acc = host(tok), host(acc)
+    assert head.check() == 0
+    assert (tok == host(t_plain)).all()
+    assert (host(gap).view(np.uint32) == host(g_plain).view(np.uint32)).all()
+    check_float_greedy(z_ref, A, tok[rows], host(gap)[rows], host(z)[rows],
+                       label="spec-verify accept")
+    acc_ref = oracle.verify_accept(t_ref.reshape(len(checked), P), drafts[checked])
+    assert (acc[checked] == acc_ref).all()
+    assert (acc == oracle.verify_accept(tok.reshape(R, P), drafts)).all()

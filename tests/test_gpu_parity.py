@@ -118,3 +118,67 @@ def test_int8_wide_batch_path_exact(torch_cuda, V, d):
     assert (host(gap).astype(np.int64) == np.minimum(ref["gap"], 2**31 - 1)).all()
     t2, g2, z2 = head.greedy(h[:40], with_logits=True)      # narrow path
     assert (host(z2) == host(z)[:40]).all() and (host(t2) == host(tok)[:40]).all()
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "int8"])
+def test_verify_accept(torch_cuda, fmt):
+    """Greedy speculative verify on 16 requests x 16 positions: tokens and
+    gaps bitwise those of the plain greedy call, tokens equal to the oracle's,
+    accepted lengths equal to the oracle's rule on drafts planted from the
+    oracle's tokens."""
+    from invariant_output_head_gb300 import Head
+    torch = torch_cuda
+    R, P = 16, 16
+    if fmt == "int8":
+        case = synth.small_int8(61, 1000, 1040, R * P)
+        t_ref = oracle.head_greedy(case["W"], case["h"], "int8")["token"]
+    else:
+        case = synth.small_float(61, 1000, 520, R * P)
+        t_ref = oracle.head_greedy(case["W"], case["h"], "bf16")["token"]
+    drafts, cut = synth.plant_drafts(t_ref.reshape(R, P), case["V"], seed=3)
+    acc_ref = oracle.verify_accept(t_ref.reshape(R, P), drafts)
+    assert (acc_ref == cut).all()            # the planted mismatch is the first
+    head = Head(dev(case["W"], fmt), fmt)
+    h = dev(case["h"], fmt)
+    t_plain, g_plain, _ = head.greedy(h)
+    tok, gap, _, acc = head.verify(h, torch.from_numpy(drafts).cuda())
+    assert head.check() == 0
+    assert (host(tok) == t_ref).all()
+    assert (host(tok) == host(t_plain)).all()
+    assert (host(gap).view(np.uint32) == host(g_plain).view(np.uint32)).all()
+    assert (host(acc) == acc_ref).all()
+
+
+@pytest.mark.parametrize("R,P", [(1, 1), (3, 1), (1, 33), (5, 40), (9, 7)])
+def test_verify_accept_shapes(torch_cuda, R, P):
+    """Ragged request counts and draft lengths (one warp covers 32 positions;
+    P > 32 takes a second ballot)."""
+    from invariant_output_head_gb300 import Head
+    torch = torch_cuda
+    case = synth.small_float(62 + P, 300, 136, R * P)
+    t_ref = oracle.head_greedy(case["W"], case["h"], "bf16")["token"]
+    drafts, _ = synth.plant_drafts(t_ref.reshape(R, P), case["V"], seed=R * 100 + P)
+    head = Head(dev(case["W"], "bf16"), "bf16")
+    tok, _, _, acc = head.verify(dev(case["h"], "bf16"), torch.from_numpy(drafts).cuda())
+    assert head.check() == 0
+    assert (host(tok) == t_ref).all()
+    assert (host(acc) == oracle.verify_accept(t_ref.reshape(R, P), drafts)).all()
+
+
+def test_verify_accept_call_sequence(torch_cuda):
+    """Verify calls of changing shapes on one handle, interleaved with plain
+    greedy calls: the per-request workspace returns to its idle state after
+    every call, so each call's accepted lengths stand alone."""
+    from invariant_output_head_gb300 import Head
+    torch = torch_cuda
+    case = synth.small_float(70, 400, 200, 360)
+    t_ref = oracle.head_greedy(case["W"], case["h"], "bf16")["token"]
+    head = Head(dev(case["W"], "bf16"), "bf16")
+    h = dev(case["h"], "bf16")
+    for k, (R, P) in enumerate([(4, 8), (4, 8), (2, 3), (30, 12), (9, 40), (4, 8)]):
+        n = R * P
+        drafts, _ = synth.plant_drafts(t_ref[:n].reshape(R, P), case["V"], seed=500 + k)
+        _, _, _, acc = head.verify(h[:n], torch.from_numpy(drafts).cuda())
+        head.greedy(h[:7])
+        assert (host(acc) == oracle.verify_accept(t_ref[:n].reshape(R, P), drafts)).all(), (R, P)
+    assert head.check() == 0

@@ -47,6 +47,9 @@ MUTANTS = {
     "int_narrow_accumulator": ("return np.asarray(h, dtype=np.int64) @ np.asarray(W, dtype=np.int64).T",
                                "return (np.asarray(h, dtype=np.int64) @ np.asarray(W, dtype=np.int64).T).astype(np.int16).astype(np.int64)"),
     "int_gap_reversed": ("        gap = m - s\n", "        gap = s - m\n"),
+    "verify_accept_counts_all_matches": ("        while a < P and drafts[r, a] == tokens[r, a]:\n            a += 1",
+                                         "        a = int((drafts[r] == tokens[r]).sum())"),
+    "verify_accept_off_by_one": ("        out[r] = a\n", "        out[r] = min(a + 1, P)\n"),
     "gap_f32_rounded_difference": ("    with np.errstate(invalid=\"ignore\"):\n        return ((m - s) / ulp_bf16(m)).astype(np.float32)",
                                    "    with np.errstate(invalid=\"ignore\"):\n        return ((m - s) / ulp_bf16(s)).astype(np.float32)"),
 }
