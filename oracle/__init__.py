@@ -15,7 +15,10 @@ Everything is computed exactly or in float64 with numpy:
   below 2^63), cross-checked on samples with Python big-integer dots;
 * greedy token (lowest index among the maxima), runner-up value of the
   multiset, top-2 gap in bf16 ulps of the winning logit, logsumexp and the
-  log-probability of a target.
+  log-probability of a target;
+* the accepted draft length of greedy speculative verification;
+* the margin-gated decision: rounding of the logits to bf16 / fp16, the
+  rounded head's token and top-two margin, the gate and the gated token.
 
 Parity pins: every function here is pinned by tests that do not re-use its
 own formula (hand-worked tiny cases, brute force with exact rationals,
@@ -28,4 +31,5 @@ from .head import (  # noqa: F401
     ulp_bf16, top2, greedy, greedy_int, gap_from_top2_f32,
     logsumexp, logprob,
     head_greedy, head_logprob, verify_accept,
+    round_to_format, gated_greedy,
 )

@@ -20,6 +20,12 @@ Sources, by page title:
   Temperature: p_i = exp(z_i / tau) / sum_j exp(z_j / tau); tau = 1 here.
 * [LogprobGap] "batch-logprob-gap" -- the trainer's per-token log-probability
   log p(target) and the ratio exp(logp_new - logp_old).
+* [Precision] section "Correct the vulnerable token decisions, not every
+  calculation": ordinary inference is left as it is unless the top-two margin
+  of its logits is below a threshold tau (0.001 in the page's experiments);
+  at such a step the output projection is recomputed in FP32 and the token is
+  taken from that. The ordinary head is a 16-bit one, so its logits are the
+  16-bit roundings of the products' sums.
 * [Decoding] section 6 (Speculative decoding): the target scores all drafted
   positions in one forward pass and keeps the drafted tokens while they agree
   with it; [Exactness] 12.1: greedy speculative output equals plain greedy
@@ -38,7 +44,14 @@ Readings where the pages are silent (each also listed with the design notes):
   (float heads) and gap = INT32_MAX (integer head);
 * the integer head's gap is the exact integer m - s (a bf16 ulp has no meaning
   for int32 logits);
-* a target id outside [0, V) has no log-probability: NaN.
+* a target id outside [0, V) has no log-probability: NaN;
+* margin gate: the ordinary 16-bit head's logits are the exact logits rounded
+  once, to nearest with ties to even, into the head's storage format (bf16 or
+  fp16); its token is the lowest index of their maximum; the margin is the
+  difference of the two largest rounded values of the multiset (zero on a
+  tie), rounded once to float32; the gate fires when margin < tau (tau and
+  the comparison in float32); a fired row takes the FP32 recompute over the
+  full vocabulary, i.e. the argmax of the unrounded logits.
 """
 from __future__ import annotations
 
@@ -255,3 +268,62 @@ def verify_accept(tokens: np.ndarray, drafts: np.ndarray) -> np.ndarray:
         out[r] = a
     return out
 
+
+
+# --------------------------------------------------------------------------
+# Margin-gated FP32 recompute
+# --------------------------------------------------------------------------
+
+# (significand bits after the point, smallest normal exponent, largest finite)
+_FORMATS = {
+    "bf16": (7, -126, (2.0 - 2.0 ** -7) * 2.0 ** 127),
+    "fp16": (10, -14, 65504.0),
+}
+
+
+def round_to_format(x, fmt: str) -> np.ndarray:
+    """Round float64 values once to the nearest value of bf16 or fp16, ties to
+    even (IEEE 754 roundTiesToEven), returned as float64.
+
+    In the binade [2^E, 2^(E+1)) (E clamped below at the smallest normal
+    exponent, which also covers the subnormals) the format's numbers are the
+    multiples of q = 2^(E - p); |x| / q is exact, np.rint rounds it half to
+    even, and a result above the largest finite value overflows to infinity.
+    """
+    p, emin, vmax = _FORMATS[fmt]
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.abs(x)
+    _, e = np.frexp(ax)
+    E = np.maximum(e - 1, emin)
+    q = np.ldexp(1.0, E - p)
+    with np.errstate(invalid="ignore", over="ignore"):
+        r = np.rint(ax / q) * q
+    r = np.where(r > vmax, np.inf, r)
+    return np.copysign(r, x)
+
+
+def gated_greedy(z: np.ndarray, tau: float, fmt: str) -> dict:
+    """Margin-gated decision ([Precision], "Correct the vulnerable token
+    decisions"), row by row.
+
+    z [B, V]: the unrounded logits (exact, or the head's own float32 values).
+    base = lowest index of the maximum of the rounded logits (the ordinary
+    16-bit head's greedy token); margin = float32(M16 - S16) with M16, S16
+    the two largest rounded values of the multiset; fired = margin < tau in
+    float32; token = argmax of the unrounded logits (lowest index) where
+    fired, else base.
+    """
+    z = np.asarray(z, dtype=np.float64)
+    z16 = round_to_format(z, fmt)
+    base = np.argmax(z16, axis=1).astype(np.int64)
+    M16 = z16[np.arange(z.shape[0]), base]
+    if z.shape[1] >= 2:
+        S16 = np.sort(z16, axis=1)[:, -2]
+    else:
+        S16 = np.full(z.shape[0], -np.inf)
+    with np.errstate(invalid="ignore"):
+        margin = (M16 - S16).astype(np.float32)
+    fired = margin < np.float32(tau)
+    full = np.argmax(z, axis=1).astype(np.int64)
+    token = np.where(fired, full, base)
+    return {"token": token, "base": base, "margin": margin, "fired": fired}

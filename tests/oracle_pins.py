@@ -373,9 +373,138 @@ def pin_verify_accept(o):
         assert a[r] == 16 or d[r, a[r]] != t[r, a[r]]
 
 
+# ---- rounding into the 16-bit formats, by exact search over bit patterns
+
+def _format_table(fmt):
+    """All non-negative finite values of the format, ascending, with their
+    bit patterns (decoded through struct, not numpy)."""
+    if fmt == "bf16":
+        bits = range(0x0000, 0x7F80)
+        vals = [struct.unpack(">f", struct.pack(">I", b << 16))[0] for b in bits]
+    else:
+        bits = range(0x0000, 0x7C00)
+        vals = [struct.unpack("<e", struct.pack("<H", b))[0] for b in bits]
+    return list(vals), list(bits)
+
+
+_TABLES = {}
+
+
+def exact_round(x: float, fmt: str) -> float:
+    """Nearest value of the format by exact rational comparison; on a tie the
+    one whose bit pattern is even; beyond the largest finite value by half a
+    step or more (ties included, as the step above is even), infinity."""
+    import bisect
+    if fmt not in _TABLES:
+        _TABLES[fmt] = _format_table(fmt)
+    vals, bits = _TABLES[fmt]
+    ax = Fraction(abs(x))
+    vmax = Fraction(vals[-1])
+    step = vmax - Fraction(vals[-2])
+    if ax >= vmax + step / 2:
+        return math.copysign(math.inf, x)
+    k = bisect.bisect_left(vals, float(ax))
+    if k < len(vals) and Fraction(vals[k]) == ax:
+        r = vals[k]
+    else:
+        lo, hi = vals[k - 1], vals[k]
+        dl, dh = ax - Fraction(lo), Fraction(hi) - ax
+        if dl < dh:
+            r = lo
+        elif dh < dl:
+            r = hi
+        else:
+            r = lo if bits[k - 1] % 2 == 0 else hi
+    return math.copysign(r, x)
+
+
+def pin_round_to_format(o):
+    """Rounding into bf16 / fp16: hand-picked midpoints, subnormals and
+    overflow, brute force on random float64 values, and the library
+    conversions (torch float32 -> bfloat16, numpy float32 -> float16) on
+    random float32 values."""
+    hand = {
+        "bf16": [(1 + 2 ** -8, 1.0), (1 + 3 * 2 ** -8, 1 + 2 ** -6), (-(1 + 2 ** -8), -1.0),
+                 (2 ** -134, 0.0), (1.5 * 2 ** -133, 2 ** -132), ((2 - 2 ** -8) * 2 ** 127, math.inf),
+                 ((2 - 2 ** -7) * 2 ** 127, (2 - 2 ** -7) * 2 ** 127), (3.0 + 2 ** -8, 3.0)],
+        "fp16": [(65520.0, math.inf), (65519.0, 65504.0), (2 ** -25, 0.0),
+                 (1.5 * 2 ** -24, 2 ** -23), (2.5 * 2 ** -24, 2 ** -23), (2 + 2 ** -10, 2.0),
+                 (2 + 3 * 2 ** -10, 2 + 2 ** -8)],
+    }
+    for fmt, cases in hand.items():
+        got = o.round_to_format(np.array([c[0] for c in cases]), fmt)
+        assert got.tolist() == [c[1] for c in cases], (fmt, got)
+    rng = np.random.default_rng(21)
+    for fmt, scale in (("bf16", 8.0), ("fp16", 8.0)):
+        x = rng.normal(0, scale, 300) * np.exp2(rng.integers(-20, 20, 300))
+        x = np.concatenate([x, rng.normal(0, 1e-6, 40)])
+        got = o.round_to_format(x, fmt)
+        want = [exact_round(float(v), fmt) for v in x]
+        assert got.tolist() == want, fmt
+    x32 = (rng.normal(0, 4, 4000) * np.exp2(rng.integers(-30, 30, 4000))).astype(np.float32)
+    import torch
+    lib_bf16 = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
+    assert (o.round_to_format(x32.astype(np.float64), "bf16") == lib_bf16).all()
+    lib_fp16 = x32.astype(np.float16).astype(np.float64)
+    assert (o.round_to_format(x32.astype(np.float64), "fp16") == lib_fp16).all()
+
+
+def _loop_gated(row, tau, fmt):
+    """Gated decision of one row by Python loops over exactly rounded values."""
+    r16 = [exact_round(float(v), fmt) for v in row]
+    base, M = 0, r16[0]
+    for v in range(1, len(row)):
+        if r16[v] > M:
+            base, M = v, r16[v]
+    rest = sorted(r16, reverse=True)
+    S = rest[1] if len(rest) > 1 else -math.inf
+    margin = np.float32(M - S) if S != -math.inf else np.float32(math.inf)
+    fired = bool(margin < np.float32(tau))
+    full = loop_argmax_lowest(list(row))
+    return (full if fired else base), base, float(margin), fired
+
+
+def pin_gated_greedy(o):
+    """Margin gate: hand-worked rows, brute force on small rows, and the
+    consequence of monotone rounding (with tau > 0 the gated token is the
+    argmax of the unrounded logits)."""
+    cases = [  # (row, tau, fmt) -> (token, base, margin, fired)
+        ([2.0, 2.0 + 2 ** -10, 1.0], 0.001, "bf16", (1, 0, 0.0, True)),
+        ([1.0, 3.0, 3.0 - 2 ** -6], 0.001, "bf16", (1, 1, 2 ** -6, False)),
+        ([5.0, 5.0], 0.001, "bf16", (0, 0, 0.0, True)),
+        ([2.0, 2.0 + 2 ** -10, 1.0], 0.0, "bf16", (0, 0, 0.0, False)),
+        ([1.0, 3.0, 3.0 - 2 ** -6], 0.02, "bf16", (1, 1, 2 ** -6, True)),
+        ([3.0 + 2 ** -8, 3.0], 0.001, "bf16", (0, 0, 0.0, True)),
+        ([2.0, 2.0 + 2 ** -8], 0.001, "bf16", (1, 0, 0.0, True)),
+        ([2.0, 2.0 + 2 ** -8], 0.001, "fp16", (1, 1, 2 ** -8, False)),
+        ([2.0, 2.0 + 2 ** -12, -7.0], 0.001, "fp16", (1, 0, 0.0, True)),
+        ([-4.0, -4.0 - 2 ** -5, -4.0 + 2 ** -8], 0.001, "bf16", (2, 0, 0.0, True)),
+        ([-4.0, -4.0 - 2 ** -5, -4.0 + 2 ** -6], 0.001, "bf16", (2, 2, 2 ** -6, False)),
+    ]
+    for row, tau, fmt, (tok, base, margin, fired) in cases:
+        g = o.gated_greedy(np.array([row]), tau, fmt)
+        got = (int(g["token"][0]), int(g["base"][0]), float(g["margin"][0]), bool(g["fired"][0]))
+        assert got == (tok, base, margin, fired), (row, tau, fmt, got)
+    g = o.gated_greedy(np.array([[7.0]]), 0.001, "bf16")
+    assert int(g["token"][0]) == 0 and g["margin"][0] == np.inf and not g["fired"][0]
+    rng = np.random.default_rng(22)
+    for fmt in ("bf16", "fp16"):
+        z = rng.integers(-40, 40, size=(150, 5)) / 16.0 + rng.normal(0, 0.004, (150, 5))
+        for tau in (0.001, 0.0, 0.05):
+            g = o.gated_greedy(z, tau, fmt)
+            for n in range(z.shape[0]):
+                want = _loop_gated(z[n], tau, fmt)
+                got = (int(g["token"][n]), int(g["base"][n]), float(g["margin"][n]),
+                       bool(g["fired"][n]))
+                assert got == want, (fmt, tau, z[n], got, want)
+            if tau > 0:
+                assert (g["token"] == np.array([loop_argmax_lowest(list(r)) for r in z])).all()
+
+
 ALL_PINS = [pin_tiny_golden, pin_bruteforce_float, pin_logsumexp_mpmath,
             pin_closed_forms, pin_page_examples, pin_int_head, pin_invariants,
-            pin_gap_from_top2, pin_verify_accept]
+            pin_gap_from_top2, pin_verify_accept, pin_round_to_format,
+            pin_gated_greedy]
 
 
 def failing_pins(o):

@@ -50,6 +50,17 @@ MUTANTS = {
     "verify_accept_counts_all_matches": ("        while a < P and drafts[r, a] == tokens[r, a]:\n            a += 1",
                                          "        a = int((drafts[r] == tokens[r]).sum())"),
     "verify_accept_off_by_one": ("        out[r] = a\n", "        out[r] = min(a + 1, P)\n"),
+    "round_toward_zero": ("        r = np.rint(ax / q) * q\n", "        r = np.trunc(ax / q) * q\n"),
+    "round_ties_away": ("        r = np.rint(ax / q) * q\n", "        r = np.floor(ax / q + 0.5) * q\n"),
+    "round_no_overflow": ("    r = np.where(r > vmax, np.inf, r)\n", ""),
+    "round_no_subnormal_clamp": ("    E = np.maximum(e - 1, emin)\n", "    E = e - 1\n"),
+    "gate_base_highest_on_tie": ("    base = np.argmax(z16, axis=1).astype(np.int64)\n",
+                                 "    base = (z16.shape[1] - 1 - np.argmax(z16[:, ::-1], axis=1)).astype(np.int64)\n"),
+    "gate_margin_unrounded": ("        margin = (M16 - S16).astype(np.float32)\n",
+                              "        margin = (np.sort(z, axis=1)[:, -1] - (np.sort(z, axis=1)[:, -2] if z.shape[1] > 1 else -np.inf)).astype(np.float32)\n"),
+    "gate_fires_at_equality": ("    fired = margin < np.float32(tau)\n", "    fired = margin <= np.float32(tau)\n"),
+    "gate_token_always_base": ("    token = np.where(fired, full, base)\n", "    token = base\n"),
+    "gate_token_always_full": ("    token = np.where(fired, full, base)\n", "    token = full\n"),
     "gap_f32_rounded_difference": ("    with np.errstate(invalid=\"ignore\"):\n        return ((m - s) / ulp_bf16(m)).astype(np.float32)",
                                    "    with np.errstate(invalid=\"ignore\"):\n        return ((m - s) / ulp_bf16(s)).astype(np.float32)"),
 }
