@@ -111,6 +111,32 @@ int detlm_head_logprob(detlm_head_t* head, const void* h_dev,
                        const int32_t* targets_dev, int64_t B, float* logp_dev,
                        cudaStream_t stream);
 
+/* Margin-gated greedy call ("Greedy Decoding Has a Precision Clause",
+ * section "Correct the vulnerable token decisions, not every calculation"):
+ * an ordinary 16-bit head returns its logits rounded to its storage format
+ * and picks their argmax; where the top-two margin of those rounded logits
+ * is below tau, the output projection is redone in FP32 and the token is
+ * taken from it. Here the FP32 logits are what the projection computes in
+ * the first place, so one pass yields both decisions and the gate costs no
+ * second projection.
+ *
+ * Float heads only (INT8: DETLM_EUNSUPPORTED). Per row n:
+ *   z16 = each fp32 logit rounded once (nearest, ties to even) to bf16 for
+ *         a BF16 head, to fp16 for an FP16 head;
+ *   base_token[n] = lowest index of max z16 (the ordinary head's token);
+ *   margin[n]     = fp32(max z16 - runner-up of the multiset z16), +inf if
+ *                   V == 1;
+ *   token[n]      = the fp32 argmax (lowest index, as detlm_head_greedy)
+ *                   where margin[n] < tau, else base_token[n];
+ *   gap[n], logits: as detlm_head_greedy.
+ * tau: any non-NaN float (0.001 in the page's experiments; tau <= 0 never
+ * fires and returns the ordinary head's tokens); NaN gives DETLM_EINVAL.
+ * base_token_dev and margin_dev may be NULL. */
+int detlm_head_greedy_gated(detlm_head_t* head, const void* h_dev, int64_t B,
+                            float tau, int32_t* token_dev, float* gap_dev,
+                            float* logits_dev, int32_t* base_token_dev,
+                            float* margin_dev, cudaStream_t stream);
+
 /* Greedy speculative verify: the greedy call on n_req * P hidden rows (the P
  * verified positions of each request, request-major) that also returns the
  * accepted draft length of each request. The acceptance is folded into the

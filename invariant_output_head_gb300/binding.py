@@ -26,6 +26,8 @@ _SIGS = {
     "detlm_head_greedy": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp]),
     "detlm_head_logprob": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
     "detlm_head_verify": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "detlm_head_greedy_gated": (_i32, [_vp, _vp, _i64, ctypes.c_float, _vp, _vp, _vp, _vp, _vp,
+                                       _vp]),
     "detlm_head_greedy_host": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp]),
     "detlm_head_logprob_host": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
     "detlm_head_check": (_i32, [_vp, _vp]),
@@ -99,6 +101,14 @@ def detlm_head_greedy(handle, h_ptr, B, token_ptr, gap_ptr, logits_ptr, stream) 
 def detlm_head_logprob(handle, h_ptr, targets_ptr, B, logp_ptr, stream) -> None:
     _check(load_library().detlm_head_logprob(handle, h_ptr, targets_ptr, B, logp_ptr,
                                              stream), "detlm_head_logprob")
+
+
+def detlm_head_greedy_gated(handle, h_ptr, B, tau, token_ptr, gap_ptr, logits_ptr,
+                            base_token_ptr, margin_ptr, stream) -> None:
+    _check(load_library().detlm_head_greedy_gated(handle, h_ptr, B, tau, token_ptr, gap_ptr,
+                                                  logits_ptr, base_token_ptr, margin_ptr,
+                                                  stream),
+           "detlm_head_greedy_gated")
 
 
 def detlm_head_verify(handle, h_ptr, n_req, P, drafts_ptr, token_ptr, gap_ptr, logits_ptr,
@@ -225,6 +235,23 @@ class Head:
         detlm_head_logprob(self.handle, h.data_ptr(), targets.data_ptr(), B, logp.data_ptr(),
                            _stream_ptr(stream))
         return logp
+
+    def greedy_gated(self, h, tau: float = 0.001, with_logits: bool = False, stream=None):
+        """Margin-gated greedy call. Returns (token, gap, logits or None,
+        base_token, margin)."""
+        import torch
+        self._check_h(h)
+        B = int(h.shape[0])
+        token = torch.empty(B, dtype=torch.int32, device=h.device)
+        gap = torch.empty(B, dtype=torch.float32, device=h.device)
+        base = torch.empty(B, dtype=torch.int32, device=h.device)
+        margin = torch.empty(B, dtype=torch.float32, device=h.device)
+        logits = (torch.empty((B, self.V), dtype=torch.float32, device=h.device)
+                  if with_logits else None)
+        detlm_head_greedy_gated(self.handle, h.data_ptr(), B, float(tau), token.data_ptr(),
+                                gap.data_ptr(), logits.data_ptr() if logits is not None else None,
+                                base.data_ptr(), margin.data_ptr(), _stream_ptr(stream))
+        return token, gap, logits, base, margin
 
     def verify(self, h, drafts, with_logits: bool = False, stream=None):
         """Greedy speculative verify. h [R*P, d] request-major, drafts int32

@@ -114,8 +114,8 @@ int slots_for(int N) {
   return s > kMaxSlots ? kMaxSlots : s;
 }
 
-int stages_for(int N) {
-  const SmemLayout L1 = smem_layout(N, 1);
+int stages_for(int N, bool gated = false) {
+  const SmemLayout L1 = smem_layout(N, 1, gated);
   const uint32_t fixed = L1.total - L1.stage_bytes + 2u * kMaxStages * 8u + 1024u;
   int s = static_cast<int>((kSmemLimit - fixed) / L1.stage_bytes);
   if (s > kMaxStages) s = kMaxStages;
@@ -128,10 +128,11 @@ int status_from_cuda(cudaError_t e) {
   return DETLM_ECUDA;
 }
 
-// workspace: rec_m, rec_i, rec_s [B, n_vt] and zt [B], 256-byte aligned parts
+// workspace: rec_m, rec_i, rec_s, rec_b [B, n_vt] and zt [B], 256-byte
+// aligned parts
 size_t ws_part(int64_t n) { return (static_cast<size_t>(n) * 4 + 255) & ~static_cast<size_t>(255); }
 size_t ws_bytes_for(const detlm_head* h, int64_t B) {
-  return 3 * ws_part(static_cast<int64_t>(h->n_vt) * B) + ws_part(B);
+  return 4 * ws_part(static_cast<int64_t>(h->n_vt) * B) + ws_part(B);
 }
 
 int ensure_ws(detlm_head* h, int64_t B, cudaStream_t stream) {
@@ -151,7 +152,7 @@ int ensure_ws(detlm_head* h, int64_t B, cudaStream_t stream) {
   return DETLM_OK;
 }
 
-struct WsView { float* m; int32_t* i; float* s; float* zt; };
+struct WsView { float* m; int32_t* i; float* s; int32_t* b; float* zt; };
 WsView ws_view(const detlm_head* h, int64_t B) {
   uint8_t* b = static_cast<uint8_t*>(h->ws);
   const size_t part = ws_part(static_cast<int64_t>(h->n_vt) * B);
@@ -159,7 +160,8 @@ WsView ws_view(const detlm_head* h, int64_t B) {
   w.m = reinterpret_cast<float*>(b);
   w.i = reinterpret_cast<int32_t*>(b + part);
   w.s = reinterpret_cast<float*>(b + 2 * part);
-  w.zt = reinterpret_cast<float*>(b + 3 * part);
+  w.b = reinterpret_cast<int32_t*>(b + 3 * part);
+  w.zt = reinterpret_cast<float*>(b + 4 * part);
   return w;
 }
 
@@ -236,9 +238,13 @@ cudaError_t launch_gemm(const CUtensorMap& tmW, const CUtensorMap& tmH, const He
   }
 }
 
+// margin gate of the gated greedy call
+struct GateArgs { float tau; int32_t* base_token; float* margin; };
+
 template <int MODE>
 int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* targets,
-                 int32_t* token, float* gap, float* logits, float* logp, cudaStream_t stream) {
+                 int32_t* token, float* gap, float* logits, float* logp, cudaStream_t stream,
+                 const GateArgs* gate = nullptr) {
   const int N = cols_for(B);
   CUtensorMap tmH;
   if (!encode_2d(&tmH, h->dtype, h_dev, h->d, B, static_cast<uint32_t>(N))) return DETLM_EINVAL;
@@ -257,7 +263,7 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   p.nk = h->nk;
   p.n_chunks = static_cast<int32_t>((h->d + kChunkK - 1) / kChunkK);
   p.n_slots = slots_for(N);
-  p.stages = stages_for(N);
+  p.stages = stages_for(N, MODE == MODE_GATED);
   p.tmem_cols = tmem_cols_for(p.n_slots * N);
   p.idesc = idesc_f16(h->dtype == DETLM_BF16 ? 1u : 0u, kBM, static_cast<uint32_t>(N));
   p.logits = logits;
@@ -269,8 +275,10 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   p.err = h->d_err;
   p.stall = h->stall;
   p.timeout_ns = h->timeout_ns;
+  p.rec_b = w.b;
+  p.round_fp16 = h->dtype == DETLM_FP16 ? 1 : 0;
 
-  const SmemLayout L = smem_layout(N, p.stages);
+  const SmemLayout L = smem_layout(N, p.stages, MODE == MODE_GATED);
   const size_t smem = L.total + 1024;
   const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
   const int grid = static_cast<int>(units < h->num_sms ? units : h->num_sms);
@@ -297,6 +305,11 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   mp.logp = logp;
   mp.err = h->d_err;
   mp.acc = h->acc;
+  mp.rec_b = w.b;
+  mp.round_fp16 = p.round_fp16;
+  mp.tau = gate != nullptr ? gate->tau : 0.0f;
+  mp.base_token = gate != nullptr ? gate->base_token : nullptr;
+  mp.margin = gate != nullptr ? gate->margin : nullptr;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(static_cast<unsigned>(B));
@@ -640,6 +653,23 @@ int detlm_head_logprob(detlm_head_t* h, const void* h_dev, const int32_t* target
   if (logp_dev == nullptr || !aligned(logp_dev, 4)) return DETLM_EINVAL;
   return launch_float<MODE_LOGPROB>(h, h_dev, B, targets_dev, nullptr, nullptr, nullptr, logp_dev,
                                     stream);
+}
+
+int detlm_head_greedy_gated(detlm_head_t* h, const void* h_dev, int64_t B, float tau,
+                            int32_t* token_dev, float* gap_dev, float* logits_dev,
+                            int32_t* base_token_dev, float* margin_dev, cudaStream_t stream) {
+  if (h == nullptr || bad_B(B) || std::isnan(tau)) return DETLM_EINVAL;
+  if (h->dtype == DETLM_INT8) return DETLM_EUNSUPPORTED;
+  if (B == 0) return DETLM_OK;
+  if (h_dev == nullptr || !aligned(h_dev, 16)) return DETLM_EINVAL;
+  if (token_dev == nullptr || !aligned(token_dev, 4)) return DETLM_EINVAL;
+  if (gap_dev == nullptr || !aligned(gap_dev, 4)) return DETLM_EINVAL;
+  if (logits_dev != nullptr && !aligned(logits_dev, 4)) return DETLM_EINVAL;
+  if (base_token_dev != nullptr && !aligned(base_token_dev, 4)) return DETLM_EINVAL;
+  if (margin_dev != nullptr && !aligned(margin_dev, 4)) return DETLM_EINVAL;
+  const GateArgs gate{tau, base_token_dev, margin_dev};
+  return launch_float<MODE_GATED>(h, h_dev, B, nullptr, token_dev, gap_dev, logits_dev, nullptr,
+                                  stream, &gate);
 }
 
 int detlm_head_verify(detlm_head_t* h, const void* h_dev, int64_t n_req, int64_t P,

@@ -45,6 +45,8 @@
 // operators that are commutative bit for bit.
 #pragma once
 #include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 #include <cmath>
 #include <type_traits>
@@ -65,7 +67,11 @@ constexpr int kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
 // are held as fp16 (exact), every 128-element chunk sum is an integer below
 // 2^21 (exact in the fp32 accumulator) and the chunk sums are added in
 // int32; logits, records and the decision are int32.
-enum : int { MODE_GREEDY = 0, MODE_LOGPROB = 1, MODE_INT = 2 };
+// MODE_GATED: the greedy call plus the margin gate of "Greedy Decoding Has a
+// Precision Clause" (section on correcting the vulnerable token decisions):
+// the record also carries, for the logits rounded to the head's 16-bit
+// format, the lowest index of their maximum.
+enum : int { MODE_GREEDY = 0, MODE_LOGPROB = 1, MODE_INT = 2, MODE_GATED = 3 };
 enum : int { ERR_TIMEOUT = 1, ERR_TARGET = 2 };
 
 struct HeadParams {
@@ -87,6 +93,8 @@ struct HeadParams {
   int* err;                 // device error word
   int32_t stall;            // test hook: MMA issuer waits on a dead barrier
   uint64_t timeout_ns;
+  int32_t* rec_b;           // [B, n_vt] gated: lowest index of the rounded maximum
+  int32_t round_fp16;       // gated: 1 rounds logits to fp16, 0 to bf16
 };
 
 // Greedy speculative verify, folded into the merge ("Inference and Decoding",
@@ -133,6 +141,12 @@ struct MergeParams {
   float* logp;
   int* err;
   AcceptArgs acc;
+  // margin gate
+  const int32_t* rec_b;
+  int32_t round_fp16;
+  float tau;
+  int32_t* base_token;      // optional [B]
+  float* margin;            // optional [B]
 };
 
 // ------------------------------------------------------------ merge rules
@@ -218,6 +232,52 @@ __device__ __forceinline__ Top2 xp_top2(const float* xp, int lane, int v_row0) {
   return top2_merge(t, shfl_xor(t, 16));
 }
 
+// A logit rounded once (to nearest, ties to even) into the head's 16-bit
+// format: the value an ordinary bf16 / fp16 projection returns. Rounding is
+// monotone, so the rounded maximum of any subset is the rounding of its
+// maximum and the rounded runner-up that of its runner-up.
+__device__ __forceinline__ float round16(float x, bool fp16) {
+  return fp16 ? __half2float(__float2half_rn(x)) : __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// Lowest index attaining the maximum of the rounded logits; the value is
+// carried only during a fold (elsewhere it is round16 of the record's m).
+struct Low16 { float m; int32_t i; };
+__device__ __forceinline__ Low16 low16_merge(const Low16& a, const Low16& b) {
+  const bool aw = (a.m > b.m) || (a.m == b.m && a.i < b.i);
+  return aw ? a : b;
+}
+__device__ __forceinline__ Low16 shfl_xor(const Low16& x, int b) {
+  return Low16{__shfl_xor_sync(0xffffffffu, x.m, b), __shfl_xor_sync(0xffffffffu, x.i, b)};
+}
+
+// gated: the greedy fold plus the lowest row index of the rounded maximum
+__device__ __forceinline__ Top2 xp_gated(const float* xp, int lane, int v_row0, bool fp16,
+                                         int32_t& i16) {
+  const int c = lane & 15, h = lane >> 4;
+  Top2 t{-INFINITY, INT32_MAX, -INFINITY};
+  Low16 b{-INFINITY, INT32_MAX};
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int r = h * 16 + j;
+    const float x = xp[r * kXpStride + c];
+    if (x > t.m) {
+      t.s = t.m;
+      t.m = x;
+      t.i = v_row0 + r;
+    } else {
+      t.s = fmaxf(t.s, x);
+    }
+    const float x16 = round16(x, fp16);
+    if (x16 > b.m) {            // strictly greater: on a tie the lower row stays
+      b.m = x16;
+      b.i = v_row0 + r;
+    }
+  }
+  i16 = low16_merge(b, shfl_xor(b, 16)).i;
+  return top2_merge(t, shfl_xor(t, 16));
+}
+
 // log-prob: exact maximum M of the 16 rows, then sum of exp(z - M) in
 // ascending row order; the two halves merge commutatively
 __device__ __forceinline__ Lse xp_lse(const float* xp, int lane) {
@@ -283,7 +343,7 @@ struct SmemLayout {
 // Stage s: kblocks_per_stage 128-byte K boxes of the W tile (each [128 rows x
 // 128 B], swizzled) followed by as many boxes of the hidden-row tile
 // ([N rows x 128 B] each).
-__host__ __device__ inline SmemLayout smem_layout(int N, int stages) {
+__host__ __device__ inline SmemLayout smem_layout(int N, int stages, bool gated = false) {
   SmemLayout L;
   const uint32_t kps = static_cast<uint32_t>(kblocks_per_stage(N));
   L.a_bytes = kps * kBM * kRowBytes;
@@ -295,7 +355,10 @@ __host__ __device__ inline SmemLayout smem_layout(int N, int stages) {
   L.red_off = L.ctrl_off + (2u * stages + 2u * kMaxSlots + 2u) * 8u + 16u;
   // per-quadrant column results: 3 words x 4 quadrants x N columns, the
   // unit's target rows (N words), then the epilogue warps' transpose areas
-  L.xp_off = L.red_off + 3u * 4u * static_cast<uint32_t>(N) * 4u + static_cast<uint32_t>(N) * 4u;
+  // (gated: 4 x N more words, the quadrants' lowest indices of the rounded
+  // maximum)
+  L.xp_off = L.red_off + 3u * 4u * static_cast<uint32_t>(N) * 4u + static_cast<uint32_t>(N) * 4u +
+             (gated ? 4u * static_cast<uint32_t>(N) * 4u : 0u);
   L.total = L.xp_off + static_cast<uint32_t>(epi_warps_for(N)) * kXpWords * 4u;
   return L;
 }
@@ -332,7 +395,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = p.stages;
-  const SmemLayout L = smem_layout(N, S);
+  const SmemLayout L = smem_layout(N, S, MODE == MODE_GATED);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.ctrl_off);
   const uint32_t bar0 = smem_u32(bars);
@@ -349,6 +412,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   int32_t* red_i = reinterpret_cast<int32_t*>(red_m + 4 * N);
   float* red_s = reinterpret_cast<float*>(red_i + 4 * N);
   int* tgt_row = reinterpret_cast<int*>(red_s + 4 * N);   // log-prob: target row in tile, or -1
+  int32_t* red_b = tgt_row + N;                            // gated: [4][N]
   float* xpose = reinterpret_cast<float*>(smem + L.xp_off);
   const uint32_t smem_base = smem_u32(smem);
   auto sA = [&](int s) { return smem_base + static_cast<uint32_t>(s) * L.stage_bytes; };
@@ -604,6 +668,15 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
             red_i[q * N + c0 + lane] = t.i;
             red_s[q * N + c0 + lane] = t.s;
           }
+        } else if constexpr (MODE == MODE_GATED) {
+          int32_t i16;
+          const Top2 t = xp_gated(xp, lane, vt * kBM + q * 32, p.round_fp16 != 0, i16);
+          if (lane < 16) {
+            red_m[q * N + c0 + lane] = t.m;
+            red_i[q * N + c0 + lane] = t.i;
+            red_s[q * N + c0 + lane] = t.s;
+            red_b[q * N + c0 + lane] = i16;
+          }
         } else {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -632,7 +705,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           reinterpret_cast<int32_t*>(p.rec_m)[o] = r.m;
           p.rec_i[o] = r.i;
           reinterpret_cast<int32_t*>(p.rec_s)[o] = r.s;
-        } else if constexpr (MODE == MODE_GREEDY) {
+        } else if constexpr (MODE == MODE_GREEDY || MODE == MODE_GATED) {
           Top2 t[4];
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq)
@@ -641,6 +714,13 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           p.rec_m[o] = r.m;
           p.rec_i[o] = r.i;
           p.rec_s[o] = r.s;
+          if constexpr (MODE == MODE_GATED) {
+            const bool f16 = p.round_fp16 != 0;
+            Low16 b[4];
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) b[qq] = Low16{round16(t[qq].m, f16), red_b[qq * N + c]};
+            p.rec_b[o] = low16_merge(low16_merge(b[0], b[1]), low16_merge(b[2], b[3])).i;
+          }
         } else {
           Lse t[4];
 #pragma unroll
@@ -718,6 +798,43 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
       p.token[n] = tot.i;
       p.gap[n] = gap_ulp_bf16(tot.m, tot.s);
       accept_fold(p.acc, n, tot.i);
+    }
+  } else if constexpr (MODE == MODE_GATED) {
+    // the greedy fold and, beside it, the lowest index of the rounded maximum
+    __shared__ Top2 part[4];
+    __shared__ Low16 partb[4];
+    const bool f16 = p.round_fp16 != 0;
+    Top2 acc{-INFINITY, INT32_MAX, -INFINITY};
+    Low16 accb{-INFINITY, INT32_MAX};
+    for (int t0 = g; t0 < p.n_vt; t0 += kMergeThreads * kMergeBatch) {
+      Top2 r[kMergeBatch];
+      Low16 rb[kMergeBatch];
+#pragma unroll
+      for (int j = 0; j < kMergeBatch; ++j) {
+        const int t = t0 + j * kMergeThreads;
+        r[j] = t < p.n_vt ? Top2{p.rec_m[base + t], p.rec_i[base + t], p.rec_s[base + t]}
+                          : Top2{-INFINITY, INT32_MAX, -INFINITY};
+        rb[j] = t < p.n_vt ? Low16{round16(r[j].m, f16), p.rec_b[base + t]}
+                           : Low16{-INFINITY, INT32_MAX};
+      }
+#pragma unroll
+      for (int j = 0; j < kMergeBatch; ++j) {
+        acc = top2_merge(acc, r[j]);
+        accb = low16_merge(accb, rb[j]);
+      }
+    }
+    const Top2 tot = block_tree128(acc, top2_merge, part);
+    const Low16 totb = block_tree128(accb, low16_merge, partb);
+    if (g == 0) {
+      // margin of the rounded logits: round16 of the top two values
+      const float margin = __fsub_rn(round16(tot.m, f16), round16(tot.s, f16));
+      const bool fired = margin < p.tau;
+      const int32_t tok = fired ? tot.i : totb.i;
+      p.token[n] = tok;
+      p.gap[n] = gap_ulp_bf16(tot.m, tot.s);
+      if (p.base_token != nullptr) p.base_token[n] = totb.i;
+      if (p.margin != nullptr) p.margin[n] = margin;
+      accept_fold(p.acc, n, tok);
     }
   } else {
     __shared__ Lse part[4];

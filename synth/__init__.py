@@ -83,7 +83,8 @@ def pr1(n_rows: int = 16, V: int = 32000, d: int = 2048):
 
 
 def _next_bf16_bits(bits: np.uint16, up: bool) -> np.uint16:
-    """Neighbouring bf16 value, one ulp larger (up) or smaller in value."""
+    """Neighbouring value, one ulp larger (up) or smaller in value, of a
+    16-bit sign-magnitude format (bf16 or fp16, finite non-extreme values)."""
     b = int(bits)
     neg = bool(b & 0x8000)
     mag = b & 0x7FFF
@@ -204,11 +205,16 @@ def int8_head(V: int = 128256, d: int = 4096, B: int = 512, n_dup: int = 8):
 
 
 def small_float(seed: int, V: int, d: int, B: int, fmt: str = "bf16",
-                sigma_w: float = 0.02, sigma_h: float = 1.0, n_ties: int = 0):
-    """Small float case for parity tests: ragged V and d, optional exact ties.
+                sigma_w: float = 0.02, sigma_h: float = 1.0, n_ties: int = 0,
+                n_near: int = 0):
+    """Small float case for parity tests: ragged V and d, optional exact ties
+    and near ties.
 
     Exact ties copy a W row; hidden rows 0..n_ties-1 are then drawn close to
-    the copied row so the tie is the winner.
+    the copied row so the tie is the winner. Near ties (hidden rows n_ties ..
+    n_ties+n_near-1) copy a W row with one or two elements moved by one step
+    of the storage format, so the two best logits differ by far less than a
+    16-bit step of their value.
     """
     rng = _rng(seed)
     Wf = _normal_f32(rng, (V, d), sigma_w)
@@ -219,6 +225,16 @@ def small_float(seed: int, V: int, d: int, B: int, fmt: str = "bf16",
     for k in range(min(n_ties, B) if V >= 2 else 0):
         a, b = (int(x) for x in rng.choice(V, size=2, replace=False))
         W[b] = W[a]
+        wa = (W[a].astype(np.uint32) << 16).view(np.float32) if fmt == "bf16" \
+            else W[a].view(np.float16).astype(np.float32)
+        h[k] = conv(np.float32(40.0) * wa / np.float32(np.linalg.norm(wa) + 1e-30)
+                    + _normal_f32(rng, (d,), 0.01))
+    for k in range(n_ties, min(n_ties + n_near, B) if V >= 2 else 0):
+        a, b = (int(x) for x in rng.choice(V, size=2, replace=False))
+        row = W[a].copy()
+        for p in rng.choice(d, size=min(1 + (k % 2), d), replace=False):
+            row[p] = _next_bf16_bits(row[p], bool(rng.integers(0, 2)))
+        W[b] = row
         wa = (W[a].astype(np.uint32) << 16).view(np.float32) if fmt == "bf16" \
             else W[a].view(np.float16).astype(np.float32)
         h[k] = conv(np.float32(40.0) * wa / np.float32(np.linalg.norm(wa) + 1e-30)
