@@ -1,6 +1,7 @@
 """Benchmark of the batch-invariant output head on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload pr1|sweep|spec|logprob|int8]
+    python bench.py [--gpus N] [--steps K] [--warmup W]
+                    [--workload pr1|sweep|spec|logprob|int8|gated|verify]
                     [--impl ours|reference]
 
 Prints ONE JSON line. A step is one pass of the whole hot path over one batch
@@ -13,7 +14,11 @@ of synthetic input:
   B = 1, 2, 3, 8, 17, 64;
 * spec: speculative-verify block, bf16 d=3584, V=152064, B=256, with logits;
 * logprob: trainer scoring, bf16 d=1536, V=151936, 8192 rows, target logp;
-* int8: the integer head d=4096, V=128256 at --batch rows (default 512).
+* int8: the integer head d=4096, V=128256 at --batch rows (default 512);
+* gated: the pr1 calls through the margin-gated greedy call (tau = 0.001),
+  adding the rounded head's token and its top-two margin per row;
+* verify: the spec block through the speculative-verify call, 16 requests
+  x 16 drafted positions, adding the accepted length per request.
 
 value = rows/s for the whole job (all ranks); inputs resident in HBM. Several
 copies of W rotate so that every call streams W from HBM (their total is
@@ -57,7 +62,15 @@ WORKLOADS = {
                     mode="logprob", bound="tensor"),
     "int8": dict(desc="integer-only head: int8 d=4096 V=128256, exact int32 logits + token",
                  fmt="int8", V=128256, d=4096, mode="greedy", bound="hbm"),
+    "gated": dict(desc="margin-gated greedy decode (tau=0.001): bf16 head d=2048 V=32000, "
+                       "16 independent B=1 rows, fp32 logits + token + gap + bf16-head token "
+                       "+ margin", fmt="bf16", V=32000, d=2048, mode="gated", bound="hbm"),
+    "verify": dict(desc="greedy speculative verify: bf16 head d=3584 V=152064, 16 requests x "
+                        "16 drafted positions, logits + token + gap + accepted length",
+                   fmt="bf16", V=152064, d=3584, B=256, mode="verify", bound="tensor"),
 }
+GATE_TAU = 0.001
+SEED_DRAFTS = 3103
 
 
 # ------------------------------------------------------------------ helpers
@@ -187,7 +200,7 @@ def job_rows_per_s(rows_per_step: int, steps: int, world: int, elapsed_ms: float
 
 def make_inputs(name: str, batch: int):
     import synth
-    if name == "pr1":
+    if name in ("pr1", "gated"):
         c = synth.pr1()
         c["calls"] = [(r, 1) for r in range(c["h"].shape[0])]
     elif name == "sweep":
@@ -197,9 +210,14 @@ def make_inputs(name: str, batch: int):
             for r0 in range(0, 64, B):
                 calls.append((r0, min(B, 64 - r0)))
         c["calls"] = calls
-    elif name == "spec":
+    elif name in ("spec", "verify"):
         c = synth.spec_verify()
         c["calls"] = [(0, 256)]
+        if name == "verify":
+            # drafts planted on a seeded stand-in sequence (acceptance does not
+            # change the work of the call)
+            seq = np.random.default_rng(SEED_DRAFTS).integers(0, c["V"], size=(16, 16))
+            c["drafts"], _ = synth.plant_drafts(seq, c["V"], seed=SEED_DRAFTS + 1)
     elif name == "logprob":
         c = synth.logprob()
         c["calls"] = [(0, c["h"].shape[0])]
@@ -216,10 +234,15 @@ def algorithmic(name, c, B):
     V, d = c["V"], c["d"]
     eb = 1 if c["dtype"] == "int8" else 2
     by = V * d * eb + B * d * eb
-    if WORKLOADS[name]["mode"] == "greedy":
-        by += B * V * 4 + B * 8          # logits + token + gap
-    else:
+    mode = WORKLOADS[name]["mode"]
+    if mode == "logprob":
         by += B * 8                      # targets + logp
+    else:
+        by += B * V * 4 + B * 8          # logits + token + gap
+    if mode == "gated":
+        by += B * 8                      # rounded head's token + margin
+    if mode == "verify":
+        by += B * 4 + (B // 16) * 4      # drafts + accepted
     return by, 2.0 * B * V * d
 
 
@@ -257,17 +280,25 @@ def run_ours(args, rank, world, local_rank):
     maxB = max(B for _, B in calls)
     for hd in heads:
         bd.detlm_head_reserve(hd.handle, maxB)
-    greedy = spec["mode"] == "greedy"
+    mode = spec["mode"]
+    greedy = mode != "logprob"
     gdt = torch.int32 if fmt == "int8" else torch.float32
     outs = []
     for r0, B in calls:
         if greedy:
-            outs.append((torch.empty(B, dtype=torch.int32, device=dev),
-                         torch.empty(B, dtype=gdt, device=dev),
-                         torch.empty((B, V), dtype=gdt, device=dev)))
+            o = [torch.empty(B, dtype=torch.int32, device=dev),
+                 torch.empty(B, dtype=gdt, device=dev),
+                 torch.empty((B, V), dtype=gdt, device=dev)]
+            if mode == "gated":
+                o += [torch.empty(B, dtype=torch.int32, device=dev),
+                      torch.empty(B, dtype=torch.float32, device=dev)]
+            if mode == "verify":
+                o += [torch.empty(B // 16, dtype=torch.int32, device=dev)]
+            outs.append(tuple(o))
         else:
             outs.append(torch.empty(B, dtype=torch.float32, device=dev))
     targets = torch.from_numpy(c["targets"]).to(dev) if not greedy else None
+    drafts = torch.from_numpy(c["drafts"]).to(dev) if mode == "verify" else None
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     n_calls = len(calls)
@@ -280,10 +311,20 @@ def run_ours(args, rank, world, local_rank):
             if ev is not None and ev[j] is not None:
                 bd.detlm_head_time_next(hd.handle, ev[j][0].cuda_event, ev[j][1].cuda_event)
             hv = h_all[r0:r0 + B]
-            if greedy:
+            if mode == "greedy":
                 tok, gap, lg = outs[j]
                 bd.detlm_head_greedy(hd.handle, hv.data_ptr(), B, tok.data_ptr(),
                                      gap.data_ptr(), lg.data_ptr(), sp)
+            elif mode == "gated":
+                tok, gap, lg, base, margin = outs[j]
+                bd.detlm_head_greedy_gated(hd.handle, hv.data_ptr(), B, GATE_TAU, tok.data_ptr(),
+                                           gap.data_ptr(), lg.data_ptr(), base.data_ptr(),
+                                           margin.data_ptr(), sp)
+            elif mode == "verify":
+                tok, gap, lg, acc = outs[j]
+                bd.detlm_head_verify(hd.handle, hv.data_ptr(), B // 16, 16, drafts.data_ptr(),
+                                     tok.data_ptr(), gap.data_ptr(), lg.data_ptr(),
+                                     acc.data_ptr(), sp)
             else:
                 bd.detlm_head_logprob(hd.handle, hv.data_ptr(), targets[r0:r0 + B].data_ptr(),
                                       B, outs[j].data_ptr(), sp)
@@ -399,19 +440,23 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
     }
     if rank == 0 and not args.profile:
-        res["e2e"] = run_e2e(args, c, heads, calls, greedy, rows_per_step, dev, stream)
+        res["e2e"] = run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream)
         res["cpu_baseline"] = cpu_baseline(args.workload, c, budget_s=args.cpu_seconds)
     if args.profile:
         res["profile_run"] = "e2e and cpu_baseline legs skipped (--profile)"
     return res
 
 
-def run_e2e(args, c, heads, calls, greedy, rows_per_step, dev, stream):
-    """Same metric through the host-buffer entry points: pinned host inputs are
-    copied in and the results copied out on every call."""
+def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
+    """Same metric end to end: pinned host inputs are copied in and the
+    results copied out on every call. The greedy and log-prob calls go
+    through their host-buffer entry points; the gated and verify calls, which
+    have none, through their device entry points between explicit copies on
+    the same stream."""
     import torch
     from invariant_output_head_gb300 import binding as bd
     fmt, V = c["dtype"], c["V"]
+    greedy = mode != "logprob"
     h_host = torch.from_numpy(np.ascontiguousarray(
         c["h"].view(np.int16) if fmt != "int8" else c["h"])).pin_memory()
     esz = h_host.element_size()
@@ -422,19 +467,49 @@ def run_e2e(args, c, heads, calls, greedy, rows_per_step, dev, stream):
     lg = torch.empty((maxB, V), dtype=torch.int32).pin_memory() if greedy else None
     lp = torch.empty(maxB, dtype=torch.float32).pin_memory()
     tg = torch.from_numpy(c["targets"]).pin_memory() if not greedy else None
+    extra = torch.empty(2 * maxB, dtype=torch.int32).pin_memory()   # base+margin / accepted
     sp = stream.cuda_stream
     steps = max(3, min(args.steps, int(args.e2e_seconds / 0.002)))
+    if mode in ("gated", "verify"):
+        tdt = {"bf16": torch.bfloat16, "fp16": torch.float16}[fmt]
+        h_dev = torch.empty((maxB, d), dtype=tdt, device=dev)
+        o_dev = [torch.empty(maxB, dtype=torch.int32, device=dev),
+                 torch.empty(maxB, dtype=torch.float32, device=dev),
+                 torch.empty((maxB, V), dtype=torch.float32, device=dev),
+                 torch.empty(2 * maxB, dtype=torch.int32, device=dev)]
+        dr_host = (torch.from_numpy(c["drafts"]).pin_memory() if mode == "verify" else None)
+        dr_dev = torch.empty(maxB, dtype=torch.int32, device=dev)
 
     def one_step(i):
         for j, (r0, B) in enumerate(calls):
             hd = heads[(i * len(calls) + j) % len(heads)]
             hp = h_host.data_ptr() + r0 * d * esz
-            if greedy:
+            if mode == "greedy":
                 bd.detlm_head_greedy_host(hd.handle, hp, B, tok.data_ptr(), gap.data_ptr(),
                                           lg.data_ptr(), sp)
-            else:
+            elif mode == "logprob":
                 bd.detlm_head_logprob_host(hd.handle, hp, tg.data_ptr() + r0 * 4, B,
                                            lp.data_ptr(), sp)
+            else:
+                with torch.cuda.stream(stream):
+                    h_dev[:B].view(torch.int16).copy_(h_host[r0:r0 + B], non_blocking=True)
+                    if mode == "gated":
+                        bd.detlm_head_greedy_gated(
+                            hd.handle, h_dev.data_ptr(), B, GATE_TAU, o_dev[0].data_ptr(),
+                            o_dev[1].data_ptr(), o_dev[2].data_ptr(), o_dev[3].data_ptr(),
+                            o_dev[3].data_ptr() + 4 * B, sp)
+                        n_extra = 2 * B
+                    else:
+                        dr_dev[:B].copy_(dr_host.view(-1)[:B], non_blocking=True)
+                        bd.detlm_head_verify(
+                            hd.handle, h_dev.data_ptr(), B // 16, 16, dr_dev.data_ptr(),
+                            o_dev[0].data_ptr(), o_dev[1].data_ptr(), o_dev[2].data_ptr(),
+                            o_dev[3].data_ptr(), sp)
+                        n_extra = B // 16
+                    tok[:B].copy_(o_dev[0][:B], non_blocking=True)
+                    gap[:B].view(torch.float32).copy_(o_dev[1][:B], non_blocking=True)
+                    lg[:B].view(torch.float32).copy_(o_dev[2][:B], non_blocking=True)
+                    extra[:n_extra].copy_(o_dev[3][:n_extra], non_blocking=True)
     for i in range(3):
         one_step(i)
     torch.cuda.synchronize()
@@ -443,11 +518,15 @@ def run_e2e(args, c, heads, calls, greedy, rows_per_step, dev, stream):
         one_step(i)
     torch.cuda.synchronize()
     dt = time.perf_counter() - t
-    h2d = sum(B * d * esz + (0 if greedy else 4 * B) for _, B in calls)
-    d2h = sum((8 * B + 4 * B * V) if greedy else 4 * B for _, B in calls)
+    h2d = sum(B * d * esz + (4 * B if mode in ("logprob", "verify") else 0) for _, B in calls)
+    d2h = sum(4 * B if mode == "logprob" else 8 * B + 4 * B * V for _, B in calls)
+    d2h += sum(8 * B if mode == "gated" else (4 * (B // 16) if mode == "verify" else 0)
+               for _, B in calls)
+    api = {"greedy": "detlm_head_greedy_host", "logprob": "detlm_head_logprob_host",
+           "gated": "detlm_head_greedy_gated + pinned copies on the call's stream",
+           "verify": "detlm_head_verify + pinned copies on the call's stream"}[mode]
     return {"value": round(rows_per_step * steps / dt, 2), "unit": "rows/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "api": "detlm_head_greedy_host" if greedy else "detlm_head_logprob_host"}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps, "api": api}
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -469,14 +548,28 @@ def oracle_rows_per_s(name, c, budget_s, max_rows=None):
     t0 = time.perf_counter()
     while True:
         r = n % h.shape[0]
-        if WORKLOADS[name]["mode"] == "greedy":
-            oracle.head_greedy(c["W"], h[r:r + 1], fmt)
-        else:
-            oracle.head_logprob(c["W"], h[r:r + 1], c["targets"][r:r + 1], fmt)
+        oracle_row(name, c, r)
         n += 1
         dt = time.perf_counter() - t0
         if dt >= budget_s or (max_rows is not None and n >= max_rows):
             return n / dt, n, dt
+
+
+def oracle_row(name, c, r):
+    """The oracle on row r of the workload: what one row of the call computes."""
+    import oracle
+    fmt, h, mode = c["dtype"], c["h"], WORKLOADS[name]["mode"]
+    if mode == "logprob":
+        return oracle.head_logprob(c["W"], h[r:r + 1], c["targets"][r:r + 1], fmt)
+    out = oracle.head_greedy(c["W"], h[r:r + 1], fmt)
+    if mode == "gated":
+        out["gate"] = oracle.gated_greedy(out["logits"], GATE_TAU, fmt)
+    if mode == "verify":
+        # the row's comparison with its draft (the request's accepted length
+        # is a prefix scan over its 16 rows)
+        out["accept"] = oracle.verify_accept(out["token"].reshape(1, 1),
+                                             c["drafts"].reshape(-1, 1)[r:r + 1])
+    return out
 
 
 def cpu_baseline(name, c, budget_s):
@@ -491,17 +584,11 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     c = make_inputs(args.workload, args.batch)
-    import oracle
     fmt = c["dtype"]
-    greedy = WORKLOADS[args.workload]["mode"] == "greedy"
     h = c["h"]
 
     def one(i):
-        r = i % h.shape[0]
-        if greedy:
-            oracle.head_greedy(c["W"], h[r:r + 1], fmt)
-        else:
-            oracle.head_logprob(c["W"], h[r:r + 1], c["targets"][r:r + 1], fmt)
+        oracle_row(args.workload, c, i % h.shape[0])
     for i in range(args.warmup):
         one(i)
     # bound the timed work to a few minutes of CPU time
