@@ -18,7 +18,9 @@ Everything is computed exactly or in float64 with numpy:
   log-probability of a target;
 * the accepted draft length of greedy speculative verification;
 * the margin-gated decision: rounding of the logits to bf16 / fp16, the
-  rounded head's token and top-two margin, the gate and the gated token.
+  rounded head's token and top-two margin, the gate and the gated token;
+* seeded Gumbel-max sampling: the Philox4x32-10 generator, the uniform and
+  Gumbel transforms and the sampled token.
 
 Parity pins: every function here is pinned by tests that do not re-use its
 own formula (hand-worked tiny cases, brute force with exact rationals,
@@ -32,4 +34,5 @@ from .head import (  # noqa: F401
     logsumexp, logprob,
     head_greedy, head_logprob, verify_accept,
     round_to_format, gated_greedy,
+    philox4x32_10, uniform_from_word, gumbel_rows, gumbel_noise, sample,
 )

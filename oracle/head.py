@@ -26,6 +26,10 @@ Sources, by page title:
   at such a step the output projection is recomputed in FP32 and the token is
   taken from that. The ordinary head is a 16-bit one, so its logits are the
   16-bit roundings of the products' sums.
+* [Exactness] section 12.5 (Sampling): a request with a seed draws
+  the token at index t as the argmax of log p_t + G_t, G_t Gumbel noise from
+  a generator seeded by (seed, t) -- an exact sample from p_t that does not
+  depend on what else was computed. [Decoding] section 3: p = softmax(z/T).
 * [Decoding] section 6 (Speculative decoding): the target scores all drafted
   positions in one forward pass and keeps the drafted tokens while they agree
   with it; [Exactness] 12.1: greedy speculative output equals plain greedy
@@ -51,7 +55,14 @@ Readings where the pages are silent (each also listed with the design notes):
   difference of the two largest rounded values of the multiset (zero on a
   tie), rounded once to float32; the gate fires when margin < tau (tau and
   the comparison in float32); a fired row takes the FP32 recompute over the
-  full vocabulary, i.e. the argmax of the unrounded logits.
+  full vocabulary, i.e. the argmax of the unrounded logits;
+* seeded sampling: the pages name no generator. Philox4x32-10 (Salmon et al.,
+  "Parallel random numbers: as easy as 1, 2, 3", SC'11) keyed by the 64-bit
+  seed (low word first); entry v of position t takes word (v mod 4) of the
+  block with counter (v div 4, t low word, t high word, 0); a word x maps to
+  the uniform U = (2 floor(x / 2^9) + 1) 2^-24 in (0, 1), exact in float32;
+  G = -log(-log U). log p_t + G differs from z/T + G by a constant per row,
+  so the sample is the argmax of z/T + G (lowest index on a tie).
 """
 from __future__ import annotations
 
@@ -327,3 +338,77 @@ def gated_greedy(z: np.ndarray, tau: float, fmt: str) -> dict:
     full = np.argmax(z, axis=1).astype(np.int64)
     token = np.where(fired, full, base)
     return {"token": token, "base": base, "margin": margin, "fired": fired}
+
+
+# --------------------------------------------------------------------------
+# Seeded Gumbel-max sampling
+# --------------------------------------------------------------------------
+
+_M32 = np.uint64(0xFFFFFFFF)
+PHILOX_M = (np.uint64(0xD2511F53), np.uint64(0xCD9E8D57))
+PHILOX_W = (np.uint64(0x9E3779B9), np.uint64(0xBB67AE85))
+
+
+def philox4x32_10(counter, key) -> np.ndarray:
+    """Philox4x32 with 10 rounds (Salmon et al., SC'11), vectorised.
+
+    counter [..., 4] and key [..., 2] of 32-bit words (any integer dtype);
+    returns [..., 4] uint32. One round: the products M0 * c0 and M1 * c2
+    (64-bit, exact in uint64) give the new block (hi(M1 c2) ^ c1 ^ k0,
+    lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)); the key then advances by the
+    Weyl increments (mod 2^32).
+    """
+    c = np.asarray(counter, dtype=np.uint64) & _M32
+    k = np.asarray(key, dtype=np.uint64) & _M32
+    c0, c1, c2, c3 = c[..., 0], c[..., 1], c[..., 2], c[..., 3]
+    k0, k1 = k[..., 0], k[..., 1]
+    for _ in range(10):
+        p0 = PHILOX_M[0] * c0
+        p1 = PHILOX_M[1] * c2
+        c0, c1, c2, c3 = ((p1 >> np.uint64(32)) ^ c1 ^ k0, p1 & _M32,
+                          (p0 >> np.uint64(32)) ^ c3 ^ k1, p0 & _M32)
+        k0 = (k0 + PHILOX_W[0]) & _M32
+        k1 = (k1 + PHILOX_W[1]) & _M32
+    return np.stack([c0, c1, c2, c3], axis=-1).astype(np.uint32)
+
+
+def uniform_from_word(x) -> np.ndarray:
+    """U = (2 * (x >> 9) + 1) * 2^-24: 2^23 equally spaced values in (0, 1),
+    each exact in float32 (and float64)."""
+    x = np.asarray(x, dtype=np.uint64)
+    return ((x >> np.uint64(9)) * np.uint64(2) + np.uint64(1)).astype(np.float64) * 2.0 ** -24
+
+
+def gumbel_rows(seeds, positions, V: int) -> np.ndarray:
+    """G[n, v] = -log(-log U) for the (seed_n, position_n) of each row."""
+    seeds = [int(x) for x in np.asarray(seeds).reshape(-1)]
+    pos = [int(x) for x in np.asarray(positions).reshape(-1)]
+    B = len(seeds)
+    v = np.arange(V, dtype=np.uint64)[None, :].repeat(B, axis=0)
+    t_lo = np.array([t & 0xFFFFFFFF for t in pos], dtype=np.uint64)[:, None].repeat(V, axis=1)
+    t_hi = np.array([(t >> 32) & 0xFFFFFFFF for t in pos], dtype=np.uint64)[:, None].repeat(V, axis=1)
+    counter = np.stack([v >> np.uint64(2), t_lo, t_hi, np.zeros_like(v)], axis=-1)
+    k_lo = np.array([x & 0xFFFFFFFF for x in seeds], dtype=np.uint64)[:, None].repeat(V, axis=1)
+    k_hi = np.array([(x >> 32) & 0xFFFFFFFF for x in seeds], dtype=np.uint64)[:, None].repeat(V, axis=1)
+    words = philox4x32_10(counter, np.stack([k_lo, k_hi], axis=-1))
+    x = np.take_along_axis(words, (v & np.uint64(3)).astype(np.int64)[..., None], axis=-1)[..., 0]
+    return -np.log(-np.log(uniform_from_word(x)))
+
+
+def gumbel_noise(seed: int, t: int, V: int) -> np.ndarray:
+    """G_v = -log(-log U_v), v = 0 .. V-1, for one (seed, position)."""
+    return gumbel_rows([seed], [t], V)[0]
+
+
+def sample(z: np.ndarray, temperature: float, seeds, positions) -> dict:
+    """Seeded Gumbel-max sample per row ([Exactness] 12.5, [Decoding] 3).
+
+    score[n, v] = z[n, v] / T + G(seed_n, t_n)_v in float64; token = lowest
+    index of the maximum score; also the best and runner-up scores (the
+    runner-up of the multiset), whose difference says how near the draw was
+    to going the other way.
+    """
+    z = np.asarray(z, dtype=np.float64)
+    score = z / float(temperature) + gumbel_rows(seeds, positions, z.shape[1])
+    token, m, s = top2(score)
+    return {"token": token, "m": m, "s": s, "score": score}

@@ -502,10 +502,112 @@ def pin_gated_greedy(o):
                 assert (g["token"] == np.array([loop_argmax_lowest(list(r)) for r in z])).all()
 
 
+# ---- seeded sampling
+
+def read_philox_kat():
+    out = []
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            w = [int(x, 16) for x in line.split()]
+            out.append((w[0:4], w[4:6], w[6:10]))
+    return out
+
+
+def _philox_py(c, k):
+    """Philox4x32-10 on Python integers (a second route, checked by the same
+    published vectors as the oracle's)."""
+    M0, M1, W0, W1, MASK = 0xD2511F53, 0xCD9E8D57, 0x9E3779B9, 0xBB67AE85, 0xFFFFFFFF
+    c = list(c)
+    k0, k1 = k
+    for _ in range(10):
+        p0, p1 = M0 * c[0], M1 * c[2]
+        c = [(p1 >> 32) ^ c[1] ^ k0, p1 & MASK, (p0 >> 32) ^ c[3] ^ k1, p0 & MASK]
+        k0, k1 = (k0 + W0) & MASK, (k1 + W1) & MASK
+    return c
+
+
+def pin_philox_kat(o):
+    """The generator against the published known-answer vectors."""
+    for c, k, r in read_philox_kat():
+        assert o.philox4x32_10(np.array(c), np.array(k)).tolist() == r
+        assert _philox_py(c, k) == r
+
+
+def pin_gumbel_layout(o):
+    """Uniform map and the (seed, t, v) -> word layout of the stated reading,
+    from the Python-integer generator and math.log; the first block of seed 0,
+    position 0 is the published all-zero vector."""
+    u = o.uniform_from_word(np.array([0, 0xFFFFFFFF, 0x80000000, 511, 512]))
+    assert u.tolist() == [2.0 ** -24, 1 - 2.0 ** -24, 0.5 + 2.0 ** -24, 2.0 ** -24, 3 * 2.0 ** -24]
+    kat0 = read_philox_kat()[0][2]
+    g = o.gumbel_noise(0, 0, 4)
+    for v in range(4):
+        U = ((kat0[v] >> 9) * 2 + 1) * 2.0 ** -24
+        assert abs(g[v] - (-math.log(-math.log(U)))) <= 1e-15 * (1 + abs(g[v]))
+    for seed, t, V in ((1, 0, 9), (0x123456789ABCDEF0, 77, 6), (5, (3 << 32) + 11, 5)):
+        g = o.gumbel_noise(seed, t, V)
+        for v in range(V):
+            w = _philox_py([v >> 2, t & 0xFFFFFFFF, t >> 32, 0],
+                           [seed & 0xFFFFFFFF, seed >> 32])[v & 3]
+            U = ((w >> 9) * 2 + 1) * 2.0 ** -24
+            assert abs(g[v] - (-math.log(-math.log(U)))) <= 1e-15 * (1 + abs(g[v])), (seed, t, v)
+
+
+def pin_gumbel_max_distribution(o):
+    """Gumbel-max gives exact samples of softmax(z / T) ([Exactness] 12.5):
+    chi-square of 24,000 seeded draws against softmax(z / T) at two
+    temperatures, and the Gumbel law's mean (Euler's constant) and variance
+    (pi^2 / 6) over the noise itself."""
+    z = np.array([[1.0, 0.2, -0.5, 2.0, 0.0, 1.5]])
+    n = 24000
+    for T, seed in ((1.0, 7), (0.5, 8)):
+        tok = o.sample(np.repeat(z, n, axis=0), T, [seed] * n, list(range(n)))["token"]
+        counts = np.bincount(tok, minlength=6).astype(np.float64)
+        p = np.exp(z[0] / T - np.max(z[0] / T))
+        p /= p.sum()
+        chi2 = float(np.sum((counts - n * p) ** 2 / (n * p)))
+        assert chi2 < 20.5, (T, chi2, counts, n * p)      # df = 5, p = 0.001
+    G = np.concatenate([o.gumbel_noise(3, t, 1000) for t in range(40)])
+    assert abs(G.mean() - 0.5772156649) < 0.02
+    assert abs(G.var() - math.pi ** 2 / 6) < 0.05
+
+
+def pin_sample_invariants(o):
+    """Rows are independent (same seed and position, same draw, whatever the
+    other rows); a tiny temperature gives the greedy token; a tie of scores
+    goes to the lower index."""
+    rng = np.random.default_rng(31)
+    z = rng.normal(0, 2, size=(5, 40))
+    seeds, pos = [11, 12, 11, 13, 11], [0, 0, 0, 1, 5]
+    joint = o.sample(z, 0.8, seeds, pos)
+    for n in range(5):
+        one = o.sample(z[n:n + 1], 0.8, seeds[n:n + 1], pos[n:n + 1])
+        assert one["token"][0] == joint["token"][n] and one["m"][0] == joint["m"][n]
+    zz = np.stack([z[0], z[0]])
+    two = o.sample(zz, 0.8, [11, 11], [0, 0])
+    assert two["token"][0] == two["token"][1] == joint["token"][0]
+    diff = o.sample(zz, 0.8, [11, 12], [0, 0])
+    assert diff["m"][0] != diff["m"][1]           # the seed keys the noise
+    later = o.sample(zz, 0.8, [11, 11], [0, 1])
+    assert later["m"][0] != later["m"][1]         # so does the position
+    cold = o.sample(z, 1e-9, seeds, pos)
+    assert (cold["token"] == np.argmax(z, axis=1)).all()
+    # an exact tie of scores: duplicate columns with equal noise cannot be
+    # arranged, so check the index rule on the returned scores
+    sc = joint["score"]
+    assert (joint["token"] == np.argmax(sc, axis=1)).all()
+    assert (joint["m"] >= joint["s"]).all()
+    assert (joint["m"] - joint["s"] == np.sort(sc, axis=1)[:, -1] - np.sort(sc, axis=1)[:, -2]).all()
+
+
 ALL_PINS = [pin_tiny_golden, pin_bruteforce_float, pin_logsumexp_mpmath,
             pin_closed_forms, pin_page_examples, pin_int_head, pin_invariants,
             pin_gap_from_top2, pin_verify_accept, pin_round_to_format,
-            pin_gated_greedy]
+            pin_gated_greedy, pin_philox_kat, pin_gumbel_layout,
+            pin_gumbel_max_distribution, pin_sample_invariants]
 
 
 def failing_pins(o):

@@ -61,6 +61,23 @@ MUTANTS = {
     "gate_fires_at_equality": ("    fired = margin < np.float32(tau)\n", "    fired = margin <= np.float32(tau)\n"),
     "gate_token_always_base": ("    token = np.where(fired, full, base)\n", "    token = base\n"),
     "gate_token_always_full": ("    token = np.where(fired, full, base)\n", "    token = full\n"),
+    "philox_no_key_bump": ("        k0 = (k0 + PHILOX_W[0]) & _M32\n", ""),
+    "philox_multipliers_swapped": ("        p0 = PHILOX_M[0] * c0\n        p1 = PHILOX_M[1] * c2\n",
+                                   "        p0 = PHILOX_M[1] * c0\n        p1 = PHILOX_M[0] * c2\n"),
+    "philox_nine_rounds": ("    for _ in range(10):\n        p0 = PHILOX_M[0] * c0", "    for _ in range(9):\n        p0 = PHILOX_M[0] * c0"),
+    "uniform_can_be_zero": ("((x >> np.uint64(9)) * np.uint64(2) + np.uint64(1)).astype(np.float64) * 2.0 ** -24",
+                            "(x >> np.uint64(8)).astype(np.float64) * 2.0 ** -24"),
+    "gumbel_layout_t_first": ("    counter = np.stack([v >> np.uint64(2), t_lo, t_hi, np.zeros_like(v)], axis=-1)",
+                              "    counter = np.stack([t_lo, v >> np.uint64(2), t_hi, np.zeros_like(v)], axis=-1)"),
+    "gumbel_word_zero": ("    x = np.take_along_axis(words, (v & np.uint64(3)).astype(np.int64)[..., None], axis=-1)[..., 0]",
+                         "    x = words[..., 0]"),
+    "gumbel_sign": ("    return -np.log(-np.log(uniform_from_word(x)))", "    return np.log(-np.log(uniform_from_word(x)))"),
+    "sample_temperature_multiplies": ("    score = z / float(temperature) + gumbel_rows",
+                                      "    score = z * float(temperature) + gumbel_rows"),
+    "sample_seed_ignored": ("gumbel_rows(seeds, positions, z.shape[1])",
+                            "gumbel_rows([0] * z.shape[0], positions, z.shape[1])"),
+    "sample_position_ignored": ("gumbel_rows(seeds, positions, z.shape[1])",
+                                "gumbel_rows(seeds, [0] * z.shape[0], z.shape[1])"),
     "gap_f32_rounded_difference": ("    with np.errstate(invalid=\"ignore\"):\n        return ((m - s) / ulp_bf16(m)).astype(np.float32)",
                                    "    with np.errstate(invalid=\"ignore\"):\n        return ((m - s) / ulp_bf16(s)).astype(np.float32)"),
 }
