@@ -379,10 +379,19 @@ def uniform_from_word(x) -> np.ndarray:
     return ((x >> np.uint64(9)) * np.uint64(2) + np.uint64(1)).astype(np.float64) * 2.0 ** -24
 
 
+def _u64_list(xs) -> list:
+    """64-bit keys as Python integers in [0, 2^64), element by element (a
+    list mixing values above and below 2^63 must not pass through a float
+    array; negative int64 values are read as their two's-complement bits)."""
+    if isinstance(xs, np.ndarray):
+        xs = xs.reshape(-1).tolist()
+    return [int(x) % (1 << 64) for x in xs]
+
+
 def gumbel_rows(seeds, positions, V: int) -> np.ndarray:
     """G[n, v] = -log(-log U) for the (seed_n, position_n) of each row."""
-    seeds = [int(x) for x in np.asarray(seeds).reshape(-1)]
-    pos = [int(x) for x in np.asarray(positions).reshape(-1)]
+    seeds = _u64_list(seeds)
+    pos = _u64_list(positions)
     B = len(seeds)
     v = np.arange(V, dtype=np.uint64)[None, :].repeat(B, axis=0)
     t_lo = np.array([t & 0xFFFFFFFF for t in pos], dtype=np.uint64)[:, None].repeat(V, axis=1)

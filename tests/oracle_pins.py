@@ -593,6 +593,18 @@ def pin_sample_invariants(o):
     assert diff["m"][0] != diff["m"][1]           # the seed keys the noise
     later = o.sample(zz, 0.8, [11, 11], [0, 1])
     assert later["m"][0] != later["m"][1]         # so does the position
+    big = [(1 << 64) - 3, 7, (1 << 63) + 12345]     # keys above and below 2^63 together
+    mixed = o.sample(z[:3], 0.8, big, [(1 << 40) + 1, 2, 3])
+    for n in range(3):
+        one = o.sample(z[n:n + 1], 0.8, big[n:n + 1], [[(1 << 40) + 1, 2, 3][n]])
+        assert one["m"][0] == mixed["m"][n]
+    g = o.gumbel_noise((1 << 64) - 3, 9, 4)
+    for v in range(4):
+        w = _philox_py([0, 9, 0, 0], [0xFFFFFFFD, 0xFFFFFFFF])[v]
+        assert abs(g[v] + math.log(-math.log(((w >> 9) * 2 + 1) * 2.0 ** -24))) < 1e-14
+    # int64 views of the same keys read as the same bits
+    assert o.sample(z[:1], 0.8, np.array([-3], np.int64), [9])["m"][0] == \
+        o.sample(z[:1], 0.8, [(1 << 64) - 3], [9])["m"][0]
     cold = o.sample(z, 1e-9, seeds, pos)
     assert (cold["token"] == np.argmax(z, axis=1)).all()
     # an exact tie of scores: duplicate columns with equal noise cannot be

@@ -78,6 +78,7 @@ MUTANTS = {
                             "gumbel_rows([0] * z.shape[0], positions, z.shape[1])"),
     "sample_position_ignored": ("gumbel_rows(seeds, positions, z.shape[1])",
                                 "gumbel_rows(seeds, [0] * z.shape[0], z.shape[1])"),
+    "sample_keys_through_float": ("    seeds = _u64_list(seeds)\n", "    seeds = [int(x) for x in np.asarray(seeds).reshape(-1)]\n"),
     "gap_f32_rounded_difference": ("    with np.errstate(invalid=\"ignore\"):\n        return ((m - s) / ulp_bf16(m)).astype(np.float32)",
                                    "    with np.errstate(invalid=\"ignore\"):\n        return ((m - s) / ulp_bf16(s)).astype(np.float32)"),
 }
