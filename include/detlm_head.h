@@ -137,6 +137,31 @@ int detlm_head_greedy_gated(detlm_head_t* head, const void* h_dev, int64_t B,
                             float* logits_dev, int32_t* base_token_dev,
                             float* margin_dev, cudaStream_t stream);
 
+/* Seeded sampling ("TandemLLM docs, 12 Exactness", 12.5; "Inference and
+ * Decoding", section 3): the token of row n is an exact sample of
+ * softmax(z_n / T), drawn as the argmax over v of z[n, v] / T + G_v with
+ * Gumbel noise G keyed by (seeds[n], positions[n]) alone, so a row draws the
+ * same token whatever B, its place in the batch or the other rows.
+ *
+ * Generator: Philox4x32-10 (Salmon et al., "Parallel random numbers: as easy
+ * as 1, 2, 3", SC'11), key = (seed low 32 bits, seed high 32 bits); entry v
+ * takes word (v mod 4) of the block with counter (v div 4, t low, t high, 0);
+ * word x gives U = (2 * (x >> 9) + 1) * 2^-24 in (0, 1) and G = -log(-log U).
+ * Scores in fp32: z / T correctly rounded, logf, one rounded add; the lowest
+ * index wins an exact tie of scores.
+ *
+ * Float heads only (INT8: DETLM_EUNSUPPORTED). temperature: finite and > 0
+ * (the greedy call is the T -> 0 limit), else DETLM_EINVAL.
+ * seeds_dev, positions_dev: uint64 [B], device, 8-byte aligned.
+ * token_dev int32 [B]; score_gap_dev (may be NULL) f32 [B]: the best minus
+ * the runner-up score, +inf if V == 1 (how close the draw came to another
+ * token); logits_dev (may be NULL): the unperturbed fp32 logits [B, V]. */
+int detlm_head_sample(detlm_head_t* head, const void* h_dev, int64_t B,
+                      float temperature, const uint64_t* seeds_dev,
+                      const uint64_t* positions_dev, int32_t* token_dev,
+                      float* score_gap_dev, float* logits_dev,
+                      cudaStream_t stream);
+
 /* Greedy speculative verify: the greedy call on n_req * P hidden rows (the P
  * verified positions of each request, request-major) that also returns the
  * accepted draft length of each request. The acceptance is folded into the

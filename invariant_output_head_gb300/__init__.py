@@ -12,7 +12,7 @@ from .binding import (  # noqa: F401
     detlm_head_greedy_host, detlm_head_logprob_host, detlm_head_check,
     detlm_head_time_next, detlm_head_debug, detlm_head_tiles, detlm_head_destroy,
     detlm_status_string, detlm_greedy_noalloc, detlm_head_verify,
-    detlm_head_greedy_gated,
+    detlm_head_greedy_gated, detlm_head_sample,
     DETLM_BF16, DETLM_FP16, DETLM_INT8, DETLM_OK, DETLM_EINVAL, DETLM_EUNSUPPORTED,
     DETLM_ECUDA, DETLM_ETIMEOUT, DETLM_ENOMEM, DETLM_ETARGET, DETLM_DEBUG_STALL,
 )

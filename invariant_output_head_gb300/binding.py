@@ -28,6 +28,7 @@ _SIGS = {
     "detlm_head_verify": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     "detlm_head_greedy_gated": (_i32, [_vp, _vp, _i64, ctypes.c_float, _vp, _vp, _vp, _vp, _vp,
                                        _vp]),
+    "detlm_head_sample": (_i32, [_vp, _vp, _i64, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp]),
     "detlm_head_greedy_host": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp]),
     "detlm_head_logprob_host": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
     "detlm_head_check": (_i32, [_vp, _vp]),
@@ -109,6 +110,14 @@ def detlm_head_greedy_gated(handle, h_ptr, B, tau, token_ptr, gap_ptr, logits_pt
                                                   logits_ptr, base_token_ptr, margin_ptr,
                                                   stream),
            "detlm_head_greedy_gated")
+
+
+def detlm_head_sample(handle, h_ptr, B, temperature, seeds_ptr, positions_ptr, token_ptr,
+                      score_gap_ptr, logits_ptr, stream) -> None:
+    _check(load_library().detlm_head_sample(handle, h_ptr, B, temperature, seeds_ptr,
+                                            positions_ptr, token_ptr, score_gap_ptr, logits_ptr,
+                                            stream),
+           "detlm_head_sample")
 
 
 def detlm_head_verify(handle, h_ptr, n_req, P, drafts_ptr, token_ptr, gap_ptr, logits_ptr,
@@ -252,6 +261,26 @@ class Head:
                                 gap.data_ptr(), logits.data_ptr() if logits is not None else None,
                                 base.data_ptr(), margin.data_ptr(), _stream_ptr(stream))
         return token, gap, logits, base, margin
+
+    def sample(self, h, temperature, seeds, positions, with_logits: bool = False, stream=None):
+        """Seeded sampling. seeds, positions: int64/uint64 CUDA tensors [B]
+        (read as unsigned 64-bit). Returns (token, score_gap, logits or None)."""
+        import torch
+        self._check_h(h)
+        B = int(h.shape[0])
+        for name, t in (("seeds", seeds), ("positions", positions)):
+            if (not t.is_cuda or t.dim() != 1 or int(t.shape[0]) != B
+                    or t.element_size() != 8 or t.is_floating_point()):
+                raise ValueError(f"{name} must be a 64-bit integer CUDA tensor [B]")
+        token = torch.empty(B, dtype=torch.int32, device=h.device)
+        gap = torch.empty(B, dtype=torch.float32, device=h.device)
+        logits = (torch.empty((B, self.V), dtype=torch.float32, device=h.device)
+                  if with_logits else None)
+        detlm_head_sample(self.handle, h.data_ptr(), B, float(temperature),
+                          seeds.contiguous().data_ptr(), positions.contiguous().data_ptr(),
+                          token.data_ptr(), gap.data_ptr(),
+                          logits.data_ptr() if logits is not None else None, _stream_ptr(stream))
+        return token, gap, logits
 
     def verify(self, h, drafts, with_logits: bool = False, stream=None):
         """Greedy speculative verify. h [R*P, d] request-major, drafts int32

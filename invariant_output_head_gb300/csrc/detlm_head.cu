@@ -238,13 +238,21 @@ cudaError_t launch_gemm(const CUtensorMap& tmW, const CUtensorMap& tmH, const He
   }
 }
 
-// margin gate of the gated greedy call
-struct GateArgs { float tau; int32_t* base_token; float* margin; };
+// arguments of the gated greedy call and of the sampling call
+struct ModeArgs {
+  float tau = 0.0f;
+  int32_t* base_token = nullptr;
+  float* margin = nullptr;
+  const uint64_t* seeds = nullptr;
+  const uint64_t* positions = nullptr;
+  float temperature = 1.0f;
+  float* score_gap = nullptr;
+};
 
 template <int MODE>
 int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* targets,
                  int32_t* token, float* gap, float* logits, float* logp, cudaStream_t stream,
-                 const GateArgs* gate = nullptr) {
+                 const ModeArgs* gate = nullptr) {
   const int N = cols_for(B);
   CUtensorMap tmH;
   if (!encode_2d(&tmH, h->dtype, h_dev, h->d, B, static_cast<uint32_t>(N))) return DETLM_EINVAL;
@@ -263,7 +271,8 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   p.nk = h->nk;
   p.n_chunks = static_cast<int32_t>((h->d + kChunkK - 1) / kChunkK);
   p.n_slots = slots_for(N);
-  p.stages = stages_for(N, MODE == MODE_GATED);
+  constexpr bool kExtraSmem = MODE == MODE_GATED || MODE == MODE_SAMPLE;
+  p.stages = stages_for(N, kExtraSmem);
   p.tmem_cols = tmem_cols_for(p.n_slots * N);
   p.idesc = idesc_f16(h->dtype == DETLM_BF16 ? 1u : 0u, kBM, static_cast<uint32_t>(N));
   p.logits = logits;
@@ -277,8 +286,13 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   p.timeout_ns = h->timeout_ns;
   p.rec_b = w.b;
   p.round_fp16 = h->dtype == DETLM_FP16 ? 1 : 0;
+  if (gate != nullptr) {
+    p.seeds = gate->seeds;
+    p.positions = gate->positions;
+    p.temperature = gate->temperature;
+  }
 
-  const SmemLayout L = smem_layout(N, p.stages, MODE == MODE_GATED);
+  const SmemLayout L = smem_layout(N, p.stages, kExtraSmem);
   const size_t smem = L.total + 1024;
   const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
   const int grid = static_cast<int>(units < h->num_sms ? units : h->num_sms);
@@ -310,6 +324,7 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   mp.tau = gate != nullptr ? gate->tau : 0.0f;
   mp.base_token = gate != nullptr ? gate->base_token : nullptr;
   mp.margin = gate != nullptr ? gate->margin : nullptr;
+  mp.score_gap = gate != nullptr ? gate->score_gap : nullptr;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(static_cast<unsigned>(B));
@@ -667,9 +682,34 @@ int detlm_head_greedy_gated(detlm_head_t* h, const void* h_dev, int64_t B, float
   if (logits_dev != nullptr && !aligned(logits_dev, 4)) return DETLM_EINVAL;
   if (base_token_dev != nullptr && !aligned(base_token_dev, 4)) return DETLM_EINVAL;
   if (margin_dev != nullptr && !aligned(margin_dev, 4)) return DETLM_EINVAL;
-  const GateArgs gate{tau, base_token_dev, margin_dev};
+  ModeArgs gate;
+  gate.tau = tau;
+  gate.base_token = base_token_dev;
+  gate.margin = margin_dev;
   return launch_float<MODE_GATED>(h, h_dev, B, nullptr, token_dev, gap_dev, logits_dev, nullptr,
                                   stream, &gate);
+}
+
+int detlm_head_sample(detlm_head_t* h, const void* h_dev, int64_t B, float temperature,
+                      const uint64_t* seeds_dev, const uint64_t* positions_dev, int32_t* token_dev,
+                      float* score_gap_dev, float* logits_dev, cudaStream_t stream) {
+  if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature)) return DETLM_EINVAL;
+  if (h->dtype == DETLM_INT8) return DETLM_EUNSUPPORTED;
+  if (B == 0) return DETLM_OK;
+  if (h_dev == nullptr || !aligned(h_dev, 16)) return DETLM_EINVAL;
+  if (seeds_dev == nullptr || !aligned(seeds_dev, 8)) return DETLM_EINVAL;
+  if (positions_dev == nullptr || !aligned(positions_dev, 8)) return DETLM_EINVAL;
+  if (token_dev == nullptr || !aligned(token_dev, 4)) return DETLM_EINVAL;
+  if (score_gap_dev != nullptr && !aligned(score_gap_dev, 4)) return DETLM_EINVAL;
+  if (logits_dev != nullptr && !aligned(logits_dev, 4)) return DETLM_EINVAL;
+  ModeArgs a;
+  a.seeds = seeds_dev;
+  a.positions = positions_dev;
+  a.temperature = temperature;
+  a.score_gap = score_gap_dev;
+  return launch_float<MODE_SAMPLE>(h, h_dev, B, nullptr, token_dev, nullptr, logits_dev, nullptr,
+                                   stream, &a);
 }
 
 int detlm_head_verify(detlm_head_t* h, const void* h_dev, int64_t n_req, int64_t P,

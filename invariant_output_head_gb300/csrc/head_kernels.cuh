@@ -71,7 +71,10 @@ constexpr int kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
 // Precision Clause" (section on correcting the vulnerable token decisions):
 // the record also carries, for the logits rounded to the head's 16-bit
 // format, the lowest index of their maximum.
-enum : int { MODE_GREEDY = 0, MODE_LOGPROB = 1, MODE_INT = 2, MODE_GATED = 3 };
+// MODE_SAMPLE: seeded Gumbel-max sampling ("TandemLLM docs, 12 Exactness",
+// 12.5): the record is the greedy record of the scores z / T + G, G the
+// Gumbel noise of the row's (seed, position) at each vocabulary entry.
+enum : int { MODE_GREEDY = 0, MODE_LOGPROB = 1, MODE_INT = 2, MODE_GATED = 3, MODE_SAMPLE = 4 };
 enum : int { ERR_TIMEOUT = 1, ERR_TARGET = 2 };
 
 struct HeadParams {
@@ -95,6 +98,9 @@ struct HeadParams {
   uint64_t timeout_ns;
   int32_t* rec_b;           // [B, n_vt] gated: lowest index of the rounded maximum
   int32_t round_fp16;       // gated: 1 rounds logits to fp16, 0 to bf16
+  const uint64_t* seeds;    // sample: [B] generator key of each row
+  const uint64_t* positions;  // sample: [B] position t of each row
+  float temperature;        // sample: T > 0
 };
 
 // Greedy speculative verify, folded into the merge ("Inference and Decoding",
@@ -147,6 +153,7 @@ struct MergeParams {
   float tau;
   int32_t* base_token;      // optional [B]
   float* margin;            // optional [B]
+  float* score_gap;         // sample: optional [B], best minus runner-up score
 };
 
 // ------------------------------------------------------------ merge rules
@@ -314,6 +321,36 @@ __device__ __forceinline__ ITop2 xp_itop2(const int32_t* xp, int lane, int v_row
   return itop2_merge(t, shfl_xor(t, 16));
 }
 
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplications
+// (multipliers 0xD2511F53, 0xCD9E8D57) mixed with the key, which advances by
+// the Weyl increments 0x9E3779B9, 0xBB67AE85 between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// Sampling score of vocabulary entry v for the row keyed by (seed, t):
+// z / T + G, G = -log(-log U), U = (2 (x >> 9) + 1) 2^-24 (exact in fp32,
+// strictly inside (0, 1)), x = word (v mod 4) of the Philox block with
+// counter (v div 4, t low, t high, 0) and key (seed low, seed high).
+__device__ __forceinline__ float sample_score(float z, float T, uint32_t k0, uint32_t k1,
+                                              uint32_t t_lo, uint32_t t_hi, uint32_t v) {
+  const uint4 w = philox4x32_10(make_uint4(v >> 2, t_lo, t_hi, 0u), k0, k1);
+  const uint32_t j = v & 3u;
+  const uint32_t x = j == 0 ? w.x : j == 1 ? w.y : j == 2 ? w.z : w.w;
+  const float U = __uint2float_rn(((x >> 9) << 1) | 1u) * 5.9604644775390625e-8f;   // 2^-24
+  const float G = -logf(-logf(U));
+  return __fadd_rn(__fdiv_rn(z, T), G);
+}
+
 __device__ __forceinline__ int brev4(int l) {
   return ((l & 1) << 3) | ((l & 2) << 1) | ((l & 4) >> 1) | ((l & 8) >> 3);
 }
@@ -395,7 +432,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = p.stages;
-  const SmemLayout L = smem_layout(N, S, MODE == MODE_GATED);
+  const SmemLayout L = smem_layout(N, S, MODE == MODE_GATED || MODE == MODE_SAMPLE);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.ctrl_off);
   const uint32_t bar0 = smem_u32(bars);
@@ -413,6 +450,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   float* red_s = reinterpret_cast<float*>(red_i + 4 * N);
   int* tgt_row = reinterpret_cast<int*>(red_s + 4 * N);   // log-prob: target row in tile, or -1
   int32_t* red_b = tgt_row + N;                            // gated: [4][N]
+  uint32_t* skey = reinterpret_cast<uint32_t*>(red_b);     // sample: [4][N] seed lo/hi, t lo/hi
   float* xpose = reinterpret_cast<float*>(smem + L.xp_off);
   const uint32_t smem_base = smem_u32(smem);
   auto sA = [&](int s) { return smem_base + static_cast<uint32_t>(s) * L.stage_bytes; };
@@ -634,6 +672,20 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
         }
         named_bar_sync(1, ET);
       }
+      if constexpr (MODE == MODE_SAMPLE) {
+        // the unit's column keys, once per unit (ordered before the reads by
+        // this barrier, after the previous unit's reads by the one above)
+        for (int c = et; c < N; c += ET) {
+          const int n = n0 + c;
+          const uint64_t sd = n < p.B ? p.seeds[n] : 0ull;
+          const uint64_t tp = n < p.B ? p.positions[n] : 0ull;
+          skey[c] = static_cast<uint32_t>(sd);
+          skey[N + c] = static_cast<uint32_t>(sd >> 32);
+          skey[2 * N + c] = static_cast<uint32_t>(tp);
+          skey[3 * N + c] = static_cast<uint32_t>(tp >> 32);
+        }
+        named_bar_sync(1, ET);
+      }
 #pragma unroll
       for (int bb = 0; bb < WBLK; ++bb) {
         const int c0 = (g * WBLK + bb) * 16;
@@ -649,6 +701,20 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           int32_t* xpi = reinterpret_cast<int32_t*>(xp);
 #pragma unroll
           for (int i = 0; i < 16; ++i) xpi[lane * kXpStride + i] = vok ? acc[bb][i] : INT32_MIN;
+        } else if constexpr (MODE == MODE_SAMPLE) {
+          // logits to this lane's transpose row first, then the scores in
+          // place (a rolled loop: the noise is long code)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) xp[lane * kXpStride + i] = acc[bb][i];
+#pragma unroll 1
+          for (int i = 0; i < 16; ++i) {
+            const int c = c0 + i;
+            float x = -INFINITY;
+            if (vok && n0 + c < p.B)
+              x = sample_score(xp[lane * kXpStride + i], p.temperature, skey[c], skey[N + c],
+                               skey[2 * N + c], skey[3 * N + c], static_cast<uint32_t>(v));
+            xp[lane * kXpStride + i] = x;
+          }
         } else {
 #pragma unroll
           for (int i = 0; i < 16; ++i) xp[lane * kXpStride + i] = vok ? acc[bb][i] : -INFINITY;
@@ -661,7 +727,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
             red_i[q * N + c0 + lane] = t.i;
             reinterpret_cast<int32_t*>(red_s)[q * N + c0 + lane] = t.s;
           }
-        } else if constexpr (MODE == MODE_GREEDY) {
+        } else if constexpr (MODE == MODE_GREEDY || MODE == MODE_SAMPLE) {
           const Top2 t = xp_top2(xp, lane, vt * kBM + q * 32);
           if (lane < 16) {
             red_m[q * N + c0 + lane] = t.m;
@@ -705,7 +771,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           reinterpret_cast<int32_t*>(p.rec_m)[o] = r.m;
           p.rec_i[o] = r.i;
           reinterpret_cast<int32_t*>(p.rec_s)[o] = r.s;
-        } else if constexpr (MODE == MODE_GREEDY || MODE == MODE_GATED) {
+        } else if constexpr (MODE == MODE_GREEDY || MODE == MODE_GATED || MODE == MODE_SAMPLE) {
           Top2 t[4];
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq)
@@ -779,7 +845,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
   const int n = blockIdx.x;
   const int g = threadIdx.x;
   const size_t base = static_cast<size_t>(n) * p.n_vt;
-  if constexpr (MODE == MODE_GREEDY) {
+  if constexpr (MODE == MODE_GREEDY || MODE == MODE_SAMPLE) {
     __shared__ Top2 part[4];
     Top2 acc{-INFINITY, INT32_MAX, -INFINITY};
     for (int t0 = g; t0 < p.n_vt; t0 += kMergeThreads * kMergeBatch) {
@@ -796,7 +862,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     const Top2 tot = block_tree128(acc, top2_merge, part);
     if (g == 0) {
       p.token[n] = tot.i;
-      p.gap[n] = gap_ulp_bf16(tot.m, tot.s);
+      if constexpr (MODE == MODE_GREEDY) {
+        p.gap[n] = gap_ulp_bf16(tot.m, tot.s);
+      } else {
+        if (p.score_gap != nullptr) p.score_gap[n] = __fsub_rn(tot.m, tot.s);
+      }
       accept_fold(p.acc, n, tot.i);
     }
   } else if constexpr (MODE == MODE_GATED) {

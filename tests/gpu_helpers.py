@@ -99,3 +99,38 @@ def logprob_tol(A, lse_ref, targets):
     B = A.shape[0]
     et = e[np.arange(B), targets]
     return et + e.max(axis=1) + 1e-6 * (1.0 + np.abs(lse_ref)) + 8e-6
+
+
+def sample_tol(z_ref, A, T, G):
+    """Bound on |score_gpu - score_ref| of the sampling call, per entry:
+    the logit's own bound over T, the rounding of z / T, the fp32 Gumbel
+    transform (two logf calls, each within 1 ulp by CUDA's documented bound;
+    U is exact: 2^-23 from the inner log, 2^-23 |G| from the outer, doubled
+    for margin) and the rounding of the final add."""
+    zt = np.abs(z_ref) / T
+    return (LOGIT_RTOL * A / T + 2.0 ** -24 * zt + 2.0 ** -22 * (1.0 + np.abs(G))
+            + 2.0 ** -24 * (zt + np.abs(G)))
+
+
+def check_sample(z_ref, A, T, seeds, positions, tok_g, gap_g, label=""):
+    """Sampled tokens against the oracle's draws; rows where the oracle's two
+    best scores lie within the sum of their bounds are listed, and there the
+    GPU token must be one of those candidates."""
+    ref = oracle.sample(z_ref, T, seeds, positions)
+    G = oracle.gumbel_rows(seeds, positions, z_ref.shape[1])
+    e = sample_tol(z_ref, A, T, G)
+    sc = ref["score"]
+    listed = []
+    for n in range(z_ref.shape[0]):
+        t, tg = int(ref["token"][n]), int(tok_g[n])
+        if tg != t:
+            assert sc[n, t] - sc[n, tg] <= e[n, t] + e[n, tg], (
+                label, "sampled token differs outside the bound", n, t, tg,
+                sc[n, t] - sc[n, tg], e[n, t] + e[n, tg])
+            listed.append({"row": n, "oracle": t, "gpu": tg})
+        if z_ref.shape[1] >= 2 and gap_g is not None and tg == t:
+            srt = np.argsort(-sc[n], kind="stable")
+            bound = e[n, srt[0]] + 2 * e[n, srt[1:3]].max() + 2.0 ** -24 * abs(float(gap_g[n]))
+            assert abs(float(gap_g[n]) - (ref["m"][n] - ref["s"][n])) <= bound, (
+                label, "score gap", n, gap_g[n], ref["m"][n] - ref["s"][n], bound)
+    return listed
