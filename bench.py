@@ -1,7 +1,7 @@
 """Benchmark of the batch-invariant output head on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W]
-                    [--workload pr1|sweep|spec|logprob|int8|gated|verify]
+                    [--workload pr1|sweep|spec|logprob|int8|gated|sample|verify]
                     [--impl ours|reference]
 
 Prints ONE JSON line. A step is one pass of the whole hot path over one batch
@@ -17,6 +17,8 @@ of synthetic input:
 * int8: the integer head d=4096, V=128256 at --batch rows (default 512);
 * gated: the pr1 calls through the margin-gated greedy call (tau = 0.001),
   adding the rounded head's token and its top-two margin per row;
+* sample: the pr1 calls through the seeded sampling call (T = 1, one seed
+  and position per row), returning the drawn token and its score gap;
 * verify: the spec block through the speculative-verify call, 16 requests
   x 16 drafted positions, adding the accepted length per request.
 
@@ -65,11 +67,15 @@ WORKLOADS = {
     "gated": dict(desc="margin-gated greedy decode (tau=0.001): bf16 head d=2048 V=32000, "
                        "16 independent B=1 rows, fp32 logits + token + gap + bf16-head token "
                        "+ margin", fmt="bf16", V=32000, d=2048, mode="gated", bound="hbm"),
+    "sample": dict(desc="seeded Gumbel-max sampling (T=1): bf16 head d=2048 V=32000, 16 "
+                        "independent B=1 rows, fp32 logits + sampled token + score gap",
+                   fmt="bf16", V=32000, d=2048, mode="sample", bound="hbm"),
     "verify": dict(desc="greedy speculative verify: bf16 head d=3584 V=152064, 16 requests x "
                         "16 drafted positions, logits + token + gap + accepted length",
                    fmt="bf16", V=152064, d=3584, B=256, mode="verify", bound="tensor"),
 }
 GATE_TAU = 0.001
+SAMPLE_T = 1.0
 SEED_DRAFTS = 3103
 
 
@@ -200,9 +206,13 @@ def job_rows_per_s(rows_per_step: int, steps: int, world: int, elapsed_ms: float
 
 def make_inputs(name: str, batch: int):
     import synth
-    if name in ("pr1", "gated"):
+    if name in ("pr1", "gated", "sample"):
         c = synth.pr1()
         c["calls"] = [(r, 1) for r in range(c["h"].shape[0])]
+        if name == "sample":
+            rk = np.random.default_rng(SEED_DRAFTS + 2)
+            c["seeds"] = rk.integers(0, 2 ** 63, size=16).astype(np.int64)
+            c["positions"] = rk.integers(0, 4096, size=16).astype(np.int64)
     elif name == "sweep":
         c = synth.sweep()
         calls = []
@@ -243,6 +253,8 @@ def algorithmic(name, c, B):
         by += B * 8                      # rounded head's token + margin
     if mode == "verify":
         by += B * 4 + (B // 16) * 4      # drafts + accepted
+    if mode == "sample":
+        by += B * 16                     # seeds + positions
     return by, 2.0 * B * V * d
 
 
@@ -299,6 +311,9 @@ def run_ours(args, rank, world, local_rank):
             outs.append(torch.empty(B, dtype=torch.float32, device=dev))
     targets = torch.from_numpy(c["targets"]).to(dev) if not greedy else None
     drafts = torch.from_numpy(c["drafts"]).to(dev) if mode == "verify" else None
+    if mode == "sample":
+        seeds_d = torch.from_numpy(c["seeds"]).to(dev)
+        pos_d = torch.from_numpy(c["positions"]).to(dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     n_calls = len(calls)
@@ -320,6 +335,11 @@ def run_ours(args, rank, world, local_rank):
                 bd.detlm_head_greedy_gated(hd.handle, hv.data_ptr(), B, GATE_TAU, tok.data_ptr(),
                                            gap.data_ptr(), lg.data_ptr(), base.data_ptr(),
                                            margin.data_ptr(), sp)
+            elif mode == "sample":
+                tok, gap, lg = outs[j]
+                bd.detlm_head_sample(hd.handle, hv.data_ptr(), B, SAMPLE_T,
+                                     seeds_d[r0:r0 + B].data_ptr(), pos_d[r0:r0 + B].data_ptr(),
+                                     tok.data_ptr(), gap.data_ptr(), lg.data_ptr(), sp)
             elif mode == "verify":
                 tok, gap, lg, acc = outs[j]
                 bd.detlm_head_verify(hd.handle, hv.data_ptr(), B // 16, 16, drafts.data_ptr(),
@@ -470,7 +490,7 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
     extra = torch.empty(2 * maxB, dtype=torch.int32).pin_memory()   # base+margin / accepted
     sp = stream.cuda_stream
     steps = max(3, min(args.steps, int(args.e2e_seconds / 0.002)))
-    if mode in ("gated", "verify"):
+    if mode in ("gated", "verify", "sample"):
         tdt = {"bf16": torch.bfloat16, "fp16": torch.float16}[fmt]
         h_dev = torch.empty((maxB, d), dtype=tdt, device=dev)
         o_dev = [torch.empty(maxB, dtype=torch.int32, device=dev),
@@ -479,6 +499,9 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
                  torch.empty(2 * maxB, dtype=torch.int32, device=dev)]
         dr_host = (torch.from_numpy(c["drafts"]).pin_memory() if mode == "verify" else None)
         dr_dev = torch.empty(maxB, dtype=torch.int32, device=dev)
+        if mode == "sample":
+            sd_host = torch.from_numpy(np.stack([c["seeds"], c["positions"]])).pin_memory()
+            sd_dev = torch.empty((2, sd_host.shape[1]), dtype=torch.int64, device=dev)
 
     def one_step(i):
         for j, (r0, B) in enumerate(calls):
@@ -499,6 +522,13 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
                             o_dev[1].data_ptr(), o_dev[2].data_ptr(), o_dev[3].data_ptr(),
                             o_dev[3].data_ptr() + 4 * B, sp)
                         n_extra = 2 * B
+                    elif mode == "sample":
+                        sd_dev[:, r0:r0 + B].copy_(sd_host[:, r0:r0 + B], non_blocking=True)
+                        bd.detlm_head_sample(
+                            hd.handle, h_dev.data_ptr(), B, SAMPLE_T,
+                            sd_dev[0, r0:r0 + B].data_ptr(), sd_dev[1, r0:r0 + B].data_ptr(),
+                            o_dev[0].data_ptr(), o_dev[1].data_ptr(), o_dev[2].data_ptr(), sp)
+                        n_extra = 0
                     else:
                         dr_dev[:B].copy_(dr_host.view(-1)[:B], non_blocking=True)
                         bd.detlm_head_verify(
@@ -509,7 +539,8 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
                     tok[:B].copy_(o_dev[0][:B], non_blocking=True)
                     gap[:B].view(torch.float32).copy_(o_dev[1][:B], non_blocking=True)
                     lg[:B].view(torch.float32).copy_(o_dev[2][:B], non_blocking=True)
-                    extra[:n_extra].copy_(o_dev[3][:n_extra], non_blocking=True)
+                    if n_extra:
+                        extra[:n_extra].copy_(o_dev[3][:n_extra], non_blocking=True)
     for i in range(3):
         one_step(i)
     torch.cuda.synchronize()
@@ -518,13 +549,15 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
         one_step(i)
     torch.cuda.synchronize()
     dt = time.perf_counter() - t
-    h2d = sum(B * d * esz + (4 * B if mode in ("logprob", "verify") else 0) for _, B in calls)
+    h2d = sum(B * d * esz + (4 * B if mode in ("logprob", "verify") else 0)
+              + (16 * B if mode == "sample" else 0) for _, B in calls)
     d2h = sum(4 * B if mode == "logprob" else 8 * B + 4 * B * V for _, B in calls)
     d2h += sum(8 * B if mode == "gated" else (4 * (B // 16) if mode == "verify" else 0)
                for _, B in calls)
     api = {"greedy": "detlm_head_greedy_host", "logprob": "detlm_head_logprob_host",
            "gated": "detlm_head_greedy_gated + pinned copies on the call's stream",
-           "verify": "detlm_head_verify + pinned copies on the call's stream"}[mode]
+           "verify": "detlm_head_verify + pinned copies on the call's stream",
+           "sample": "detlm_head_sample + pinned copies on the call's stream"}[mode]
     return {"value": round(rows_per_step * steps / dt, 2), "unit": "rows/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps, "api": api}
 
@@ -564,6 +597,9 @@ def oracle_row(name, c, r):
     out = oracle.head_greedy(c["W"], h[r:r + 1], fmt)
     if mode == "gated":
         out["gate"] = oracle.gated_greedy(out["logits"], GATE_TAU, fmt)
+    if mode == "sample":
+        out["sample"] = oracle.sample(out["logits"], SAMPLE_T, c["seeds"][r:r + 1],
+                                      c["positions"][r:r + 1])
     if mode == "verify":
         # the row's comparison with its draft (the request's accepted length
         # is a prefix scan over its 16 rows)
