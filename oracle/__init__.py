@@ -20,7 +20,9 @@ Everything is computed exactly or in float64 with numpy:
 * the margin-gated decision: rounding of the logits to bf16 / fp16, the
   rounded head's token and top-two margin, the gate and the gated token;
 * seeded Gumbel-max sampling: the Philox4x32-10 generator, the uniform and
-  Gumbel transforms and the sampled token.
+  Gumbel transforms and the sampled token;
+* the integer front end: per-row int8 quantization of float rows with a
+  dyadic multiplier M / 2^S.
 
 Parity pins: every function here is pinned by tests that do not re-use its
 own formula (hand-worked tiny cases, brute force with exact rationals,
@@ -28,11 +30,12 @@ closed forms, invariants, and planted-mistake checks). Nothing is marked
 "parity unpinned".
 """
 from .head import (  # noqa: F401
-    decode_bf16, decode_fp16, decode_int8, decode,
+    decode_bf16, decode_fp16, decode_fp32, decode_int8, decode,
     logits_float, logits_int, bigint_dot,
     ulp_bf16, top2, greedy, greedy_int, gap_from_top2_f32,
     logsumexp, logprob,
     head_greedy, head_logprob, verify_accept,
     round_to_format, gated_greedy,
     philox4x32_10, uniform_from_word, gumbel_rows, gumbel_noise, sample,
+    quantize_rows,
 )

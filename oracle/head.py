@@ -30,6 +30,10 @@ Sources, by page title:
   the token at index t as the argmax of log p_t + G_t, G_t Gumbel noise from
   a generator seeded by (seed, t) -- an exact sample from p_t that does not
   depend on what else was computed. [Decoding] section 3: p = softmax(z/T).
+* [DetLLM] section "DetLLM": every tensor carries a dyadic scale (an integer
+  multiplier and a shift, one fixed rounding rule); each token's activations
+  are quantized from that token's own values, so its bits cannot depend on
+  the rest of the batch.
 * [Decoding] section 6 (Speculative decoding): the target scores all drafted
   positions in one forward pass and keeps the drafted tokens while they agree
   with it; [Exactness] 12.1: greedy speculative output equals plain greedy
@@ -62,7 +66,13 @@ Readings where the pages are silent (each also listed with the design notes):
   block with counter (v div 4, t low word, t high word, 0); a word x maps to
   the uniform U = (2 floor(x / 2^9) + 1) 2^-24 in (0, 1), exact in float32;
   G = -log(-log U). log p_t + G differs from z/T + G by a constant per row,
-  so the sample is the argmax of z/T + G (lowest index on a tie).
+  so the sample is the argmax of z/T + G (lowest index on a tie);
+* integer front end: a float row x (bf16, fp16 or fp32 values, exact
+  dyadic rationals) becomes int8 q = RNE(x * M / 2^S) with amax = max |x|,
+  E = floor(log2 amax), S = E + 8 and M = floor(127 * 2^S / amax) (a 15-bit
+  multiplier in [16256, 32512]); RNE rounds to nearest, ties to even; the
+  largest element maps to +-127 and no value leaves [-127, 127]; an all-zero
+  row gives q = 0, M = 0, S = 0. x ~ q * 2^S / M.
 """
 from __future__ import annotations
 
@@ -90,7 +100,14 @@ def decode_int8(x: np.ndarray) -> np.ndarray:
     return np.asarray(x, dtype=np.int8).astype(np.int64)
 
 
+def decode_fp32(bits: np.ndarray) -> np.ndarray:
+    """IEEE binary32 bit patterns (uint32) -> float64, exactly."""
+    return np.asarray(bits, dtype=np.uint32).view(np.float32).astype(np.float64)
+
+
 def decode(arr: np.ndarray, fmt: str) -> np.ndarray:
+    if fmt == "fp32":
+        return decode_fp32(arr)
     if fmt == "bf16":
         return decode_bf16(arr)
     if fmt == "fp16":
@@ -421,3 +438,36 @@ def sample(z: np.ndarray, temperature: float, seeds, positions) -> dict:
     score = z / float(temperature) + gumbel_rows(seeds, positions, z.shape[1])
     token, m, s = top2(score)
     return {"token": token, "m": m, "s": s, "score": score}
+
+
+# --------------------------------------------------------------------------
+# Integer front end: per-token requantization to int8 with a dyadic scale
+# --------------------------------------------------------------------------
+
+def quantize_rows(x: np.ndarray):
+    """Per-row int8 quantization with a dyadic multiplier ([DetLLM]).
+
+    x [B, d] float64 holding exactly decoded bf16 / fp16 / fp32 values.
+    Returns (q int8 [B, d], M int64 [B], S int64 [B]) with, per row,
+    amax = max |x|, E = floor(log2 amax), S = E + 8,
+    M = floor(127 * 2^S / amax) in exact rational arithmetic, and
+    q = round-half-even(x * M * 2^-S). x * M has at most 24 + 15 significant
+    bits and the scaling is a power of two, so the float64 product is exact
+    and np.rint rounds it once, ties to even.
+    """
+    from fractions import Fraction
+    x = np.asarray(x, dtype=np.float64)
+    B, d = x.shape
+    q = np.zeros((B, d), dtype=np.int8)
+    M = np.zeros(B, dtype=np.int64)
+    S = np.zeros(B, dtype=np.int64)
+    for n in range(B):
+        amax = float(np.max(np.abs(x[n]))) if d > 0 else 0.0
+        if amax == 0.0:
+            continue
+        E = int(np.frexp(amax)[1]) - 1                  # amax in [2^E, 2^(E+1))
+        s = E + 8
+        m = (Fraction(127) * Fraction(2) ** s) // Fraction(amax)
+        M[n], S[n] = int(m), s
+        q[n] = np.rint(x[n] * float(m) * 2.0 ** (-s)).astype(np.int8)
+    return q, M, S

@@ -615,11 +615,82 @@ def pin_sample_invariants(o):
     assert (joint["m"] - joint["s"] == np.sort(sc, axis=1)[:, -1] - np.sort(sc, axis=1)[:, -2]).all()
 
 
+# ---- integer front end
+
+def _quantize_exact(row):
+    """One row by exact rationals: M by search, q by Python's round() of a
+    Fraction (half to even)."""
+    xs = [Fraction(float(v)) for v in row]
+    amax = max(abs(v) for v in xs)
+    if amax == 0:
+        return [0] * len(xs), 0, 0
+    E = 0
+    while Fraction(2) ** (E + 1) <= amax:
+        E += 1
+    while Fraction(2) ** E > amax:
+        E -= 1
+    S = E + 8
+    lo, hi = 0, 1 << 20
+    while hi - lo > 1:                         # largest M with M * amax <= 127 * 2^S
+        mid = (lo + hi) // 2
+        if mid * amax <= 127 * Fraction(2) ** S:
+            lo = mid
+        else:
+            hi = mid
+    M = lo
+    return [round(v * M / Fraction(2) ** S) for v in xs], M, S
+
+
+def pin_quantize_rows(o):
+    """Per-row int8 quantization: hand-worked rows, exact-rational brute force
+    on bf16 / fp16 / fp32 rows (subnormal and huge values included), and the
+    invariants of the reading (the largest element maps to +-127, the
+    multiplier stays in [16256, 32512], scaling a row by 2^j only moves S,
+    rows are independent, the error is at most half a step)."""
+    q, M, S = o.quantize_rows(np.array([[1.0, -0.5, 0.25], [0.0, 0.0, 0.0], [3.0, -1.0, 0.0],
+                                        [-2.0, 1.0, 0.015625],
+                                        [1.984375, 0.0078125, -0.0390625],
+                                        [1.984375, 0.0234375, 0.0]]))
+    # amax = 127/64 gives M = 2^14: q = 64 x, and 0.5 / -2.5 / 1.5 are exact ties
+    assert q.tolist() == [[127, -64, 32], [0, 0, 0], [127, -42, 0], [-127, 64, 1],
+                          [127, 0, -2], [127, 2, 0]]
+    assert M.tolist() == [32512, 0, 21674, 32512, 16384, 16384]
+    assert S.tolist() == [8, 0, 9, 9, 8, 8]
+    rng = np.random.default_rng(41)
+    rows = []
+    for fmt, bits in (("bf16", rng.integers(0, 1 << 16, size=(6, 9)) & 0xBF7F),
+                      ("fp16", rng.integers(0, 1 << 16, size=(6, 9)) & 0xFBFF),
+                      ("fp32", rng.integers(0, 1 << 32, size=(6, 9), dtype=np.uint64)
+                       .astype(np.uint32) & np.uint32(0xFF7FFFFF))):
+        x = o.decode(bits.astype(np.uint16) if fmt != "fp32" else bits, fmt)
+        x = x * np.exp2(rng.integers(-4, 4, size=(6, 1)))
+        rows.append(x)
+    rows.append(np.array([[2.0 ** -149, -2.0 ** -148, 0.0, 2.0 ** -140] + [0.0] * 5]))
+    rows.append(np.array([[3.0e38, -1.0e38, 1.0, 2.0 ** 100, -3.4e38, 0.0, 5.0, -7.0, 1e-30]]))
+    X = np.concatenate(rows)
+    X = X[np.all(np.isfinite(X), axis=1)]
+    q, M, S = o.quantize_rows(X)
+    for n in range(X.shape[0]):
+        qe, Me, Se = _quantize_exact(X[n])
+        assert q[n].tolist() == qe and int(M[n]) == Me and int(S[n]) == Se, n
+        if Me:
+            assert 16256 <= Me <= 32512
+            assert int(np.max(np.abs(q[n].astype(int)))) == 127
+            step = Fraction(2) ** Se / Me
+            for xv, qv in zip(X[n], qe):
+                assert abs(Fraction(float(xv)) - qv * step) <= step / 2
+    q2, M2, S2 = o.quantize_rows(X * 8.0)
+    assert (q2 == q).all() and (M2 == M).all() and (S2[M != 0] == S[M != 0] + 3).all()
+    for n in range(X.shape[0]):
+        qn, Mn, Sn = o.quantize_rows(X[n:n + 1])
+        assert (qn[0] == q[n]).all() and Mn[0] == M[n] and Sn[0] == S[n]
+
+
 ALL_PINS = [pin_tiny_golden, pin_bruteforce_float, pin_logsumexp_mpmath,
             pin_closed_forms, pin_page_examples, pin_int_head, pin_invariants,
             pin_gap_from_top2, pin_verify_accept, pin_round_to_format,
             pin_gated_greedy, pin_philox_kat, pin_gumbel_layout,
-            pin_gumbel_max_distribution, pin_sample_invariants]
+            pin_gumbel_max_distribution, pin_sample_invariants, pin_quantize_rows]
 
 
 def failing_pins(o):

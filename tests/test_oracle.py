@@ -79,6 +79,15 @@ MUTANTS = {
     "sample_position_ignored": ("gumbel_rows(seeds, positions, z.shape[1])",
                                 "gumbel_rows(seeds, [0] * z.shape[0], z.shape[1])"),
     "sample_keys_through_float": ("    seeds = _u64_list(seeds)\n", "    seeds = [int(x) for x in np.asarray(seeds).reshape(-1)]\n"),
+    "quantize_ties_away": ("        q[n] = np.rint(x[n] * float(m) * 2.0 ** (-s)).astype(np.int8)",
+                           "        q[n] = (np.sign(x[n]) * np.floor(np.abs(x[n]) * float(m) * 2.0 ** (-s) + 0.5)).astype(np.int8)"),
+    "quantize_multiplier_ceil": ("        m = (Fraction(127) * Fraction(2) ** s) // Fraction(amax)",
+                                 "        m = -((-Fraction(127) * Fraction(2) ** s) // Fraction(amax))"),
+    "quantize_shift_off_by_one": ("        s = E + 8\n", "        s = E + 7\n"),
+    "quantize_signed_max": ("        amax = float(np.max(np.abs(x[n]))) if d > 0 else 0.0",
+                            "        amax = float(np.max(x[n])) if d > 0 else 0.0"),
+    "quantize_batch_scale": ("        amax = float(np.max(np.abs(x[n]))) if d > 0 else 0.0",
+                             "        amax = float(np.max(np.abs(x))) if d > 0 else 0.0"),
     "gap_f32_rounded_difference": ("    with np.errstate(invalid=\"ignore\"):\n        return ((m - s) / ulp_bf16(m)).astype(np.float32)",
                                    "    with np.errstate(invalid=\"ignore\"):\n        return ((m - s) / ulp_bf16(s)).astype(np.float32)"),
 }
