@@ -48,7 +48,8 @@ typedef struct detlm_head detlm_head_t;     /* opaque handle */
 typedef enum {
   DETLM_BF16 = 0,   /* bf16 W and h, fp32 accumulation, fp32 logits        */
   DETLM_FP16 = 1,   /* IEEE fp16 W and h, fp32 accumulation, fp32 logits   */
-  DETLM_INT8 = 2    /* int8 W and h, exact int32 accumulation and logits   */
+  DETLM_INT8 = 2,   /* int8 W and h, exact int32 accumulation and logits   */
+  DETLM_FP32 = 3    /* fp32 rows: input of the integer front end only      */
 } detlm_dtype_t;
 
 typedef enum {
@@ -161,6 +162,35 @@ int detlm_head_sample(detlm_head_t* head, const void* h_dev, int64_t B,
                       const uint64_t* positions_dev, int32_t* token_dev,
                       float* score_gap_dev, float* logits_dev,
                       cudaStream_t stream);
+
+/* Integer front end ("Eliminating Nondeterminism in LLM Inference with
+ * Integer-Only Arithmetic", section DetLLM: dyadic scales, an integer
+ * multiplier and a shift with one fixed rounding rule; each token quantized
+ * from its own values). Row n of x (dtype BF16, FP16 or FP32; [B, d],
+ * row-major) becomes int8 q[n, :] with, from that row alone,
+ *   amax = max_k |x[n, k]|, E = floor(log2 amax), S = E + 8,
+ *   M = floor(127 * 2^S / amax)   (in [16256, 32512]),
+ *   q = round-half-to-even(x * M / 2^S)   (in [-127, 127]; amax -> +-127),
+ * all in exact integer arithmetic on the inputs' significands and
+ * exponents; x ~ q * 2^S / M. An all-zero row gives q = 0, M = 0, S = 0.
+ * Non-finite inputs give unspecified q (no error is raised).
+ * mult_dev / shift_dev: int32 [B] receive M and S. Requirements: B >= 0,
+ * 1 <= d < 2^31, x aligned to its element size. */
+int detlm_quantize_rows(const void* x_dev, int dtype, int64_t B, int64_t d,
+                        int8_t* q_dev, int32_t* mult_dev, int32_t* shift_dev,
+                        cudaStream_t stream);
+
+/* The int8 head fed by float rows: detlm_quantize_rows into a buffer the
+ * handle owns (grown on demand; growth synchronizes the stream), then the
+ * greedy call on the quantized rows. Exact int32 logits of q . W; the
+ * row's dequantized logits are logits * 2^S / M (times W's own scale), so
+ * the token is the same. INT8 heads only (else DETLM_EUNSUPPORTED);
+ * x_dtype BF16, FP16 or FP32. mult_dev / shift_dev may be NULL. */
+int detlm_head_greedy_from_float(detlm_head_t* head, const void* x_dev,
+                                 int x_dtype, int64_t B, int32_t* token_dev,
+                                 int32_t* gap_dev, int32_t* logits_dev,
+                                 int32_t* mult_dev, int32_t* shift_dev,
+                                 cudaStream_t stream);
 
 /* Greedy speculative verify: the greedy call on n_req * P hidden rows (the P
  * verified positions of each request, request-major) that also returns the

@@ -2,9 +2,11 @@
 
 The CUDA library (``_lib/libdetlm_head.so``, C ABI in ``include/detlm_head.h``)
 computes logits = h . W^T on sm_103a tensor cores and fuses the greedy
-decision (lowest-index argmax, top-2 gap in bf16 ulps) or the target
-log-probability, bit-identical for a row whatever the batch size. This
-package is the thin Python binding; see ``binding.Head``.
+decision (lowest-index argmax, top-2 gap in bf16 ulps), the target
+log-probability, the margin-gated decision, seeded sampling or speculative
+verification, bit-identical for a row whatever the batch size; an integer
+front end quantizes float rows for the exact int8 head. This package is the
+thin Python binding; see ``binding.Head``.
 """
 from .binding import (  # noqa: F401
     Head, DetlmError, load_library, library_path, status_string,
@@ -12,7 +14,8 @@ from .binding import (  # noqa: F401
     detlm_head_greedy_host, detlm_head_logprob_host, detlm_head_check,
     detlm_head_time_next, detlm_head_debug, detlm_head_tiles, detlm_head_destroy,
     detlm_status_string, detlm_greedy_noalloc, detlm_head_verify,
-    detlm_head_greedy_gated, detlm_head_sample,
-    DETLM_BF16, DETLM_FP16, DETLM_INT8, DETLM_OK, DETLM_EINVAL, DETLM_EUNSUPPORTED,
+    detlm_head_greedy_gated, detlm_head_sample, detlm_quantize_rows,
+    detlm_head_greedy_from_float, quantize_rows,
+    DETLM_BF16, DETLM_FP16, DETLM_INT8, DETLM_FP32, DETLM_OK, DETLM_EINVAL, DETLM_EUNSUPPORTED,
     DETLM_ECUDA, DETLM_ETIMEOUT, DETLM_ENOMEM, DETLM_ETARGET, DETLM_DEBUG_STALL,
 )

@@ -13,7 +13,7 @@ import os
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib",
                          "libdetlm_head.so")
 
-DETLM_BF16, DETLM_FP16, DETLM_INT8 = 0, 1, 2
+DETLM_BF16, DETLM_FP16, DETLM_INT8, DETLM_FP32 = 0, 1, 2, 3
 DTYPES = {"bf16": DETLM_BF16, "fp16": DETLM_FP16, "int8": DETLM_INT8}
 DETLM_OK, DETLM_EINVAL, DETLM_EUNSUPPORTED, DETLM_ECUDA = 0, -1, -2, -3
 DETLM_ETIMEOUT, DETLM_ENOMEM, DETLM_ETARGET = -4, -5, -6
@@ -29,6 +29,8 @@ _SIGS = {
     "detlm_head_greedy_gated": (_i32, [_vp, _vp, _i64, ctypes.c_float, _vp, _vp, _vp, _vp, _vp,
                                        _vp]),
     "detlm_head_sample": (_i32, [_vp, _vp, _i64, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "detlm_quantize_rows": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "detlm_head_greedy_from_float": (_i32, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     "detlm_head_greedy_host": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp]),
     "detlm_head_logprob_host": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
     "detlm_head_check": (_i32, [_vp, _vp]),
@@ -42,6 +44,30 @@ _SIGS = {
 }
 
 _lib = None
+
+
+def _float_dtype_code(x) -> int:
+    import torch
+    codes = {torch.bfloat16: DETLM_BF16, torch.float16: DETLM_FP16, torch.float32: DETLM_FP32}
+    if x.dtype not in codes:
+        raise ValueError("float rows must be bfloat16, float16 or float32")
+    return codes[x.dtype]
+
+
+def quantize_rows(x, stream=None):
+    """Integer front end on a float CUDA tensor x [B, d]: returns (q int8
+    [B, d], mult int32 [B], shift int32 [B])."""
+    import torch
+    xd = _float_dtype_code(x)
+    if not x.is_cuda or not x.is_contiguous() or x.dim() != 2:
+        raise ValueError("x must be a contiguous 2-D CUDA tensor")
+    B, d = int(x.shape[0]), int(x.shape[1])
+    q = torch.empty((B, d), dtype=torch.int8, device=x.device)
+    mult = torch.empty(B, dtype=torch.int32, device=x.device)
+    shift = torch.empty(B, dtype=torch.int32, device=x.device)
+    detlm_quantize_rows(x.data_ptr(), xd, B, d, q.data_ptr(), mult.data_ptr(),
+                        shift.data_ptr(), _stream_ptr(stream))
+    return q, mult, shift
 
 
 class DetlmError(RuntimeError):
@@ -118,6 +144,20 @@ def detlm_head_sample(handle, h_ptr, B, temperature, seeds_ptr, positions_ptr, t
                                             positions_ptr, token_ptr, score_gap_ptr, logits_ptr,
                                             stream),
            "detlm_head_sample")
+
+
+def detlm_quantize_rows(x_ptr, dtype, B, d, q_ptr, mult_ptr, shift_ptr, stream) -> None:
+    _check(load_library().detlm_quantize_rows(x_ptr, dtype, B, d, q_ptr, mult_ptr, shift_ptr,
+                                              stream),
+           "detlm_quantize_rows")
+
+
+def detlm_head_greedy_from_float(handle, x_ptr, x_dtype, B, token_ptr, gap_ptr, logits_ptr,
+                                 mult_ptr, shift_ptr, stream) -> None:
+    _check(load_library().detlm_head_greedy_from_float(handle, x_ptr, x_dtype, B, token_ptr,
+                                                       gap_ptr, logits_ptr, mult_ptr, shift_ptr,
+                                                       stream),
+           "detlm_head_greedy_from_float")
 
 
 def detlm_head_verify(handle, h_ptr, n_req, P, drafts_ptr, token_ptr, gap_ptr, logits_ptr,
@@ -281,6 +321,28 @@ class Head:
                           token.data_ptr(), gap.data_ptr(),
                           logits.data_ptr() if logits is not None else None, _stream_ptr(stream))
         return token, gap, logits
+
+    def greedy_from_float(self, x, with_logits: bool = False, stream=None):
+        """int8 head fed by float rows x [B, d] (bf16, fp16 or fp32 CUDA
+        tensor). Returns (token, gap, logits or None, mult, shift)."""
+        import torch
+        if self.dtype != "int8":
+            raise DetlmError(DETLM_EUNSUPPORTED, "greedy_from_float")
+        xd = _float_dtype_code(x)
+        if not x.is_cuda or not x.is_contiguous() or x.dim() != 2 or x.shape[1] != self.d:
+            raise ValueError(f"x must be a contiguous CUDA tensor [B, {self.d}]")
+        B = int(x.shape[0])
+        token = torch.empty(B, dtype=torch.int32, device=x.device)
+        gap = torch.empty(B, dtype=torch.int32, device=x.device)
+        mult = torch.empty(B, dtype=torch.int32, device=x.device)
+        shift = torch.empty(B, dtype=torch.int32, device=x.device)
+        logits = (torch.empty((B, self.V), dtype=torch.int32, device=x.device)
+                  if with_logits else None)
+        detlm_head_greedy_from_float(self.handle, x.data_ptr(), xd, B, token.data_ptr(),
+                                     gap.data_ptr(),
+                                     logits.data_ptr() if logits is not None else None,
+                                     mult.data_ptr(), shift.data_ptr(), _stream_ptr(stream))
+        return token, gap, logits, mult, shift
 
     def verify(self, h, drafts, with_logits: bool = False, stream=None):
         """Greedy speculative verify. h [R*P, d] request-major, drafts int32

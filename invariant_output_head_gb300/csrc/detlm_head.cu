@@ -18,6 +18,7 @@
 #include "detlm_head.h"
 #include "head_kernels.cuh"
 #include "int8_kernels.cuh"
+#include "quant_kernels.cuh"
 
 using namespace detlm;
 
@@ -46,6 +47,9 @@ struct detlm_head {
   int32_t* vws = nullptr;
   int64_t vws_R = 0;
   AcceptArgs acc{};
+  // integer front end: the quantized rows and their multipliers and shifts
+  void* q8 = nullptr;
+  size_t q8_bytes = 0;
   // test hook and timing hook
   int stall = 0;
   uint64_t timeout_ns = 2000000000ull;
@@ -576,6 +580,19 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 bool bad_B(int64_t B) { return B < 0 || B >= (int64_t{1} << 31); }
 
+int launch_quantize(const void* x_dev, int dtype, int64_t B, int64_t d, int8_t* q, int32_t* mult,
+                    int32_t* shift, cudaStream_t stream) {
+  QuantParams qp;
+  qp.x = x_dev;
+  qp.fmt = dtype;
+  qp.d = d;
+  qp.q = q;
+  qp.mult = mult;
+  qp.shift = shift;
+  quantize_rows_kernel<<<static_cast<unsigned>(B), kQThreads, 0, stream>>>(qp);
+  return status_from_cuda(cudaGetLastError());
+}
+
 }  // namespace
 
 extern "C" {
@@ -712,6 +729,59 @@ int detlm_head_sample(detlm_head_t* h, const void* h_dev, int64_t B, float tempe
                                    stream, &a);
 }
 
+int detlm_quantize_rows(const void* x_dev, int dtype, int64_t B, int64_t d, int8_t* q_dev,
+                        int32_t* mult_dev, int32_t* shift_dev, cudaStream_t stream) {
+  if (dtype != DETLM_BF16 && dtype != DETLM_FP16 && dtype != DETLM_FP32) return DETLM_EINVAL;
+  if (bad_B(B) || d < 1 || d >= (int64_t{1} << 31)) return DETLM_EINVAL;
+  if (B == 0) return DETLM_OK;
+  const size_t eb = dtype == DETLM_FP32 ? 4 : 2;
+  if (x_dev == nullptr || !aligned(x_dev, eb)) return DETLM_EINVAL;
+  if (q_dev == nullptr) return DETLM_EINVAL;
+  if (mult_dev == nullptr || !aligned(mult_dev, 4)) return DETLM_EINVAL;
+  if (shift_dev == nullptr || !aligned(shift_dev, 4)) return DETLM_EINVAL;
+  return launch_quantize(x_dev, dtype, B, d, q_dev, mult_dev, shift_dev, stream);
+}
+
+int detlm_head_greedy_from_float(detlm_head_t* h, const void* x_dev, int x_dtype, int64_t B,
+                                 int32_t* token_dev, int32_t* gap_dev, int32_t* logits_dev,
+                                 int32_t* mult_dev, int32_t* shift_dev, cudaStream_t stream) {
+  if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
+  if (h->dtype != DETLM_INT8) return DETLM_EUNSUPPORTED;
+  if (x_dtype != DETLM_BF16 && x_dtype != DETLM_FP16 && x_dtype != DETLM_FP32) return DETLM_EINVAL;
+  if (B == 0) return DETLM_OK;
+  const size_t eb = x_dtype == DETLM_FP32 ? 4 : 2;
+  if (x_dev == nullptr || !aligned(x_dev, eb)) return DETLM_EINVAL;
+  if (token_dev == nullptr || !aligned(token_dev, 4)) return DETLM_EINVAL;
+  if (gap_dev == nullptr || !aligned(gap_dev, 4)) return DETLM_EINVAL;
+  if (logits_dev != nullptr && !aligned(logits_dev, 4)) return DETLM_EINVAL;
+  if (mult_dev != nullptr && !aligned(mult_dev, 4)) return DETLM_EINVAL;
+  if (shift_dev != nullptr && !aligned(shift_dev, 4)) return DETLM_EINVAL;
+  // handle buffer: q [B, d] (256-byte aligned, rows of d bytes, d % 16 == 0
+  // for an int8 head) and, when the caller passes none, M and S [B]
+  const size_t qb = round256(static_cast<size_t>(B) * h->d);
+  const size_t need = qb + 2 * round256(static_cast<size_t>(B) * 4);
+  if (need > h->q8_bytes) {
+    if (h->q8 != nullptr) {
+      cudaError_t e = cudaStreamSynchronize(stream);
+      if (e != cudaSuccess) return status_from_cuda(e);
+      cudaFree(h->q8);
+      h->q8 = nullptr;
+      h->q8_bytes = 0;
+    }
+    cudaError_t e = cudaMalloc(&h->q8, need);
+    if (e != cudaSuccess) return status_from_cuda(e);
+    h->q8_bytes = need;
+  }
+  uint8_t* base = static_cast<uint8_t*>(h->q8);
+  int8_t* q = reinterpret_cast<int8_t*>(base);
+  int32_t* m = mult_dev ? mult_dev : reinterpret_cast<int32_t*>(base + qb);
+  int32_t* s = shift_dev ? shift_dev
+                         : reinterpret_cast<int32_t*>(base + qb + round256(static_cast<size_t>(B) * 4));
+  int st = launch_quantize(x_dev, x_dtype, B, h->d, q, m, s, stream);
+  if (st != DETLM_OK) return st;
+  return launch_int8(h, q, B, token_dev, gap_dev, logits_dev, stream);
+}
+
 int detlm_head_verify(detlm_head_t* h, const void* h_dev, int64_t n_req, int64_t P,
                       const int32_t* drafts_dev, int32_t* token_dev, void* gap_dev,
                       void* logits_dev, int32_t* accepted_dev, cudaStream_t stream) {
@@ -813,6 +883,7 @@ void detlm_head_destroy(detlm_head_t* h) {
   if (h == nullptr) return;
   if (h->ws) cudaFree(h->ws);
   if (h->vws) cudaFree(h->vws);
+  if (h->q8) cudaFree(h->q8);
   if (h->W16) cudaFree(h->W16);
   if (h->h16) cudaFree(h->h16);
   if (h->stage) cudaFree(h->stage);

@@ -26,7 +26,7 @@ import numpy as np
 __all__ = [
     "bf16_bits_from_f32", "f16_bits_from_f32", "normal_bf16", "uniform_int8",
     "pr1", "sweep", "spec_verify", "logprob", "int8_head", "small_float",
-    "small_int8", "plant_drafts", "SEED_W", "SEED_H", "SEED_X",
+    "small_int8", "plant_drafts", "float_rows", "SEED_W", "SEED_H", "SEED_X",
 ]
 
 SEED_W, SEED_H, SEED_X = 1000, 2000, 3000
@@ -274,3 +274,29 @@ def plant_drafts(tokens: np.ndarray, V: int, seed: int):
             drafts[r, c] = (tokens[r, c] + 1 + rng.integers(0, max(V - 1, 1))) % V
             drafts[r, c + 1:] = rng.integers(0, V, size=P - c - 1)
     return drafts.astype(np.int32), cut
+
+
+def float_rows(seed: int, B: int, d: int, fmt: str, special: bool = True):
+    """Float hidden rows for the integer front end, as raw storage (uint16
+    for bf16 / fp16, uint32 for fp32). Rows are N(0, 1) times a per-row scale
+    2^U{-20..20}; with ``special`` the first rows are an all-zero row, a row
+    with one non-zero entry, a row of subnormals and a row near the format's
+    largest values (when B allows)."""
+    rng = _rng(seed)
+    x = _normal_f32(rng, (B, d), 1.0) * np.exp2(rng.integers(-20, 21, size=(B, 1))).astype(np.float32)
+    if special:
+        tiny = {"bf16": 2.0 ** -130, "fp16": 2.0 ** -20, "fp32": 2.0 ** -140}[fmt]
+        big = {"bf16": 1e38, "fp16": 6e4, "fp32": 3e38}[fmt]
+        rows = [np.zeros(d, np.float32)]
+        one = np.zeros(d, np.float32)
+        one[rng.integers(0, d)] = -3.0
+        rows.append(one)
+        rows.append((rng.integers(-4, 5, size=d) * tiny).astype(np.float32))
+        rows.append(np.clip(_normal_f32(rng, (d,), 0.4), -1, 1).astype(np.float32) * np.float32(big))
+        for k, r in enumerate(rows[:B]):
+            x[k] = r
+    if fmt == "bf16":
+        return bf16_bits_from_f32(x)
+    if fmt == "fp16":
+        return f16_bits_from_f32(np.clip(x, -65504, 65504))
+    return x.view(np.uint32).copy()
