@@ -126,6 +126,12 @@ int stages_for(int N, bool gated = false) {
   return s;
 }
 
+// Two MMA-issuing threads where the kernel allows it (N <= 128) and both
+// rings they wait on have even lengths (the kernel's parity waits rely on it).
+int issuers_for(int N, int stages, int slots) {
+  return (max_mma_issuers(N) == 2 && stages % 2 == 0 && slots % 2 == 0) ? 2 : 1;
+}
+
 int status_from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return DETLM_OK;
   if (e == cudaErrorMemoryAllocation) return DETLM_ENOMEM;
@@ -277,6 +283,7 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   p.n_slots = slots_for(N);
   constexpr bool kExtraSmem = MODE == MODE_GATED || MODE == MODE_SAMPLE;
   p.stages = stages_for(N, kExtraSmem);
+  p.n_issuers = issuers_for(N, p.stages, p.n_slots);
   p.tmem_cols = tmem_cols_for(p.n_slots * N);
   p.idesc = idesc_f16(h->dtype == DETLM_BF16 ? 1u : 0u, kBM, static_cast<uint32_t>(N));
   p.logits = logits;
@@ -431,6 +438,7 @@ int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token
   p.n_chunks = static_cast<int32_t>((h->d + kChunkK - 1) / kChunkK);
   p.n_slots = slots_for(N);
   p.stages = stages_for(N);
+  p.n_issuers = issuers_for(N, p.stages, p.n_slots);
   p.tmem_cols = tmem_cols_for(p.n_slots * N);
   p.idesc = idesc_f16(0u, kBM, static_cast<uint32_t>(N));
   p.logits = reinterpret_cast<float*>(logits);
@@ -978,6 +986,7 @@ extern "C" int detlm_greedy_noalloc(const void* W_dev, int64_t V, int64_t d, int
   p.n_chunks = static_cast<int32_t>((d + kChunkK - 1) / kChunkK);
   p.n_slots = slots_for(N);
   p.stages = stages_for(N);
+  p.n_issuers = issuers_for(N, p.stages, p.n_slots);
   p.tmem_cols = tmem_cols_for(p.n_slots * N);
   p.idesc = idesc_f16(dtype == DETLM_BF16 ? 1u : 0u, kBM, static_cast<uint32_t>(N));
   p.logits = logits_dev;

@@ -20,8 +20,9 @@
 // ascending chunk order. This keeps every logit within 1e-6 * sum|w h| and
 // is the same arithmetic for every B.
 //
-// Warp 0 issues TMA loads into an S-stage ring, warp 1 issues the MMAs into
-// the chunk slot ring, warps 2..5 drain each slot into running sums (one
+// Warp 0 issues TMA loads into an S-stage ring, warp 1 (and, up to N = 128,
+// warp 6, alternate chunks) issues the MMAs into the chunk slot ring, warps
+// 2..5 drain each slot into running sums (one
 // thread per vocabulary row, up to 128 hidden rows per thread), then write
 // the optional fp32 logits and the per-tile decision record of each hidden
 // row:
@@ -96,6 +97,7 @@ struct HeadParams {
   int* err;                 // device error word
   int32_t stall;            // test hook: MMA issuer waits on a dead barrier
   uint64_t timeout_ns;
+  int32_t n_issuers;        // MMA-issuing threads: 1, or 2 when N <= 128 and both rings are even
   int32_t* rec_b;           // [B, n_vt] gated: lowest index of the rounded maximum
   int32_t round_fp16;       // gated: 1 rounds logits to fp16, 0 to bf16
   const uint64_t* seeds;    // sample: [B] generator key of each row
@@ -366,7 +368,15 @@ __device__ __forceinline__ int brev4(int l) {
 __host__ __device__ constexpr int epi_warps_for(int N) { return N > 128 ? 8 : 4; }
 __host__ __device__ constexpr int epi_first_warp(int N) { return N > 128 ? 4 : 2; }
 __host__ __device__ constexpr int kblocks_per_stage(int N) { return N > 128 ? 1 : 2; }
-__host__ __device__ constexpr int threads_for(int N) { return N > 128 ? 384 : 192; }
+// Up to N = 128 a second thread (warp 6) can issue the MMAs of every other
+// K chunk: one thread's tcgen05.mma issue rate holds back the TMA ring at
+// small N. Each chunk keeps its own MMAs in K order, so the arithmetic does
+// not change. The host enables it only when both rings the issuers wait on
+// (stages, chunk slots) have even lengths: then a chunk and the one a ring
+// length earlier belong to the same issuer and every parity wait is
+// unambiguous (the kernel refuses other combinations).
+__host__ __device__ constexpr int max_mma_issuers(int N) { return N > 128 ? 1 : 2; }
+__host__ __device__ constexpr int threads_for(int N) { return N > 128 ? 384 : 224; }
 constexpr int kRegsLaunchWide = 168;   // registers per thread at launch, N = 256
 constexpr int kRegsWg0Wide = 40;
 constexpr int kRegsEpiWide = 232;
@@ -425,6 +435,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   constexpr int KPS = kblocks_per_stage(N);     // K boxes per stage
   constexpr int WBLK = NBLK / (EW / 4);         // 16-column blocks per epilogue warp
   constexpr int E0 = epi_first_warp(N);         // first epilogue warp
+  const int NWAY = p.n_issuers;                 // MMA-issuing threads (1 or 2)
   static_assert(N <= kMaxN && NBLK % (EW / 4) == 0 && kBlocksPerChunk % KPS == 0, "shape");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -466,7 +477,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       mbar_init(acce_bar(b), EW);
     }
     mbar_init(never_bar, 1);
-    mbar_init(drain_bar, 1);
+    mbar_init(drain_bar, static_cast<uint32_t>(NWAY));
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -556,40 +567,80 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 1 || (max_mma_issuers(N) == 2 && warp == E0 + EW)) {
     // ------------------------------------------------------- MMA issuer
     if constexpr (EW == 8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegsWg0Wide));
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
-      bool ok = true;
-      if (p.stall) ok = mbar_wait(never_bar, 0, abort_flag, p.timeout_ns);
-      uint32_t slot = 0, sph = 0;   // chunk slot ring position and phase
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        for (int c = 0; c < p.n_chunks && ok; ++c) {
-          if (!mbar_wait(acce_bar(slot), sph ^ 1u, abort_flag, p.timeout_ns)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t d_tmem = tmem_base + slot * static_cast<uint32_t>(N);
-#pragma unroll
-          for (int sc = 0; sc < kBlocksPerChunk / KPS; ++sc) {
-            const int kb0 = c * kBlocksPerChunk + sc * KPS;
-            if (kb0 >= p.nk) break;
-            if (!mbar_wait(full_bar(stage), phase, abort_flag, p.timeout_ns)) { ok = false; break; }
+    const int which = warp == 1 ? 0 : 1;             // chunks which, which + NWAY, ...
+    if (lane == 0 && which < NWAY) {
+      constexpr int SPC = kBlocksPerChunk / KPS;     // pipeline stages per chunk
+      // ring lengths must be multiples of NWAY (the host only enables two
+      // issuers then)
+      bool ok = S % NWAY == 0 && p.n_slots % NWAY == 0 && NWAY <= S && NWAY <= p.n_slots;
+      if (p.stall) ok = ok && mbar_wait(never_bar, 0, abort_flag, p.timeout_ns);
+      if constexpr (max_mma_issuers(N) == 1) {
+        // one issuer (N = 256, 40 registers): ring positions by increments
+        uint32_t stage = 0, phase = 0, slot = 0, sph = 0;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+          for (int c = 0; c < p.n_chunks && ok; ++c) {
+            if (!mbar_wait(acce_bar(slot), sph ^ 1u, abort_flag, p.timeout_ns)) { ok = false; break; }
             tc_fence_after();
-            const int nb = min(KPS, p.nk - kb0);
-            for (int b = 0; b < nb; ++b) {
-              const uint64_t da = sdesc_sw128(sA(stage) + b * kBM * kRowBytes);
-              const uint64_t db = sdesc_sw128(sB(stage) + b * N * kRowBytes);
-              const bool first = (kb0 + b) == c * kBlocksPerChunk;
+            const uint32_t d_tmem = tmem_base + slot * static_cast<uint32_t>(N);
 #pragma unroll
-              for (int k = 0; k < 4; ++k)   // K = 16 per MMA: 32 bytes = 2 descriptor units
-                mma_f16(d_tmem, da + 2u * k, db + 2u * k, p.idesc, !(first && k == 0));
+            for (int sc = 0; sc < SPC; ++sc) {
+              const int kb0 = c * kBlocksPerChunk + sc * KPS;
+              if (kb0 >= p.nk) break;
+              if (!mbar_wait(full_bar(stage), phase, abort_flag, p.timeout_ns)) { ok = false; break; }
+              tc_fence_after();
+              const int nb = min(KPS, p.nk - kb0);
+              for (int b = 0; b < nb; ++b) {
+                const uint64_t da = sdesc_sw128(sA(stage) + b * kBM * kRowBytes);
+                const uint64_t db = sdesc_sw128(sB(stage) + b * N * kRowBytes);
+                const bool first = (kb0 + b) == c * kBlocksPerChunk;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  mma_f16(d_tmem, da + 2u * k, db + 2u * k, p.idesc, !(first && k == 0));
+              }
+              mma_commit(empty_bar(stage));
+              if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
             }
-            mma_commit(empty_bar(stage));
-            if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+            if (!ok) break;
+            mma_commit(accf_bar(slot));
+            if (++slot == static_cast<uint32_t>(p.n_slots)) { slot = 0; sph ^= 1u; }
           }
-          if (!ok) break;
-          mma_commit(accf_bar(slot));
-          if (++slot == static_cast<uint32_t>(p.n_slots)) { slot = 0; sph ^= 1u; }
+        }
+      } else {
+        // N <= 128: one stage per chunk; issuer `which` takes chunks which,
+        // which + NWAY, ... and its ring positions advance by NWAY (both
+        // ring lengths are multiples of NWAY, so no position is shared
+        // with the other issuer in between)
+        static_assert(SPC == 1, "one pipeline stage per chunk");
+        uint32_t stage = which, phase = 0, slot = which, sph = 0;
+        bool mine = which == 0;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+          for (int c = 0; c < p.n_chunks && ok; ++c) {
+            if (mine) {
+              if (!mbar_wait(acce_bar(slot), sph ^ 1u, abort_flag, p.timeout_ns)) { ok = false; break; }
+              if (!mbar_wait(full_bar(stage), phase, abort_flag, p.timeout_ns)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t d_tmem = tmem_base + slot * static_cast<uint32_t>(N);
+              const int kb0 = c * kBlocksPerChunk;
+              const int nb = min(KPS, p.nk - kb0);
+              for (int b = 0; b < nb; ++b) {
+                const uint64_t da = sdesc_sw128(sA(stage) + b * kBM * kRowBytes);
+                const uint64_t db = sdesc_sw128(sB(stage) + b * N * kRowBytes);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)   // K = 16 per MMA: 32 bytes = 2 descriptor units
+                  mma_f16(d_tmem, da + 2u * k, db + 2u * k, p.idesc, !(b == 0 && k == 0));
+              }
+              mma_commit(empty_bar(stage));
+              mma_commit(accf_bar(slot));
+              stage += static_cast<uint32_t>(NWAY);
+              if (stage >= static_cast<uint32_t>(S)) { stage -= static_cast<uint32_t>(S); phase ^= 1u; }
+              slot += static_cast<uint32_t>(NWAY);
+              if (slot >= static_cast<uint32_t>(p.n_slots)) { slot -= static_cast<uint32_t>(p.n_slots); sph ^= 1u; }
+            }
+            if (NWAY == 2) mine = !mine;
+          }
         }
       }
       if (!ok) {
@@ -602,7 +653,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       mbar_wait(drain_bar, 0, &zero, p.timeout_ns);
     }
     __syncwarp();
-  } else if (warp >= E0) {
+  } else if (warp >= E0 && warp < E0 + EW) {
     // --------------------------------------------------------- epilogue
     if constexpr (EW == 8) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(kRegsEpiWide));
     grid_dep_wait();          // outputs and records: only after the previous kernels
