@@ -662,7 +662,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--e2e-seconds", type=float, default=3.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
-    ap.add_argument("--event-every", type=int, default=8,
+    ap.add_argument("--event-every", type=int, default=16,
                     help="bracket every n-th call's projection kernel with CUDA events")
     ap.add_argument("--copies", type=int, default=0,
                     help="copies of W to rotate (default: enough to exceed 2x L2)")

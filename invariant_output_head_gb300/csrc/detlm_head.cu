@@ -287,17 +287,20 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   p.tmem_cols = tmem_cols_for(p.n_slots * N);
   p.idesc = idesc_f16(h->dtype == DETLM_BF16 ? 1u : 0u, kBM, static_cast<uint32_t>(N));
   p.logits = logits;
-  p.targets = targets;
   p.rec_m = w.m;
   p.rec_i = w.i;
   p.rec_s = w.s;
-  p.zt = w.zt;
   p.err = h->d_err;
   p.stall = h->stall;
   p.timeout_ns = h->timeout_ns;
-  p.rec_b = w.b;
-  p.round_fp16 = h->dtype == DETLM_FP16 ? 1 : 0;
-  if (gate != nullptr) {
+  // the mode's own inputs (these members share storage)
+  if constexpr (MODE == MODE_LOGPROB) {
+    p.targets = targets;
+    p.zt = w.zt;
+  } else if constexpr (MODE == MODE_GATED) {
+    p.rec_b = w.b;
+    p.round_fp16 = h->dtype == DETLM_FP16 ? 1 : 0;
+  } else if constexpr (MODE == MODE_SAMPLE) {
     p.seeds = gate->seeds;
     p.positions = gate->positions;
     p.temperature = gate->temperature;
@@ -317,25 +320,30 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   if (e != cudaSuccess) return status_from_cuda(e);
 
   MergeParams mp;
+  std::memset(&mp, 0, sizeof(mp));
   mp.V = p.V;
   mp.B = p.B;
   mp.n_vt = p.n_vt;
   mp.rec_m = w.m;
   mp.rec_i = w.i;
   mp.rec_s = w.s;
-  mp.zt = w.zt;
-  mp.targets = targets;
   mp.token = token;
   mp.gap = gap;
-  mp.logp = logp;
   mp.err = h->d_err;
   mp.acc = h->acc;
-  mp.rec_b = w.b;
-  mp.round_fp16 = p.round_fp16;
-  mp.tau = gate != nullptr ? gate->tau : 0.0f;
-  mp.base_token = gate != nullptr ? gate->base_token : nullptr;
-  mp.margin = gate != nullptr ? gate->margin : nullptr;
-  mp.score_gap = gate != nullptr ? gate->score_gap : nullptr;
+  if constexpr (MODE == MODE_LOGPROB) {
+    mp.zt = w.zt;
+    mp.targets = targets;
+    mp.logp = logp;
+  } else if constexpr (MODE == MODE_GATED) {
+    mp.rec_b = w.b;
+    mp.round_fp16 = h->dtype == DETLM_FP16 ? 1 : 0;
+    mp.tau = gate->tau;
+    mp.base_token = gate->base_token;
+    mp.margin = gate->margin;
+  } else if constexpr (MODE == MODE_SAMPLE) {
+    mp.score_gap = gate->score_gap;
+  }
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(static_cast<unsigned>(B));
@@ -802,8 +810,8 @@ int detlm_head_verify(detlm_head_t* h, const void* h_dev, int64_t n_req, int64_t
   if (st != DETLM_OK) return st;
   h->acc.P = static_cast<int32_t>(P);
   h->acc.drafts = drafts_dev;
-  h->acc.first_miss = h->vws;
-  h->acc.arrived = h->vws + h->vws_R;
+  h->acc.R = static_cast<int32_t>(h->vws_R);
+  h->acc.words = h->vws;
   h->acc.accepted = accepted_dev;
   st = detlm_head_greedy(h, h_dev, n_req * P, token_dev, gap_dev, logits_dev, stream);
   h->acc = AcceptArgs{};

@@ -78,6 +78,9 @@ constexpr int kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
 enum : int { MODE_GREEDY = 0, MODE_LOGPROB = 1, MODE_INT = 2, MODE_GATED = 3, MODE_SAMPLE = 4 };
 enum : int { ERR_TIMEOUT = 1, ERR_TARGET = 2 };
 
+// Kept at 128 bytes or less: with the parameter struct above 128 bytes the
+// N = 256 log-prob kernel ran 12 % slower on GB300 (same registers and code
+// otherwise). Mode-specific pointers share storage.
 struct HeadParams {
   int32_t V, d, B;
   int32_t N;            // hidden rows per unit (MMA N), multiple of 16, <= kMaxN
@@ -88,22 +91,29 @@ struct HeadParams {
   int32_t stages;
   uint32_t tmem_cols;
   uint32_t idesc;
+  int32_t stall;            // test hook: MMA issuer waits on a dead barrier
+  int32_t n_issuers;        // MMA-issuing threads: 1, or 2 when N <= 128 and both rings are even
   float* logits;            // optional fp32 [B, V]
-  const int32_t* targets;   // logprob: [B]
   float* rec_m;             // [B, n_vt] tile maximum
   int32_t* rec_i;           // [B, n_vt] greedy: lowest index of the maximum
   float* rec_s;             // [B, n_vt] greedy: runner-up; logprob: sum exp
-  float* zt;                // [B] logprob: target logit
   int* err;                 // device error word
-  int32_t stall;            // test hook: MMA issuer waits on a dead barrier
   uint64_t timeout_ns;
-  int32_t n_issuers;        // MMA-issuing threads: 1, or 2 when N <= 128 and both rings are even
-  int32_t* rec_b;           // [B, n_vt] gated: lowest index of the rounded maximum
-  int32_t round_fp16;       // gated: 1 rounds logits to fp16, 0 to bf16
-  const uint64_t* seeds;    // sample: [B] generator key of each row
-  const uint64_t* positions;  // sample: [B] position t of each row
-  float temperature;        // sample: T > 0
+  union {
+    const int32_t* targets;   // logprob: [B]
+    int32_t* rec_b;           // gated: [B, n_vt] lowest index of the rounded maximum
+    const uint64_t* seeds;    // sample: [B] generator key of each row
+  };
+  union {
+    float* zt;                // logprob: [B] target logit
+    const uint64_t* positions;  // sample: [B] position t of each row
+  };
+  union {
+    int32_t round_fp16;       // gated: 1 rounds logits to fp16, 0 to bf16
+    float temperature;        // sample: T > 0
+  };
 };
+static_assert(sizeof(HeadParams) <= 128, "kernel parameter struct above 128 bytes");
 
 // Greedy speculative verify, folded into the merge ("Inference and Decoding",
 // section 6: the target scores every drafted position in one pass and keeps
@@ -116,9 +126,10 @@ struct HeadParams {
 // order-free, so the result does not depend on which block finishes last.
 struct AcceptArgs {
   int32_t P;
+  int32_t R;                // requests (length of each workspace half)
   const int32_t* drafts;    // [R, P]; nullptr: plain greedy call
-  int32_t* first_miss;      // [R] workspace, kMissNone between calls
-  int32_t* arrived;         // [R] workspace, 0 between calls
+  int32_t* words;           // workspace: first_miss [R] (kMissNone between calls),
+                            // then arrived [R] (0 between calls)
   int32_t* accepted;        // [R] output
 };
 constexpr int32_t kMissNone = 0x7f7f7f7f;   // what a 0x7f byte fill leaves
@@ -127,36 +138,46 @@ __device__ __forceinline__ void accept_fold(const AcceptArgs& a, int n, int32_t 
   if (a.drafts == nullptr) return;
   const int r = n / a.P;
   const int j = n - r * a.P;
-  if (tok != a.drafts[n]) atomicMin(a.first_miss + r, j);
+  int32_t* first_miss = a.words + r;
+  int32_t* arrived = a.words + a.R + r;
+  if (tok != a.drafts[n]) atomicMin(first_miss, j);
   __threadfence();
-  if (atomicAdd(a.arrived + r, 1) == a.P - 1) {
+  if (atomicAdd(arrived, 1) == a.P - 1) {
     __threadfence();
-    const int32_t f = atomicExch(a.first_miss + r, kMissNone);
-    a.arrived[r] = 0;
+    const int32_t f = atomicExch(first_miss, kMissNone);
+    *arrived = 0;
     a.accepted[r] = f < a.P ? f : a.P;
   }
 }
 
+// 128 bytes or less, like the projection kernel's parameters; the members
+// of one mode share storage with another mode's.
 struct MergeParams {
   int32_t V, B, n_vt;
+  int32_t round_fp16;       // gated: 1 rounds logits to fp16, 0 to bf16
+  float tau;                // gated: threshold of the margin
   const float* rec_m;
   const int32_t* rec_i;
   const float* rec_s;
-  const float* zt;
-  const int32_t* targets;
   int32_t* token;
   float* gap;
-  float* logp;
   int* err;
+  union {
+    const float* zt;          // logprob: [B] target logit
+    const int32_t* rec_b;     // gated: [B, n_vt]
+  };
+  union {
+    const int32_t* targets;   // logprob: [B]
+    int32_t* base_token;      // gated: optional [B]
+  };
+  union {
+    float* logp;              // logprob: [B]
+    float* margin;            // gated: optional [B]
+    float* score_gap;         // sample: optional [B], best minus runner-up score
+  };
   AcceptArgs acc;
-  // margin gate
-  const int32_t* rec_b;
-  int32_t round_fp16;
-  float tau;
-  int32_t* base_token;      // optional [B]
-  float* margin;            // optional [B]
-  float* score_gap;         // sample: optional [B], best minus runner-up score
 };
+static_assert(sizeof(MergeParams) <= 128, "kernel parameter struct above 128 bytes");
 
 // ------------------------------------------------------------ merge rules
 struct Top2 { float m; int32_t i; float s; };   // max, its lowest index, runner-up
