@@ -1,7 +1,7 @@
 """Benchmark of the batch-invariant output head on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W]
-                    [--workload pr1|sweep|spec|logprob|int8|gated|sample|verify]
+                    [--workload pr1|sweep|spec|logprob|int8|int8f|gated|sample|verify]
                     [--impl ours|reference]
 
 Prints ONE JSON line. A step is one pass of the whole hot path over one batch
@@ -15,6 +15,8 @@ of synthetic input:
 * spec: speculative-verify block, bf16 d=3584, V=152064, B=256, with logits;
 * logprob: trainer scoring, bf16 d=1536, V=151936, 8192 rows, target logp;
 * int8: the integer head d=4096, V=128256 at --batch rows (default 512);
+* int8f: the integer head fed by bf16 rows at --batch rows: the per-token
+  int8 quantization kernel, then the int8 call;
 * gated: the pr1 calls through the margin-gated greedy call (tau = 0.001),
   adding the rounded head's token and its top-two margin per row;
 * sample: the pr1 calls through the seeded sampling call (T = 1, one seed
@@ -64,6 +66,9 @@ WORKLOADS = {
                     mode="logprob", bound="tensor"),
     "int8": dict(desc="integer-only head: int8 d=4096 V=128256, exact int32 logits + token",
                  fmt="int8", V=128256, d=4096, mode="greedy", bound="hbm"),
+    "int8f": dict(desc="integer head fed by float rows: bf16 rows quantized per token (dyadic "
+                       "multiplier), int8 d=4096 V=128256, exact int32 logits + token",
+                  fmt="int8", V=128256, d=4096, mode="int8f", bound="hbm"),
     "gated": dict(desc="margin-gated greedy decode (tau=0.001): bf16 head d=2048 V=32000, "
                        "16 independent B=1 rows, fp32 logits + token + gap + bf16-head token "
                        "+ margin", fmt="bf16", V=32000, d=2048, mode="gated", bound="hbm"),
@@ -204,6 +209,22 @@ def job_rows_per_s(rows_per_step: int, steps: int, world: int, elapsed_ms: float
 
 # ------------------------------------------------------------- workloads
 
+def launches_per_call(mode: str, fmt: str, B: int) -> int:
+    """Kernels one call launches: projection + merge; the int8 head at
+    B >= 256 first converts the rows to fp16; the float-fed int8 call first
+    quantizes them."""
+    n = 2
+    if fmt == "int8" and B >= 256:
+        n += 1
+    if mode == "int8f":
+        n += 1
+    return n
+
+
+def mode_of(name: str) -> str:
+    return WORKLOADS[name]["mode"]
+
+
 def make_inputs(name: str, batch: int):
     import synth
     if name in ("pr1", "gated", "sample"):
@@ -231,9 +252,11 @@ def make_inputs(name: str, batch: int):
     elif name == "logprob":
         c = synth.logprob()
         c["calls"] = [(0, c["h"].shape[0])]
-    elif name == "int8":
+    elif name in ("int8", "int8f"):
         c = synth.int8_head(B=batch)
         c["calls"] = [(0, batch)]
+        if name == "int8f":
+            c["x"] = synth.float_rows(SEED_DRAFTS + 3, batch, c["d"], "bf16", special=False)
     else:
         raise SystemExit(f"unknown workload {name}")
     return c
@@ -255,6 +278,8 @@ def algorithmic(name, c, B):
         by += B * 4 + (B // 16) * 4      # drafts + accepted
     if mode == "sample":
         by += B * 16                     # seeds + positions
+    if mode == "int8f":
+        by += B * d * 2 + B * d + B * 8  # bf16 rows read, int8 rows written, M and S
     return by, 2.0 * B * V * d
 
 
@@ -269,7 +294,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     spec = dict(WORKLOADS[args.workload])
-    if args.workload == "int8" and args.batch >= 256:
+    if args.workload in ("int8", "int8f") and args.batch >= 256:
         spec["bound"] = "tensor"     # fp16-rate tensor-core path, compute-bound
     c = make_inputs(args.workload, args.batch)
     fmt, V, d = c["dtype"], c["V"], c["d"]
@@ -287,6 +312,8 @@ def run_ours(args, rank, world, local_rank):
     Ws = [W0] + [W0.clone() for _ in range(n_copies - 1)]
     heads = [ioh.Head(W, fmt) for W in Ws]
     h_all = to_dev(c["h"])
+    if mode_of(args.workload) == "int8f":
+        x_all = torch.from_numpy(c["x"].view(np.int16)).to(dev).view(torch.bfloat16)
     rows = h_all.shape[0]
     calls = c["calls"]
     maxB = max(B for _, B in calls)
@@ -335,6 +362,11 @@ def run_ours(args, rank, world, local_rank):
                 bd.detlm_head_greedy_gated(hd.handle, hv.data_ptr(), B, GATE_TAU, tok.data_ptr(),
                                            gap.data_ptr(), lg.data_ptr(), base.data_ptr(),
                                            margin.data_ptr(), sp)
+            elif mode == "int8f":
+                tok, gap, lg = outs[j]
+                bd.detlm_head_greedy_from_float(hd.handle, x_all[r0:r0 + B].data_ptr(),
+                                                bd.DETLM_BF16, B, tok.data_ptr(), gap.data_ptr(),
+                                                lg.data_ptr(), None, None, sp)
             elif mode == "sample":
                 tok, gap, lg = outs[j]
                 bd.detlm_head_sample(hd.handle, hv.data_ptr(), B, SAMPLE_T,
@@ -456,7 +488,7 @@ def run_ours(args, rank, world, local_rank):
                      "peak_source": f"MEASURED_PEAKS.json ({peaks['source']}, "
                                     f"{'hbm_gbs' if unit == 'GB/s' else 'bf16_tflops_sustained'})"},
         "bit_stable": bool(stable),
-        "gpu_launches": 2 * n_calls * args.steps,
+        "gpu_launches": args.steps * sum(launches_per_call(mode, fmt, B) for _, B in calls),
         "clocks": clocks,
     }
     if rank == 0 and not args.profile:
@@ -490,6 +522,12 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
     extra = torch.empty(2 * maxB, dtype=torch.int32).pin_memory()   # base+margin / accepted
     sp = stream.cuda_stream
     steps = max(3, min(args.steps, int(args.e2e_seconds / 0.002)))
+    if mode == "int8f":
+        x_host = torch.from_numpy(np.ascontiguousarray(c["x"].view(np.int16))).pin_memory()
+        x_dev = torch.empty((maxB, d), dtype=torch.int16, device=dev)
+        o8 = [torch.empty(maxB, dtype=torch.int32, device=dev),
+              torch.empty(maxB, dtype=torch.int32, device=dev),
+              torch.empty((maxB, V), dtype=torch.int32, device=dev)]
     if mode in ("gated", "verify", "sample"):
         tdt = {"bf16": torch.bfloat16, "fp16": torch.float16}[fmt]
         h_dev = torch.empty((maxB, d), dtype=tdt, device=dev)
@@ -513,6 +551,15 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
             elif mode == "logprob":
                 bd.detlm_head_logprob_host(hd.handle, hp, tg.data_ptr() + r0 * 4, B,
                                            lp.data_ptr(), sp)
+            elif mode == "int8f":
+                with torch.cuda.stream(stream):
+                    x_dev[:B].copy_(x_host[r0:r0 + B], non_blocking=True)
+                    bd.detlm_head_greedy_from_float(hd.handle, x_dev.data_ptr(), bd.DETLM_BF16, B,
+                                                    o8[0].data_ptr(), o8[1].data_ptr(),
+                                                    o8[2].data_ptr(), None, None, sp)
+                    tok[:B].copy_(o8[0][:B], non_blocking=True)
+                    gap[:B].copy_(o8[1][:B], non_blocking=True)
+                    lg[:B].copy_(o8[2][:B], non_blocking=True)
             else:
                 with torch.cuda.stream(stream):
                     h_dev[:B].view(torch.int16).copy_(h_host[r0:r0 + B], non_blocking=True)
@@ -549,6 +596,8 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
         one_step(i)
     torch.cuda.synchronize()
     dt = time.perf_counter() - t
+    if mode == "int8f":
+        esz = 2                          # the bf16 rows are what is copied in
     h2d = sum(B * d * esz + (4 * B if mode in ("logprob", "verify") else 0)
               + (16 * B if mode == "sample" else 0) for _, B in calls)
     d2h = sum(4 * B if mode == "logprob" else 8 * B + 4 * B * V for _, B in calls)
@@ -557,7 +606,8 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
     api = {"greedy": "detlm_head_greedy_host", "logprob": "detlm_head_logprob_host",
            "gated": "detlm_head_greedy_gated + pinned copies on the call's stream",
            "verify": "detlm_head_verify + pinned copies on the call's stream",
-           "sample": "detlm_head_sample + pinned copies on the call's stream"}[mode]
+           "sample": "detlm_head_sample + pinned copies on the call's stream",
+           "int8f": "detlm_head_greedy_from_float + pinned copies on the call's stream"}[mode]
     return {"value": round(rows_per_step * steps / dt, 2), "unit": "rows/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps, "api": api}
 
@@ -594,6 +644,9 @@ def oracle_row(name, c, r):
     fmt, h, mode = c["dtype"], c["h"], WORKLOADS[name]["mode"]
     if mode == "logprob":
         return oracle.head_logprob(c["W"], h[r:r + 1], c["targets"][r:r + 1], fmt)
+    if mode == "int8f":
+        q, _, _ = oracle.quantize_rows(oracle.decode(c["x"][r:r + 1], "bf16"))
+        return oracle.head_greedy(c["W"], q, "int8")
     out = oracle.head_greedy(c["W"], h[r:r + 1], fmt)
     if mode == "gated":
         out["gate"] = oracle.gated_greedy(out["logits"], GATE_TAU, fmt)
