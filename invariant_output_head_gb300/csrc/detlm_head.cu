@@ -366,8 +366,20 @@ cudaError_t launch_int8_t(const CUtensorMap& tmW, const CUtensorMap& tmH, const 
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  int8_gemm_kernel<N><<<grid, kI8Threads, smem, stream>>>(tmW, tmH, p);
-  return cudaGetLastError();
+  // a programmatic dependent of the previous kernel on the stream (its
+  // prologue and W prefetch overlap that kernel's tail)
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kI8Threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, int8_gemm_kernel<N>, tmW, tmH, p);
 }
 
 cudaError_t launch_int8_n(int N, const CUtensorMap& tmW, const CUtensorMap& tmH,
@@ -605,8 +617,17 @@ int launch_quantize(const void* x_dev, int dtype, int64_t B, int64_t d, int8_t* 
   qp.q = q;
   qp.mult = mult;
   qp.shift = shift;
-  quantize_rows_kernel<<<static_cast<unsigned>(B), kQThreads, 0, stream>>>(qp);
-  return status_from_cuda(cudaGetLastError());
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(B));
+  cfg.blockDim = dim3(kQThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return status_from_cuda(cudaLaunchKernelEx(&cfg, quantize_rows_kernel, qp));
 }
 
 }  // namespace

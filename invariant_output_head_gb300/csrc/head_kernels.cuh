@@ -514,9 +514,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   __syncthreads();
   tc_fence_after();
   // Launched as a dependent grid: the set-up above overlapped the previous
-  // kernels on the stream. The merge kernel may be scheduled at once (it
-  // waits for this grid to complete before reading anything).
-  grid_dep_launch();
+  // kernels on the stream.
   const uint32_t tmem_base = *tmem_holder;
   const int n_units = p.n_vt * p.n_nt;
   const int kElems = kRowBytes / 2;     // 16-bit elements per 128-byte row
@@ -878,6 +876,10 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
 
   tc_fence_before();
   __syncthreads();
+  // the merge kernel may be scheduled now: triggered at the end, not after
+  // the set-up, because B waiting merge blocks would share the SMs' issue
+  // slots with this kernel for its whole run
+  grid_dep_launch();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, p.tmem_cols);

@@ -219,17 +219,36 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_h = policy_evict_last();
+      // W is read-only for the head's life: the W boxes of the first S8
+      // stages are requested before waiting for the previous kernels on the
+      // stream; the hidden rows (which a previous kernel may write) after.
+      const int n_my = (n_units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                       static_cast<int>(gridDim.x);
+      const int pre = min(S8, n_my > 0 ? n_my * p.nk : 0);
+      for (int j = 0; j < pre; ++j) {
+        const int u = blockIdx.x + (j / p.nk) * gridDim.x;
+        const int vt = u / p.n_nt, kb = j - (j / p.nk) * p.nk;
+        mbar_expect_tx(f8full(j), L.st8);
+        tma_load_2d(base + j * L.st8, &tmW, kb * kRowBytes, vt * kBM, f8full(j), pol_w);
+      }
+      grid_dep_wait();
       uint32_t stage = 0, phase = 0, outstanding = 0, out_par = 0;
       bool ok = true;
+      int j = 0;                     // stages issued by this CTA
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const int vt = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
-        for (int kb = 0; kb < p.nk; ++kb) {
-          if (!mbar_wait(f8empty(stage), phase ^ 1u, abort_flag, p.timeout_ns)) { ok = false; break; }
-          outstanding &= ~(1u << stage);
-          mbar_arrive_expect_tx(f8full(stage), L.st8);
+        for (int kb = 0; kb < p.nk; ++kb, ++j) {
           const uint32_t a = base + stage * L.st8;
-          tma_load_2d(a, &tmW, kb * kRowBytes, vt * kBM, f8full(stage), pol_w);
-          tma_load_2d(a + L.a8, &tmH, kb * kRowBytes, nt * N, f8full(stage), pol_h);
+          if (j < pre) {             // W already requested: add the hidden rows
+            tma_load_2d(a + L.a8, &tmH, kb * kRowBytes, nt * N, f8full(stage), pol_h);
+            mbar_arrive(f8full(stage));
+          } else {
+            if (!mbar_wait(f8empty(stage), phase ^ 1u, abort_flag, p.timeout_ns)) { ok = false; break; }
+            outstanding &= ~(1u << stage);
+            mbar_arrive_expect_tx(f8full(stage), L.st8);
+            tma_load_2d(a, &tmW, kb * kRowBytes, vt * kBM, f8full(stage), pol_w);
+            tma_load_2d(a + L.a8, &tmH, kb * kRowBytes, nt * N, f8full(stage), pol_h);
+          }
           outstanding |= 1u << stage;
           out_par = (out_par & ~(1u << stage)) | (phase << stage);
           if (++stage == static_cast<uint32_t>(S8)) { stage = 0; phase ^= 1u; }
@@ -316,6 +335,7 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     }
   } else {
     // --------------------------------------------------------- epilogue
+    grid_dep_wait();          // logits and records: only after the previous kernels
     const int q = warp & 3;
     const int et = threadIdx.x - 64;
     const int row = q * 32 + lane;
@@ -389,6 +409,8 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
 
   tc_fence_before();
   __syncthreads();
+  // the merge kernel may be scheduled now (at the end: waiting merge blocks
+  // would take issue slots from the converter warps)
   grid_dep_launch();
   if (warp == 1) {
     tc_fence_after();
@@ -407,6 +429,7 @@ struct Int8MergeParams {
 };
 
 __global__ void __launch_bounds__(kMergeThreads) int8_merge_kernel(const Int8MergeParams p) {
+  grid_dep_launch();  // the next call's kernel 1 may start (it prefetches only W)
   grid_dep_wait();
   const int n = blockIdx.x;
   const int g = threadIdx.x;

@@ -14,6 +14,7 @@
 // shift is exact. An all-zero row gives q = 0, M = 0, S = 0.
 #pragma once
 #include <cstdint>
+#include "ptx.cuh"
 
 namespace detlm {
 
@@ -54,6 +55,11 @@ __device__ __forceinline__ void q_decode(uint32_t mag, int fmt, uint32_t& X, int
 }
 
 __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(const QuantParams p) {
+  // launched as a dependent grid: the int8 projection that follows may
+  // start at once (it prefetches only W before waiting for this grid); x and
+  // q may be in use by the previous kernels on the stream until they complete
+  grid_dep_launch();
+  grid_dep_wait();
   const int64_t n = blockIdx.x;
   const int fmt = p.fmt;
   const size_t eb = fmt == QF_FP32 ? 4 : 2;
