@@ -522,15 +522,13 @@ int launch_int8(detlm_head* h, const void* h_dev, int64_t B, int32_t* token, int
   p.n_nt = static_cast<int32_t>((B + N - 1) / N);
   p.nk = h->nk;
   p.n_chunks = int8_chunks(h->d);
-  // fp16 ring of 3 stages when that leaves at least 4 int8 stages, else 2
-  const uint32_t fixed = int8_layout(N, 0, 0).total + (2u * kI8MaxStages8 + 2u * 3u) * 8u + 1024u;
-  const Int8Layout one = int8_layout(N, 1, 1);
-  p.s16 = 3;
-  if (static_cast<int64_t>(kSmemLimit) - fixed - 3 * one.st16 < 4 * static_cast<int64_t>(one.st8)) p.s16 = 2;
-  p.s8 = static_cast<int32_t>((kSmemLimit - fixed - p.s16 * one.st16) / one.st8);
-  if (p.s8 > kI8MaxStages8) p.s8 = kI8MaxStages8;
-  if (p.s8 < 2) return DETLM_EINVAL;   // cannot happen for N <= kI8MaxN
-  p.tmem_cols = tmem_cols_for(2 * p.n_chunks * N);
+  // as many int8 stages as shared memory holds (the W bytes in flight per SM
+  // set the rate)
+  const uint32_t fixed = int8_layout(N, 0).total + 3u * kI8MaxStages * 8u + 1024u;
+  const uint32_t stage_bytes = int8_layout(N, 1).stage;
+  p.stages = static_cast<int32_t>((kSmemLimit - fixed) / stage_bytes);
+  if (p.stages > kI8MaxStages) p.stages = kI8MaxStages;
+  if (p.stages < 2) return DETLM_EINVAL;   // cannot happen for N <= kI8MaxN
   p.idesc = idesc_f16(0u, kBM, static_cast<uint32_t>(N));
   p.logits = logits;
   p.rec_m = reinterpret_cast<int32_t*>(w.m);
@@ -540,7 +538,7 @@ int launch_int8(detlm_head* h, const void* h_dev, int64_t B, int32_t* token, int
   p.stall = h->stall;
   p.timeout_ns = h->timeout_ns;
 
-  const size_t smem = int8_layout(N, p.s8, p.s16).total + 1024;
+  const size_t smem = int8_layout(N, p.stages).total + 1024;
   const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
   const int grid = static_cast<int>(units < h->num_sms ? units : h->num_sms);
   if (h->t_start) cudaEventRecord(h->t_start, stream);
