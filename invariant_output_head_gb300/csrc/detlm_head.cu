@@ -126,10 +126,18 @@ int stages_for(int N, bool gated = false) {
   return s;
 }
 
-// Two MMA-issuing threads where the kernel allows it (N <= 128) and both
-// rings they wait on have even lengths (the kernel's parity waits rely on it).
-int issuers_for(int N, int stages, int slots) {
-  return (max_mma_issuers(N) == 2 && stages % 2 == 0 && slots % 2 == 0) ? 2 : 1;
+// MMA-issuing threads: the most the kernel allows (N <= 128: 3) that divides
+// the stage ring's length and leaves at least that many chunk slots; the slot
+// ring is then cut to a multiple of it (the kernel's parity waits rely on
+// both).
+int issuers_for(int N, int stages, int* slots) {
+  for (int k = max_mma_issuers(N); k > 1; --k) {
+    if (stages % k == 0 && *slots >= k) {
+      *slots -= *slots % k;
+      return k;
+    }
+  }
+  return 1;
 }
 
 int status_from_cuda(cudaError_t e) {
@@ -283,7 +291,7 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   p.n_slots = slots_for(N);
   constexpr bool kExtraSmem = MODE == MODE_GATED || MODE == MODE_SAMPLE;
   p.stages = stages_for(N, kExtraSmem);
-  p.n_issuers = issuers_for(N, p.stages, p.n_slots);
+  p.n_issuers = issuers_for(N, p.stages, &p.n_slots);
   p.tmem_cols = tmem_cols_for(p.n_slots * N);
   p.idesc = idesc_f16(h->dtype == DETLM_BF16 ? 1u : 0u, kBM, static_cast<uint32_t>(N));
   p.logits = logits;
@@ -458,7 +466,7 @@ int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token
   p.n_chunks = static_cast<int32_t>((h->d + kChunkK - 1) / kChunkK);
   p.n_slots = slots_for(N);
   p.stages = stages_for(N);
-  p.n_issuers = issuers_for(N, p.stages, p.n_slots);
+  p.n_issuers = issuers_for(N, p.stages, &p.n_slots);
   p.tmem_cols = tmem_cols_for(p.n_slots * N);
   p.idesc = idesc_f16(0u, kBM, static_cast<uint32_t>(N));
   p.logits = reinterpret_cast<float*>(logits);
@@ -1013,7 +1021,7 @@ extern "C" int detlm_greedy_noalloc(const void* W_dev, int64_t V, int64_t d, int
   p.n_chunks = static_cast<int32_t>((d + kChunkK - 1) / kChunkK);
   p.n_slots = slots_for(N);
   p.stages = stages_for(N);
-  p.n_issuers = issuers_for(N, p.stages, p.n_slots);
+  p.n_issuers = issuers_for(N, p.stages, &p.n_slots);
   p.tmem_cols = tmem_cols_for(p.n_slots * N);
   p.idesc = idesc_f16(dtype == DETLM_BF16 ? 1u : 0u, kBM, static_cast<uint32_t>(N));
   p.logits = logits_dev;

@@ -92,7 +92,7 @@ struct HeadParams {
   uint32_t tmem_cols;
   uint32_t idesc;
   int32_t stall;            // test hook: MMA issuer waits on a dead barrier
-  int32_t n_issuers;        // MMA-issuing threads: 1, or 2 when N <= 128 and both rings are even
+  int32_t n_issuers;        // MMA-issuing threads: 1 .. 3 (N <= 128, ring lengths multiples of it)
   float* logits;            // optional fp32 [B, V]
   float* rec_m;             // [B, n_vt] tile maximum
   int32_t* rec_i;           // [B, n_vt] greedy: lowest index of the maximum
@@ -389,15 +389,16 @@ __device__ __forceinline__ int brev4(int l) {
 __host__ __device__ constexpr int epi_warps_for(int N) { return N > 128 ? 8 : 4; }
 __host__ __device__ constexpr int epi_first_warp(int N) { return N > 128 ? 4 : 2; }
 __host__ __device__ constexpr int kblocks_per_stage(int N) { return N > 128 ? 1 : 2; }
-// Up to N = 128 a second thread (warp 6) can issue the MMAs of every other
-// K chunk: one thread's tcgen05.mma issue rate holds back the TMA ring at
-// small N. Each chunk keeps its own MMAs in K order, so the arithmetic does
-// not change. The host enables it only when both rings the issuers wait on
-// (stages, chunk slots) have even lengths: then a chunk and the one a ring
-// length earlier belong to the same issuer and every parity wait is
-// unambiguous (the kernel refuses other combinations).
-__host__ __device__ constexpr int max_mma_issuers(int N) { return N > 128 ? 1 : 2; }
-__host__ __device__ constexpr int threads_for(int N) { return N > 128 ? 384 : 224; }
+// Up to N = 128 warps 6 and 7 can issue MMAs too, every second or third K
+// chunk round robin: one thread's tcgen05.mma issue rate holds back the TMA
+// ring at small N. Each chunk keeps its own MMAs in K order, so the
+// arithmetic does not change. The host uses k issuers only when both rings
+// the issuers wait on (stages, chunk slots) have lengths that are multiples
+// of k: then a chunk and the one a ring length earlier belong to the same
+// issuer and every parity wait is unambiguous (the kernel refuses other
+// combinations).
+__host__ __device__ constexpr int max_mma_issuers(int N) { return N > 128 ? 1 : 3; }
+__host__ __device__ constexpr int threads_for(int N) { return N > 128 ? 384 : 256; }
 constexpr int kRegsLaunchWide = 168;   // registers per thread at launch, N = 256
 constexpr int kRegsWg0Wide = 40;
 constexpr int kRegsEpiWide = 232;
@@ -456,7 +457,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   constexpr int KPS = kblocks_per_stage(N);     // K boxes per stage
   constexpr int WBLK = NBLK / (EW / 4);         // 16-column blocks per epilogue warp
   constexpr int E0 = epi_first_warp(N);         // first epilogue warp
-  const int NWAY = p.n_issuers;                 // MMA-issuing threads (1 or 2)
+  const int NWAY = p.n_issuers;                 // MMA-issuing threads (1 .. 3)
   static_assert(N <= kMaxN && NBLK % (EW / 4) == 0 && kBlocksPerChunk % KPS == 0, "shape");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -586,10 +587,10 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       }
     }
     __syncwarp();
-  } else if (warp == 1 || (max_mma_issuers(N) == 2 && warp == E0 + EW)) {
+  } else if (warp == 1 || (max_mma_issuers(N) > 1 && warp >= E0 + EW)) {
     // ------------------------------------------------------- MMA issuer
     if constexpr (EW == 8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegsWg0Wide));
-    const int which = warp == 1 ? 0 : 1;             // chunks which, which + NWAY, ...
+    const int which = warp == 1 ? 0 : warp - (E0 + EW) + 1;   // chunks which, which + NWAY, ...
     if (lane == 0 && which < NWAY) {
       constexpr int SPC = kBlocksPerChunk / KPS;     // pipeline stages per chunk
       // ring lengths must be multiples of NWAY (the host only enables two
@@ -634,10 +635,10 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
         // with the other issuer in between)
         static_assert(SPC == 1, "one pipeline stage per chunk");
         uint32_t stage = which, phase = 0, slot = which, sph = 0;
-        bool mine = which == 0;
+        int turn = 0;                                // this chunk's issuer
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
           for (int c = 0; c < p.n_chunks && ok; ++c) {
-            if (mine) {
+            if (turn == which) {
               if (!mbar_wait(acce_bar(slot), sph ^ 1u, abort_flag, p.timeout_ns)) { ok = false; break; }
               if (!mbar_wait(full_bar(stage), phase, abort_flag, p.timeout_ns)) { ok = false; break; }
               tc_fence_after();
@@ -658,7 +659,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
               slot += static_cast<uint32_t>(NWAY);
               if (slot >= static_cast<uint32_t>(p.n_slots)) { slot -= static_cast<uint32_t>(p.n_slots); sph ^= 1u; }
             }
-            if (NWAY == 2) mine = !mine;
+            if (++turn == NWAY) turn = 0;
           }
         }
       }
