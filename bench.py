@@ -113,12 +113,25 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def projection_kernel(workload: str, batch: int) -> str:
+    """Name of the call's projection kernel (the one the roofline covers)."""
+    if WORKLOADS[workload]["fmt"] == "int8" and batch < 256:
+        return "int8_gemm_kernel"
+    return "head_gemm_kernel"
+
+
+def profiled_traffic(workload: str, batch: int):
     """DRAM bytes per launch of the projection kernel from a committed ncu
-    summary (profiles/<kernel>_<workload>.md), only while the kernel sources
-    still hash to the value recorded with the capture."""
-    path = os.path.join(ROOT, "profiles", f"head_gemm_{workload}.md")
-    if not os.path.exists(path):
+    summary (profiles/<kernel>_<workload>[_b<batch>].md), only while the
+    kernel sources still hash to the value recorded with the capture."""
+    kern = projection_kernel(workload, batch).replace("_kernel", "")
+    path = None
+    for name in (f"{kern}_{workload}_b{batch}.md", f"{kern}_{workload}.md"):
+        cand = os.path.join(ROOT, "profiles", name)
+        if os.path.exists(cand):
+            path = cand
+            break
+    if path is None:
         return None
     vals = {}
     with open(path) as f:
@@ -456,7 +469,7 @@ def run_ours(args, rank, world, local_rank):
     else:
         achieved = fl_launch / avg_kernel_s / 1e12
         peak, unit = peaks["bf16_tflops_sustained"], "TFLOP/s"
-    traffic = profiled_traffic(args.workload)
+    traffic = profiled_traffic(args.workload, args.batch)
 
     value = job_rows_per_s(rows_per_step, args.steps, world, elapsed_ms)
     res = {
@@ -472,7 +485,8 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": spec["bound"], "achieved": round(achieved, 1),
                      "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "kernel": "head_gemm_kernel",
+                     "traffic": traffic,
+                     "kernel": projection_kernel(args.workload, args.batch),
                      "kernel_us_per_launch": round(avg_kernel_s * 1e6, 2),
                      "timed_launches": int(kms.size),
                      "steady_us_per_call": round(elapsed_ms * 1e3 / (args.steps * n_calls), 2),
