@@ -104,12 +104,23 @@ def measured_peaks():
             "source": "fallback"}
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and blank lines (string literals in
+    these files hold no comment markers)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the CUDA sources' code (comments and blank lines ignored):
+    a profile summary applies while this matches its recorded value."""
     src = os.path.join(ROOT, "invariant_output_head_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(src)):
-        with open(os.path.join(src, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
+        with open(os.path.join(src, f), encoding="utf-8") as fh:
+            h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -20,24 +20,27 @@
 // ascending chunk order. This keeps every logit within 1e-6 * sum|w h| and
 // is the same arithmetic for every B.
 //
-// Warp 0 issues TMA loads into an S-stage ring, warp 1 (and, up to N = 128,
-// warp 6, alternate chunks) issues the MMAs into the chunk slot ring, warps
-// 2..5 drain each slot into running sums (one
-// thread per vocabulary row, up to 128 hidden rows per thread), then write
-// the optional fp32 logits and the per-tile decision record of each hidden
-// row:
+// Warp 0 issues TMA loads into an S-stage ring; warp 1 (and, up to N = 128,
+// warps 6 and 7, round robin over K chunks) issues the MMAs into the chunk
+// slot ring; the epilogue warps (2..5, or eight warps 4..11 at N = 256) drain
+// each slot into running sums (one thread per vocabulary row and up to 128
+// hidden-row columns), then write the optional fp32 logits and the per-tile
+// record of each hidden row:
 //   greedy : (m, i, s) = tile maximum, lowest index attaining it, runner-up
-//            value of the tile's multiset;
-//   logprob: (m, S) = tile maximum and sum_v exp(z_v - m), plus z[target];
-//            within a warp the exact maximum comes first and the 32 terms
-//            exp(z - m_warp) are added in a fixed tree, then the four warps'
-//            (m, S) pairs merge in a fixed order.
+//            value of the tile's multiset (gated: also the lowest index of
+//            the maximum of the logits rounded to 16 bits; sampling: the
+//            same record over the scores z/T + G);
+//   logprob: (m, S) = tile maximum and sum_v exp(z_v - m), plus z[target]:
+//            per column, each half-warp takes the exact maximum of its 16
+//            rows and adds their exp(z - m) in ascending row order; the two
+//            halves and then the four 32-row quarters merge in a fixed order.
 //
 // Kernel 2 (merge_kernel): one 128-thread block per hidden row folds the
 // n_vt tile records in a fixed order that depends on V only: thread g folds
 // tiles g, g+128, g+256, ... in ascending order, then the 128 partial
 // results combine in a balanced binary tree over g (pairs g^1, g^2, ...,
-// g^64). No atomics take part in any result.
+// g^64). No atomics take part in any logit, token, gap or log-probability
+// (the speculative-verify fold's atomicMin is order-free).
 //
 // Both reductions are written so that a row's bits do not depend on its
 // column position in the tile or on B: the greedy record is exact (a
