@@ -128,6 +128,8 @@ def projection_kernel(workload: str, batch: int) -> str:
     """Name of the call's projection kernel (the one the roofline covers)."""
     if WORKLOADS[workload]["fmt"] == "int8" and batch < 256:
         return "int8_gemm_kernel"
+    if workload == "logprob":
+        return "head_rows_kernel"
     return "head_gemm_kernel"
 
 

@@ -19,6 +19,7 @@
 #include "head_kernels.cuh"
 #include "int8_kernels.cuh"
 #include "quant_kernels.cuh"
+#include "rows_kernels.cuh"
 
 using namespace detlm;
 
@@ -28,6 +29,7 @@ struct detlm_head {
   int64_t V = 0, d = 0;
   const void* W = nullptr;
   CUtensorMap tmW;
+  CUtensorMap tmW256;        // float heads: box of 256 rows (the rows kernel's N)
   int n_vt = 0, nk = 0, num_sms = 0;
   int* d_err = nullptr;
   // split-V record workspace
@@ -267,13 +269,51 @@ struct ModeArgs {
   float* score_gap = nullptr;
 };
 
+// Stages of the rows kernel: as many 48 KB stages as shared memory holds.
+int rows_stages() {
+  const RowsLayout L1 = rows_layout(1);
+  const uint32_t fixed = L1.total - L1.stage_bytes + 2u * kRowsMaxStages * 8u + 1024u;
+  int s = static_cast<int>((kSmemLimit - fixed) / L1.stage_bytes);
+  return s > kRowsMaxStages ? kRowsMaxStages : s;
+}
+
+// The rows kernel's launch (384 threads, the register split of the wide
+// swap-AB kernel), a programmatic dependent of the previous kernel.
+cudaError_t launch_rows_kernel(const CUtensorMap& tmW, const CUtensorMap& tmH, const HeadParams& p,
+                               int grid, size_t smem, cudaStream_t stream) {
+  auto kern = head_rows_kernel;
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kRegsLaunchWide) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kRowsThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmW, tmH, p);
+}
+
 template <int MODE>
 int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* targets,
                  int32_t* token, float* gap, float* logits, float* logp, cudaStream_t stream,
                  const ModeArgs* gate = nullptr) {
-  const int N = cols_for(B);
+  // the log-prob call runs on the rows kernel for every B (its records are
+  // folded per row, in a fixed order, whatever B is)
+  constexpr bool rows = MODE == MODE_LOGPROB;
+  const int N = rows ? kRowsN : cols_for(B);
   CUtensorMap tmH;
-  if (!encode_2d(&tmH, h->dtype, h_dev, h->d, B, static_cast<uint32_t>(N))) return DETLM_EINVAL;
+  if (!encode_2d(&tmH, h->dtype, h_dev, h->d, B, rows ? static_cast<uint32_t>(kRowsM)
+                                                      : static_cast<uint32_t>(N)))
+    return DETLM_EINVAL;
   int st = ensure_ws(h, B, stream);
   if (st != DETLM_OK) return st;
   const WsView w = ws_view(h, B);
@@ -284,16 +324,27 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   p.d = static_cast<int32_t>(h->d);
   p.B = static_cast<int32_t>(B);
   p.N = N;
-  p.n_vt = h->n_vt;
-  p.n_nt = static_cast<int32_t>((B + N - 1) / N);
   p.nk = h->nk;
   p.n_chunks = static_cast<int32_t>((h->d + kChunkK - 1) / kChunkK);
-  p.n_slots = slots_for(N);
   constexpr bool kExtraSmem = MODE == MODE_GATED || MODE == MODE_SAMPLE;
-  p.stages = stages_for(N, kExtraSmem);
-  p.n_issuers = issuers_for(N, p.stages, &p.n_slots);
-  p.tmem_cols = tmem_cols_for(p.n_slots * N);
-  p.idesc = idesc_f16(h->dtype == DETLM_BF16 ? 1u : 0u, kBM, static_cast<uint32_t>(N));
+  if (rows) {
+    // units: 256-entry vocabulary tiles x 128-row hidden tiles
+    p.n_vt = static_cast<int32_t>((h->V + kRowsN - 1) / kRowsN);
+    p.n_nt = static_cast<int32_t>((B + kRowsM - 1) / kRowsM);
+    p.n_slots = 2;
+    p.stages = rows_stages();
+    p.n_issuers = 1;
+    p.tmem_cols = 512;
+    p.idesc = idesc_f16(h->dtype == DETLM_BF16 ? 1u : 0u, kRowsM, kRowsN);
+  } else {
+    p.n_vt = h->n_vt;
+    p.n_nt = static_cast<int32_t>((B + N - 1) / N);
+    p.n_slots = slots_for(N);
+    p.stages = stages_for(N, kExtraSmem);
+    p.n_issuers = issuers_for(N, p.stages, &p.n_slots);
+    p.tmem_cols = tmem_cols_for(p.n_slots * N);
+    p.idesc = idesc_f16(h->dtype == DETLM_BF16 ? 1u : 0u, kBM, static_cast<uint32_t>(N));
+  }
   p.logits = logits;
   p.rec_m = w.m;
   p.rec_i = w.i;
@@ -314,13 +365,17 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
     p.temperature = gate->temperature;
   }
 
-  const SmemLayout L = smem_layout(N, p.stages, kExtraSmem);
-  const size_t smem = L.total + 1024;
+  const size_t smem = rows ? rows_layout(p.stages).total + 1024
+                           : smem_layout(N, p.stages, kExtraSmem).total + 1024;
   const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
   const int grid = static_cast<int>(units < h->num_sms ? units : h->num_sms);
 
   if (h->t_start) cudaEventRecord(h->t_start, stream);
-  cudaError_t e = launch_gemm<MODE>(h->tmW, tmH, p, grid, smem, stream);
+  cudaError_t e;
+  if constexpr (rows)
+    e = launch_rows_kernel(h->tmW256, tmH, p, grid, smem, stream);
+  else
+    e = launch_gemm<MODE>(h->tmW, tmH, p, grid, smem, stream);
   if (h->t_stop) {
     cudaEventRecord(h->t_stop, stream);
     h->t_start = h->t_stop = nullptr;
@@ -683,6 +738,11 @@ int detlm_head_create(detlm_head_t** out, const void* W_dev, int64_t V, int64_t 
   h->n_vt = static_cast<int>((V + kBM - 1) / kBM);
   h->nk = static_cast<int>((d * static_cast<int64_t>(elem_bytes(dtype)) + kRowBytes - 1) / kRowBytes);
   h->timeout_ns = kDefaultTimeoutNs;
+  if (dtype != DETLM_INT8 && !encode_2d(&h->tmW256, dtype, W_dev, d, V, kRowsN)) {
+    cudaFree(h->d_err);
+    delete h;
+    return DETLM_EINVAL;
+  }
   if (!encode_2d(&h->tmW, dtype, W_dev, d, V, kBM)) {
     delete h;
     return DETLM_EINVAL;

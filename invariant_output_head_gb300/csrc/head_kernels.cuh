@@ -29,11 +29,11 @@
 //   greedy : (m, i, s) = tile maximum, lowest index attaining it, runner-up
 //            value of the tile's multiset (gated: also the lowest index of
 //            the maximum of the logits rounded to 16 bits; sampling: the
-//            same record over the scores z/T + G);
-//   logprob: (m, S) = tile maximum and sum_v exp(z_v - m), plus z[target]:
-//            per column, each half-warp takes the exact maximum of its 16
-//            rows and adds their exp(z - m) in ascending row order; the two
-//            halves and then the four 32-row quarters merge in a fixed order.
+//            same record over the scores z/T + G).
+// The log-prob call has its own projection kernel (head_rows_kernel, in
+// rows_kernels.cuh) with the same K chunks and fold, hence the same logits;
+// its record per (row, 256-entry vocabulary tile) is (m, S) = the tile's
+// maximum and sum_v exp(z_v - m), plus z[target].
 //
 // Kernel 2 (merge_kernel): one 128-thread block per hidden row folds the
 // n_vt tile records in a fixed order that depends on V only: thread g folds
@@ -43,10 +43,10 @@
 // (the speculative-verify fold's atomicMin is order-free).
 //
 // Both reductions are written so that a row's bits do not depend on its
-// column position in the tile or on B: the greedy record is exact (a
-// function of the multiset of values), and every floating-point sum of the
-// log-sum-exp runs in a tree whose shape is the same for every column, with
-// operators that are commutative bit for bit.
+// position in the tile or on B: the greedy record is exact (a function of
+// the multiset of values), and every floating-point sum of the log-sum-exp
+// runs in an order fixed by V alone, the same for every row, with operators
+// that are commutative bit for bit.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -311,22 +311,6 @@ __device__ __forceinline__ Top2 xp_gated(const float* xp, int lane, int v_row0, 
   return top2_merge(t, shfl_xor(t, 16));
 }
 
-// log-prob: exact maximum M of the 16 rows, then sum of exp(z - M) in
-// ascending row order; the two halves merge commutatively
-__device__ __forceinline__ Lse xp_lse(const float* xp, int lane) {
-  const int c = lane & 15, h = lane >> 4;
-  float m = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) m = fmaxf(m, xp[(h * 16 + j) * kXpStride + c]);
-  float sum = 0.0f;
-  if (m != -INFINITY) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      sum = __fadd_rn(sum, __expf(xp[(h * 16 + j) * kXpStride + c] - m));
-  }
-  return lse_merge(Lse{m, sum}, shfl_xor(Lse{m, sum}, 16));
-}
-
 // integer head: exact (max, lowest row, runner-up); INT32_MIN marks rows
 // outside the vocabulary (|z| is far below 2^31)
 __device__ __forceinline__ ITop2 xp_itop2(const int32_t* xp, int lane, int v_row0) {
@@ -425,11 +409,11 @@ __host__ __device__ inline SmemLayout smem_layout(int N, int stages, bool gated 
   // barriers: full[S], empty[S], slot_full[kMaxSlots], slot_empty[kMaxSlots],
   // never, drain; then the TMEM address holder and the abort flag
   L.red_off = L.ctrl_off + (2u * stages + 2u * kMaxSlots + 2u) * 8u + 16u;
-  // per-quadrant column results: 3 words x 4 quadrants x N columns, the
-  // unit's target rows (N words), then the epilogue warps' transpose areas
-  // (gated: 4 x N more words, the quadrants' lowest indices of the rounded
-  // maximum)
-  L.xp_off = L.red_off + 3u * 4u * static_cast<uint32_t>(N) * 4u + static_cast<uint32_t>(N) * 4u +
+  // per-quadrant column results: 3 words x 4 quadrants x N columns (gated and
+  // sampling: 4 x N more words, the quadrants' lowest indices of the rounded
+  // maximum or the columns' sampling keys), then the epilogue warps'
+  // transpose areas
+  L.xp_off = L.red_off + 3u * 4u * static_cast<uint32_t>(N) * 4u +
              (gated ? 4u * static_cast<uint32_t>(N) * 4u : 0u);
   L.total = L.xp_off + static_cast<uint32_t>(epi_warps_for(N)) * kXpWords * 4u;
   return L;
@@ -484,8 +468,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   float* red_m = reinterpret_cast<float*>(smem + L.red_off);
   int32_t* red_i = reinterpret_cast<int32_t*>(red_m + 4 * N);
   float* red_s = reinterpret_cast<float*>(red_i + 4 * N);
-  int* tgt_row = reinterpret_cast<int*>(red_s + 4 * N);   // log-prob: target row in tile, or -1
-  int32_t* red_b = tgt_row + N;                            // gated: [4][N]
+  int32_t* red_b = reinterpret_cast<int32_t*>(red_s + 4 * N);   // gated: [4][N]
   uint32_t* skey = reinterpret_cast<uint32_t*>(red_b);     // sample: [4][N] seed lo/hi, t lo/hi
   float* xpose = reinterpret_cast<float*>(smem + L.xp_off);
   const uint32_t smem_base = smem_u32(smem);
@@ -736,16 +719,6 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       const int v = vt * kBM + row;
       const bool vok = v < p.V;
       const int n0 = nt * N;
-      if constexpr (MODE == MODE_LOGPROB) {
-        // stage each column's target row within this tile once (the barrier
-        // after the folds below orders these writes before the reads)
-        for (int c = et; c < N; c += ET) {
-          const int n = n0 + c;
-          const int t = n < p.B ? p.targets[n] - vt * kBM : -1;
-          tgt_row[c] = (t >= 0 && t < kBM) ? t : -1;
-        }
-        named_bar_sync(1, ET);
-      }
       if constexpr (MODE == MODE_SAMPLE) {
         // the unit's column keys, once per unit (ordered before the reads by
         // this barrier, after the previous unit's reads by the one above)
@@ -808,7 +781,8 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
             red_i[q * N + c0 + lane] = t.i;
             red_s[q * N + c0 + lane] = t.s;
           }
-        } else if constexpr (MODE == MODE_GATED) {
+        } else {
+          static_assert(MODE == MODE_GATED, "the log-prob call runs on head_rows_kernel");
           int32_t i16;
           const Top2 t = xp_gated(xp, lane, vt * kBM + q * 32, p.round_fp16 != 0, i16);
           if (lane < 16) {
@@ -816,15 +790,6 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
             red_i[q * N + c0 + lane] = t.i;
             red_s[q * N + c0 + lane] = t.s;
             red_b[q * N + c0 + lane] = i16;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (tgt_row[c0 + i] == row) p.zt[n0 + c0 + i] = acc[bb][i];
-          const Lse t = xp_lse(xp, lane);
-          if (lane < 16) {
-            red_m[q * N + c0 + lane] = t.m;
-            red_s[q * N + c0 + lane] = t.S;
           }
         }
         __syncwarp();
@@ -845,7 +810,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           reinterpret_cast<int32_t*>(p.rec_m)[o] = r.m;
           p.rec_i[o] = r.i;
           reinterpret_cast<int32_t*>(p.rec_s)[o] = r.s;
-        } else if constexpr (MODE == MODE_GREEDY || MODE == MODE_GATED || MODE == MODE_SAMPLE) {
+        } else {
           Top2 t[4];
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq)
@@ -861,13 +826,6 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
             for (int qq = 0; qq < 4; ++qq) b[qq] = Low16{round16(t[qq].m, f16), red_b[qq * N + c]};
             p.rec_b[o] = low16_merge(low16_merge(b[0], b[1]), low16_merge(b[2], b[3])).i;
           }
-        } else {
-          Lse t[4];
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) t[qq] = Lse{red_m[qq * N + c], red_s[qq * N + c]};
-          const Lse r = lse_merge(lse_merge(t[0], t[1]), lse_merge(t[2], t[3]));
-          p.rec_m[o] = r.m;
-          p.rec_s[o] = r.S;
         }
       }
       named_bar_sync(1, ET);
