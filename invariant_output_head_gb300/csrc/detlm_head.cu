@@ -29,8 +29,8 @@ struct detlm_head {
   int64_t V = 0, d = 0;
   const void* W = nullptr;
   CUtensorMap tmW;
-  CUtensorMap tmW256;        // float heads: box of 256 rows (the rows kernel's N)
   int n_vt = 0, nk = 0, num_sms = 0;
+  int rows_pairs = 0;        // CTA pairs of the rows kernel that fit at once (0: not asked yet)
   int* d_err = nullptr;
   // split-V record workspace
   void* ws = nullptr;
@@ -269,7 +269,7 @@ struct ModeArgs {
   float* score_gap = nullptr;
 };
 
-// Stages of the rows kernel: as many 48 KB stages as shared memory holds.
+// Stages of the rows kernel: as many 32 KB stages as shared memory holds.
 int rows_stages() {
   const RowsLayout L1 = rows_layout(1);
   const uint32_t fixed = L1.total - L1.stage_bytes + 2u * kRowsMaxStages * 8u + 1024u;
@@ -277,10 +277,12 @@ int rows_stages() {
   return s > kRowsMaxStages ? kRowsMaxStages : s;
 }
 
-// The rows kernel's launch (384 threads, the register split of the wide
-// swap-AB kernel), a programmatic dependent of the previous kernel.
-cudaError_t launch_rows_kernel(const CUtensorMap& tmW, const CUtensorMap& tmH, const HeadParams& p,
-                               int grid, size_t smem, cudaStream_t stream) {
+// The rows kernel's launch: clusters of two CTAs (384 threads each, the
+// register split of the wide swap-AB kernel), as many pairs as fit on the
+// GPU at once up to one per unit, a programmatic dependent of the previous
+// kernel.
+cudaError_t launch_rows_kernel(detlm_head* h, const CUtensorMap& tmH, const HeadParams& p,
+                               int64_t units, size_t smem, cudaStream_t stream) {
   auto kern = head_rows_kernel;
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, kern);
@@ -290,16 +292,30 @@ cudaError_t launch_rows_kernel(const CUtensorMap& tmW, const CUtensorMap& tmH, c
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kRowsThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmW, tmH, p);
+  if (h->rows_pairs == 0) {
+    cfg.gridDim = dim3(static_cast<unsigned>(h->num_sms & ~1));
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters <= 0) return cudaErrorInvalidConfiguration;
+    h->rows_pairs = clusters < h->num_sms / 2 ? clusters : h->num_sms / 2;
+  }
+  const int64_t pairs = units < h->rows_pairs ? units : h->rows_pairs;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, h->tmW, tmH, p);
 }
 
 template <int MODE>
@@ -311,7 +327,7 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   constexpr bool rows = MODE == MODE_LOGPROB;
   const int N = rows ? kRowsN : cols_for(B);
   CUtensorMap tmH;
-  if (!encode_2d(&tmH, h->dtype, h_dev, h->d, B, rows ? static_cast<uint32_t>(kRowsM)
+  if (!encode_2d(&tmH, h->dtype, h_dev, h->d, B, rows ? static_cast<uint32_t>(kRowsHalf)
                                                       : static_cast<uint32_t>(N)))
     return DETLM_EINVAL;
   int st = ensure_ws(h, B, stream);
@@ -328,7 +344,7 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   p.n_chunks = static_cast<int32_t>((h->d + kChunkK - 1) / kChunkK);
   constexpr bool kExtraSmem = MODE == MODE_GATED || MODE == MODE_SAMPLE;
   if (rows) {
-    // units: 256-entry vocabulary tiles x 128-row hidden tiles
+    // units: 256-entry vocabulary tiles x 256-row hidden tiles (one CTA pair)
     p.n_vt = static_cast<int32_t>((h->V + kRowsN - 1) / kRowsN);
     p.n_nt = static_cast<int32_t>((B + kRowsM - 1) / kRowsM);
     p.n_slots = 2;
@@ -373,7 +389,7 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   if (h->t_start) cudaEventRecord(h->t_start, stream);
   cudaError_t e;
   if constexpr (rows)
-    e = launch_rows_kernel(h->tmW256, tmH, p, grid, smem, stream);
+    e = launch_rows_kernel(h, tmH, p, units, smem, stream);
   else
     e = launch_gemm<MODE>(h->tmW, tmH, p, grid, smem, stream);
   if (h->t_stop) {
@@ -738,11 +754,6 @@ int detlm_head_create(detlm_head_t** out, const void* W_dev, int64_t V, int64_t 
   h->n_vt = static_cast<int>((V + kBM - 1) / kBM);
   h->nk = static_cast<int>((d * static_cast<int64_t>(elem_bytes(dtype)) + kRowBytes - 1) / kRowBytes);
   h->timeout_ns = kDefaultTimeoutNs;
-  if (dtype != DETLM_INT8 && !encode_2d(&h->tmW256, dtype, W_dev, d, V, kRowsN)) {
-    cudaFree(h->d_err);
-    delete h;
-    return DETLM_EINVAL;
-  }
   if (!encode_2d(&h->tmW, dtype, W_dev, d, V, kBM)) {
     delete h;
     return DETLM_EINVAL;

@@ -1,9 +1,11 @@
 // ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA, tcgen05.
 //
 // Only instructions of the public PTX ISA for sm_100a/sm_103a are used:
-// mbarrier.*, cp.async.bulk.tensor (tile mode, no multicast), createpolicy,
-// tcgen05.{alloc,dealloc,relinquish_alloc_permit,mma,commit,ld,wait,fence},
-// griddepcontrol and %globaltimer.
+// mbarrier.*, cp.async.bulk.tensor (tile mode, no multicast; the pair form
+// with its barrier in the peer CTA), createpolicy,
+// tcgen05.{alloc,dealloc,relinquish_alloc_permit,mma,commit,ld,wait,fence}
+// (cta_group::1 and ::2), mapa, barrier.cluster, ex2.approx, griddepcontrol
+// and %globaltimer.
 #pragma once
 #include <cstdint>
 
@@ -171,6 +173,85 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr) {
 // (ab_fmt 1 = bf16, 0 = f16), both K-major, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_fmt, uint32_t M, uint32_t N) {
   return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// ------------------------------------------------- CTA pairs (2-SM MMA)
+// A cluster of two CTAs: rank 0 (the leader) issues tcgen05.mma.cta_group::2,
+// which takes A and half of B from each CTA's shared memory at the same
+// offset and writes each CTA's 128 rows of D into that CTA's tensor memory.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+// All threads of both CTAs (release / acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster (address from
+// cluster_addr), with the instruction's default semantics. What it hands
+// over is tensor memory this thread has finished reading (tcgen05.wait::ld
+// returned before it). A release at cluster scope here cost ~0.6 us per
+// arrival on GB300.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" :: "r"(cluster_bar) : "memory");
+}
+// 2-D tiled load into this CTA's shared memory whose completion is counted
+// on an mbarrier that may sit in the peer CTA (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int32_t c0,
+                                                 int32_t c1, uint32_t cluster_bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
+      ".mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(cluster_bar),
+         "l"(policy)
+      : "memory");
+}
+// Tensor memory of a CTA pair: one warp of each CTA takes part.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t holder_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+               :: "r"(holder_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
+               :: "r"(taddr), "r"(ncols) : "memory");
+}
+// D (256 rows over the pair) (+)= A * B^T, issued by one thread of the leader.
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// One arrival, once the leader's earlier pair MMAs are complete, on the
+// mbarrier at this shared-memory offset in every CTA named by cta_mask.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;"
+      :: "r"(bar), "h"(cta_mask) : "memory");
+}
+
+// 2^x by the special-function unit (ex2.approx.ftz: relative error about
+// 2^-22, results below 2^-126 flushed to zero).
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // -------------------------------------------------------- misc / launches

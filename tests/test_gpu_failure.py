@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 import synth
-from tests.gpu_helpers import check_float_greedy, dev, host, oracle_float_rows
+from tests.gpu_helpers import check_float_greedy, dev, host, logprob_tol, oracle_float_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -47,6 +47,26 @@ def test_stalled_wait_reports_timeout_and_context_survives(env, fmt):
     assert head.check() == b.DETLM_OK
     ref = oracle.head_greedy(case["W"], case["h"], fmt)
     assert (host(t) == ref["token"]).all()
+
+
+def test_stalled_logprob_pair_kernel_times_out_and_recovers(env):
+    """The log-prob projection runs on CTA pairs: the stalled leader's MMA
+    warp gives up, both CTAs' waits run out, and the next call is right."""
+    torch, b = env
+    case = synth.small_float(5, 900, 384, 300)
+    head = b.Head(dev(case["W"], "bf16"), "bf16")
+    h, t = dev(case["h"], "bf16"), dev(case["targets"], "int32")
+    b.detlm_head_debug(head.handle, b.DETLM_DEBUG_STALL, 20_000_000)
+    head.logprob(h, t)
+    torch.cuda.synchronize()
+    assert head.check() == b.DETLM_ETIMEOUT
+    b.detlm_head_debug(head.handle, 0, 0)
+    lp = host(head.logprob(h, t))
+    assert head.check() == b.DETLM_OK
+    z_ref, A = oracle_float_rows(case["W"], case["h"], "bf16")
+    lp_ref = oracle.logprob(z_ref, case["targets"])
+    tol = logprob_tol(A, oracle.logsumexp(z_ref), case["targets"])
+    assert (np.abs(lp.astype(np.float64) - lp_ref) <= tol).all()
 
 
 def test_out_of_range_target_gives_nan_and_status(env):
