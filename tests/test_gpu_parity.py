@@ -67,6 +67,26 @@ def test_float_logprob_parity(torch_cuda, fmt, V, d, B):
     assert (lp <= 0).all()
 
 
+@pytest.mark.parametrize("V,d,B", [(300, 200, 600), (1, 32, 5), (257, 64, 257), (512, 72, 256)])
+def test_float_logprob_pair_tiling(torch_cuda, V, d, B):
+    """The log-prob projection's units are 256 hidden rows x 256 vocabulary
+    entries on a CTA pair (each CTA 128 rows and one 128-entry half of the
+    W tile): ragged row tiles (a pair whose second CTA has no valid row),
+    vocabulary tiles whose second half is partly or wholly past V, K shorter
+    than or not a multiple of a 64-element box."""
+    from invariant_output_head_gb300 import Head
+    case = synth.small_float(900 + V + d + B, V, d, B, fmt="bf16")
+    head = Head(dev(case["W"], "bf16"), "bf16")
+    t = case["targets"]
+    lp = host(head.logprob(dev(case["h"], "bf16"), dev(t, "int32")))
+    assert head.check() == 0
+    z_ref, A = oracle_float_rows(case["W"], case["h"], "bf16")
+    lp_ref = oracle.logprob(z_ref, t)
+    tol = logprob_tol(A, oracle.logsumexp(z_ref), t)
+    err = np.abs(lp.astype(np.float64) - lp_ref)
+    assert (err <= tol).all(), (err.max(), tol[np.argmax(err - tol)])
+
+
 @pytest.mark.parametrize("V,d", [(1000, 1040), (16, 16), (130, 2064), (1, 32)])
 @pytest.mark.parametrize("B", [1, 5, 33, 100])
 def test_int8_greedy_exact(torch_cuda, V, d, B):
