@@ -113,12 +113,22 @@ def _code_only(text: str) -> str:
     return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources' code (comments and blank lines ignored):
-    a profile summary applies while this matches its recorded value."""
+# The source files that make up each projection kernel and its launch: a
+# change elsewhere leaves that kernel's profile summary valid.
+KERNEL_SOURCES = {
+    "head_gemm_kernel": ("detlm_head.cu", "head_kernels.cuh", "ptx.cuh"),
+    "head_rows_kernel": ("detlm_head.cu", "head_kernels.cuh", "ptx.cuh", "rows_kernels.cuh"),
+    "int8_gemm_kernel": ("detlm_head.cu", "head_kernels.cuh", "int8_kernels.cuh", "ptx.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the code (comments and blank lines ignored) of the files that
+    make up `kernel`: its profile summary applies while this matches the
+    value recorded with the capture."""
     src = os.path.join(ROOT, "invariant_output_head_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(src)):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(src, f), encoding="utf-8") as fh:
             h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
@@ -137,7 +147,8 @@ def profiled_traffic(workload: str, batch: int):
     """DRAM bytes per launch of the projection kernel from a committed ncu
     summary (profiles/<kernel>_<workload>[_b<batch>].md), only while the
     kernel sources still hash to the value recorded with the capture."""
-    kern = projection_kernel(workload, batch).replace("_kernel", "")
+    kernel = projection_kernel(workload, batch)
+    kern = kernel.replace("_kernel", "")
     path = None
     for name in (f"{kern}_{workload}_b{batch}.md", f"{kern}_{workload}.md"):
         cand = os.path.join(ROOT, "profiles", name)
@@ -152,7 +163,7 @@ def profiled_traffic(workload: str, batch: int):
             if line.startswith("- ") and ":" in line:
                 k, v = line[2:].split(":", 1)
                 vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash(kernel):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])

@@ -318,22 +318,36 @@ head_rows_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
           p.zt[n] = z;
         }
         const int nv = min(128, p.V - vb);      // valid entries in this half
-        float m = -INFINITY;
-#pragma unroll
-        for (int bb = 0; bb < 8; ++bb)
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (bb * 16 + i < nv) m = fmaxf(m, acc[bb][i]);
         // exp(z - m) = 2^(z log2(e) - m log2(e)): one fma and one ex2 per
         // entry (the rounding of m log2(e) scales the half's whole sum by
-        // the same factor, within |m| 2^-24 in the log)
-        const float ml = m * kLog2e;
-        float sum = 0.0f;
+        // the same factor, within |m| 2^-24 in the log). The tail is bound
+        // by instruction issue, so a full half (every tile but possibly the
+        // last) runs without the per-entry bound test.
+        float m = -INFINITY, sum = 0.0f;
+        if (nv == 128) {
 #pragma unroll
-        for (int bb = 0; bb < 8; ++bb)
+          for (int bb = 0; bb < 8; ++bb)
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (bb * 16 + i < nv) sum = __fadd_rn(sum, exp2_approx(fmaf(acc[bb][i], kLog2e, -ml)));
+            for (int i = 0; i < 16; ++i) m = fmaxf(m, acc[bb][i]);
+          const float ml = m * kLog2e;
+#pragma unroll
+          for (int bb = 0; bb < 8; ++bb)
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              sum = __fadd_rn(sum, exp2_approx(fmaf(acc[bb][i], kLog2e, -ml)));
+        } else {
+#pragma unroll
+          for (int bb = 0; bb < 8; ++bb)
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (bb * 16 + i < nv) m = fmaxf(m, acc[bb][i]);
+          const float ml = m * kLog2e;
+#pragma unroll
+          for (int bb = 0; bb < 8; ++bb)
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (bb * 16 + i < nv) sum = __fadd_rn(sum, exp2_approx(fmaf(acc[bb][i], kLog2e, -ml)));
+        }
         ls = Lse{m, sum};
       }
       // ---- the two halves of a row: the second hands its record to the first
