@@ -32,6 +32,7 @@ struct detlm_head {
   int n_vt = 0, nk = 0, num_sms = 0;
   int rows_pairs = 0;        // CTA pairs of the rows kernel that fit at once (0: not asked yet)
   int* d_err = nullptr;
+  int* err_host = nullptr;   // pinned word the error word is read into
   // split-V record workspace
   void* ws = nullptr;
   int64_t ws_B = 0;
@@ -652,10 +653,11 @@ int launch_int8(detlm_head* h, const void* h_dev, int64_t B, int32_t* token, int
 }
 
 int read_err(detlm_head* h, cudaStream_t stream) {
-  int hv = 0;
-  cudaError_t e = cudaMemcpyAsync(&hv, h->d_err, sizeof(int), cudaMemcpyDeviceToHost, stream);
+  // into a pinned word: a copy to pageable memory costs an extra staging step
+  cudaError_t e = cudaMemcpyAsync(h->err_host, h->d_err, sizeof(int), cudaMemcpyDeviceToHost, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return status_from_cuda(e);
+  const int hv = *h->err_host;
   if (hv != 0) {
     e = cudaMemsetAsync(h->d_err, 0, sizeof(int), stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
@@ -760,8 +762,11 @@ int detlm_head_create(detlm_head_t** out, const void* W_dev, int64_t V, int64_t 
   }
   e = cudaMalloc(&h->d_err, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&h->err_host), sizeof(int),
+                                          cudaHostAllocDefault);
   if (e != cudaSuccess) {
     if (h->d_err) cudaFree(h->d_err);
+    if (h->err_host) cudaFreeHost(h->err_host);
     delete h;
     return status_from_cuda(e);
   }
@@ -1002,6 +1007,7 @@ void detlm_head_destroy(detlm_head_t* h) {
   if (h->h16) cudaFree(h->h16);
   if (h->stage) cudaFree(h->stage);
   if (h->d_err) cudaFree(h->d_err);
+  if (h->err_host) cudaFreeHost(h->err_host);
   delete h;
 }
 
