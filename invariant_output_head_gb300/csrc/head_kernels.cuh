@@ -475,6 +475,16 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   auto sA = [&](int s) { return smem_base + static_cast<uint32_t>(s) * L.stage_bytes; };
   auto sB = [&](int s) { return sA(s) + L.a_bytes; };
 
+  const int kElems = kRowBytes / 2;     // 16-bit elements per 128-byte row
+  // stages whose W boxes the producer requests before the previous kernels
+  // on the stream have finished (at most the ring, at most this CTA's work)
+  auto pre_stages = [&]() {
+    const int units = p.n_vt * p.n_nt, per_unit = (p.nk + KPS - 1) / KPS;
+    const int n_my = (units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                     static_cast<int>(gridDim.x);
+    return min(S, n_my > 0 ? n_my * per_unit : 0);
+  };
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
@@ -488,10 +498,25 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
     mbar_init(drain_bar, static_cast<uint32_t>(NWAY));
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmH);
+    // this thread is the TMA producer: W is read-only for the life of the
+    // head, so the W boxes of the first S stages are requested now, before
+    // the tensor-memory allocation and before waiting for the previous
+    // kernels on the stream; the hidden rows (which a previous kernel may
+    // write) only after that wait
+    const uint64_t pol_w = policy_evict_first();
+    const int pre = pre_stages(), spu = (p.nk + KPS - 1) / KPS;
+    for (int j = 0; j < pre; ++j) {
+      const int u = blockIdx.x + (j / spu) * gridDim.x;
+      const int vt = u / p.n_nt, st = j - (j / spu) * spu;
+      const int kb0 = st * KPS;
+      const int nb = min(KPS, p.nk - kb0);
+      mbar_expect_tx(full_bar(j), static_cast<uint32_t>(nb) * (kBM + N) * kRowBytes);
+      for (int b = 0; b < nb; ++b)
+        tma_load_2d(sA(j) + b * kBM * kRowBytes, &tmW, (kb0 + b) * kElems, vt * kBM,
+                    full_bar(j), pol_w);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), p.tmem_cols);
@@ -504,7 +529,6 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   // kernels on the stream.
   const uint32_t tmem_base = *tmem_holder;
   const int n_units = p.n_vt * p.n_nt;
-  const int kElems = kRowBytes / 2;     // 16-bit elements per 128-byte row
   const int spu = (p.nk + KPS - 1) / KPS;   // stages per unit
 
   if (warp == 0) {
@@ -513,22 +537,8 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_h = policy_evict_last();
-      // W is read-only for the life of the head, so the W boxes of the first
-      // S stages are requested before waiting for the previous kernels; the
-      // hidden rows (which a previous kernel may write) only after.
-      const int n_my = (n_units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                       static_cast<int>(gridDim.x);
-      const int pre = min(S, n_my > 0 ? n_my * spu : 0);
-      for (int j = 0; j < pre; ++j) {
-        const int u = blockIdx.x + (j / spu) * gridDim.x;
-        const int vt = u / p.n_nt, st = j - (j / spu) * spu;
-        const int kb0 = st * KPS;
-        const int nb = min(KPS, p.nk - kb0);
-        mbar_expect_tx(full_bar(j), static_cast<uint32_t>(nb) * (kBM + N) * kRowBytes);
-        for (int b = 0; b < nb; ++b)
-          tma_load_2d(sA(j) + b * kBM * kRowBytes, &tmW, (kb0 + b) * kElems, vt * kBM,
-                      full_bar(j), pol_w);
-      }
+      // (the W boxes of the first `pre` stages were requested in the set-up)
+      const int pre = pre_stages();
       grid_dep_wait();
       uint32_t stage = 0, phase = 0, outstanding = 0, out_par = 0;
       bool ok = true;

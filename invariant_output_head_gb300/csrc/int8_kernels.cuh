@@ -228,6 +228,14 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   int32_t* red_s = red_i + 4 * N;
   int32_t* xpose = reinterpret_cast<int32_t*>(smem + L.xp);
   const uint32_t base = smem_u32(smem);
+  // stages whose W boxes the producer requests before the previous kernels
+  // on the stream have finished (at most the ring, at most this CTA's work)
+  auto pre_stages = [&]() {
+    const int units = p.n_vt * p.n_nt;
+    const int n_my = (units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                     static_cast<int>(gridDim.x);
+    return min(S, n_my > 0 ? n_my * p.nk : 0);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -241,10 +249,21 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     mbar_init(drain_bar, 2);
     *abort_flag = 0;
     fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmH);
+    // this thread is the TMA producer: W is read-only for the head's life,
+    // so the W boxes of the first S stages are requested now, before the
+    // tensor-memory allocation and before waiting for the previous kernels
+    // on the stream; the hidden rows (which a previous kernel may write)
+    // only after that wait
+    const uint64_t pol_w = policy_evict_first();
+    const int pre = pre_stages();
+    for (int j = 0; j < pre; ++j) {
+      const int u = blockIdx.x + (j / p.nk) * gridDim.x;
+      const int vt = u / p.n_nt, kb = j - (j / p.nk) * p.nk;
+      mbar_expect_tx(full(j), L.tx);
+      tma_load_2d(base + j * L.stage, &tmW, kb * kRowBytes, vt * kBM, full(j), pol_w);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), 512u);
@@ -262,18 +281,8 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_h = policy_evict_last();
-      // W is read-only for the head's life: the W boxes of the first S
-      // stages are requested before waiting for the previous kernels on the
-      // stream; the hidden rows (which a previous kernel may write) after.
-      const int n_my = (n_units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                       static_cast<int>(gridDim.x);
-      const int pre = min(S, n_my > 0 ? n_my * p.nk : 0);
-      for (int j = 0; j < pre; ++j) {
-        const int u = blockIdx.x + (j / p.nk) * gridDim.x;
-        const int vt = u / p.n_nt, kb = j - (j / p.nk) * p.nk;
-        mbar_expect_tx(full(j), L.tx);
-        tma_load_2d(base + j * L.stage, &tmW, kb * kRowBytes, vt * kBM, full(j), pol_w);
-      }
+      // (the W boxes of the first `pre` stages were requested in the set-up)
+      const int pre = pre_stages();
       grid_dep_wait();
       uint32_t stage = 0, phase = 0, outstanding = 0, out_par = 0;
       bool ok = true;
