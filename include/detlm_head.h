@@ -107,6 +107,11 @@ int detlm_head_greedy(detlm_head_t* head, const void* h_dev, int64_t B,
  * ("batch-logprob-gap": the trainer's per-token log-probability;
  * "Inference and Decoding", section 3, Temperature: softmax at tau = 1).
  * A target outside [0, V) gives NaN and sets DETLM_ETARGET in the error word.
+ * targets_dev: int32 [B]; logp_dev: float [B]. B == 0 is a no-op. h_dev must
+ * be 16-byte aligned; targets_dev and logp_dev 4-byte aligned. The log-sum-
+ * exp runs in a fixed order per row (exact maximum and sum of exp(z - max)
+ * per 256-entry vocabulary tile, tiles merged in an order set by V alone),
+ * so logp_dev[n] is the same bits for any B and any co-rows.
  * INT8 heads return DETLM_EUNSUPPORTED. */
 int detlm_head_logprob(detlm_head_t* head, const void* h_dev,
                        const int32_t* targets_dev, int64_t B, float* logp_dev,
