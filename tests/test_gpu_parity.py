@@ -87,6 +87,42 @@ def test_float_logprob_pair_tiling(torch_cuda, V, d, B):
     assert (err <= tol).all(), (err.max(), tol[np.argmax(err - tol)])
 
 
+@pytest.mark.parametrize("sigma_h", [60.0, 1e-3])
+def test_float_logprob_extreme_scales(torch_cuda, sigma_h):
+    """Logits up to ~125 in magnitude (most exp(z - max) flush to zero; the
+    rounding of max * log2(e) is largest here) and below ~2e-3 (every entry
+    contributes almost exactly 1)."""
+    from invariant_output_head_gb300 import Head
+    case = synth.small_float(77, 1000, 520, 300, fmt="bf16", sigma_h=sigma_h)
+    head = Head(dev(case["W"], "bf16"), "bf16")
+    t = case["targets"]
+    lp = host(head.logprob(dev(case["h"], "bf16"), dev(t, "int32")))
+    assert head.check() == 0
+    z_ref, A = oracle_float_rows(case["W"], case["h"], "bf16")
+    lp_ref = oracle.logprob(z_ref, t)
+    tol = logprob_tol(A, oracle.logsumexp(z_ref), t)
+    err = np.abs(lp.astype(np.float64) - lp_ref)
+    assert (err <= tol).all(), (err.max(), tol[np.argmax(err - tol)])
+
+
+def test_float_logprob_equal_logits(torch_cuda):
+    """Every vocabulary row the same: all logits of a row are equal, so
+    logp = -log V for every target (ties inside every tile and across
+    tiles)."""
+    from invariant_output_head_gb300 import Head
+    V, d, B = 700, 264, 40
+    case = synth.small_float(78, V, d, B, fmt="bf16")
+    W = np.repeat(case["W"][:1], V, axis=0)
+    head = Head(dev(W, "bf16"), "bf16")
+    t = case["targets"]
+    lp = host(head.logprob(dev(case["h"], "bf16"), dev(t, "int32")))
+    assert head.check() == 0
+    z_ref, A = oracle_float_rows(W, case["h"], "bf16")
+    assert np.allclose(oracle.logprob(z_ref, t), -np.log(V), rtol=0, atol=1e-12)
+    tol = logprob_tol(A, oracle.logsumexp(z_ref), t)
+    assert (np.abs(lp.astype(np.float64) + np.log(V)) <= tol).all()
+
+
 @pytest.mark.parametrize("V,d", [(1000, 1040), (16, 16), (130, 2064), (1, 32)])
 @pytest.mark.parametrize("B", [1, 5, 33, 100])
 def test_int8_greedy_exact(torch_cuda, V, d, B):
