@@ -103,6 +103,9 @@ def test_float_logprob_extreme_scales(torch_cuda, sigma_h):
     tol = logprob_tol(A, oracle.logsumexp(z_ref), t)
     err = np.abs(lp.astype(np.float64) - lp_ref)
     assert (err <= tol).all(), (err.max(), tol[np.argmax(err - tol)])
+    # the greedy call on the same rows (gap in bf16 ulps at large and tiny m)
+    tok, gap, z = head.greedy(dev(case["h"], "bf16"), with_logits=True)
+    check_float_greedy(z_ref, A, host(tok), host(gap), host(z), label=f"scale {sigma_h}")
 
 
 def test_float_logprob_equal_logits(torch_cuda):
