@@ -274,8 +274,9 @@ int detlm_head_tiles(const detlm_head_t* head, int64_t B, int32_t* n_vtiles,
  * are then undefined). NULL: the error word lives in the static array and is
  * not reported.
  * The first call on each device looks up the array's device address with
- * that device current (a one-time runtime query, no allocation); make that
- * first call before capturing any stream. All calls share the array and it
+ * that device current (a one-time runtime query, no allocation; repeated
+ * once after a device reset, which gives the device a new context); make
+ * that first call before capturing any stream. All calls share the array and it
  * keeps the last call's contents (each call clears what must start at zero):
  * calls that may run at the same time on the GPU (other streams, other host
  * threads) race on it and must be serialised by the caller. */

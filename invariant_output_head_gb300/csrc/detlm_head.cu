@@ -1026,17 +1026,41 @@ namespace {
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+CUcontext g_noalloc_ctx[kNoAllocMaxDevices] = {};
 
-// Device address of the scratch array on the current device (looked up on
-// the first call per device, with that device current).
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+std::once_flag g_ctx_once;
+
+// The calling thread's current context (the one the symbol lookup is valid
+// in), or nullptr when the driver entry point is unavailable.
+CUcontext current_context() {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  });
+  CUcontext c = nullptr;
+  if (g_ctx_current == nullptr || g_ctx_current(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+// Device address of the scratch array on the current device, looked up with
+// that device current the first time a context of it calls in; the cached
+// address is keyed to the context, so a device reset (a new primary context)
+// looks it up again.
 int noalloc_scratch(int dev, void** out) {
   if (dev < 0 || dev >= kNoAllocMaxDevices) return DETLM_EUNSUPPORTED;
+  const CUcontext ctx = current_context();
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  if (g_noalloc_ptr[dev] == nullptr || ctx == nullptr || g_noalloc_ctx[dev] != ctx) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, detlm_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) return DETLM_ECUDA;
     g_noalloc_ptr[dev] = p;
+    g_noalloc_ctx[dev] = current_context();
   }
   *out = g_noalloc_ptr[dev];
   return DETLM_OK;
@@ -1060,7 +1084,8 @@ extern "C" int detlm_greedy_noalloc(const void* W_dev, int64_t V, int64_t d, int
   if (gap_dev == nullptr || !aligned(gap_dev, 4)) return DETLM_EINVAL;
   if (logits_dev != nullptr && !aligned(logits_dev, 4)) return DETLM_EINVAL;
   if (err_dev != nullptr && !aligned(err_dev, 4)) return DETLM_EINVAL;
-  // scratch: error word (256 B), then rec_m, rec_i, rec_s [n_vt, B]
+  // scratch: error word (256 B), then rec_m, rec_i, rec_s [B, n_vt], each
+  // part rounded up to 256 bytes
   const int n_vt = static_cast<int>((V + kBM - 1) / kBM);
   const size_t part = ws_part(static_cast<int64_t>(n_vt) * B);
   if (256 + 3 * part > DETLM_NOALLOC_SCRATCH_BYTES) return DETLM_EINVAL;

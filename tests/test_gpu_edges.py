@@ -1,7 +1,7 @@
 """Edge cases across the entry points: empty batches (every call returns at
 once and the handle keeps working), the largest supported integer K
-(d = 16384, |logit| up to 2^28, streaming and wide paths), a long float K,
-the largest row count of the no-alloc scratch and d = 8 (one partial K box).
+(d = 16384, |logit| up to 2^28, streaming and wide paths), a long float K
+and d = 8 (one partial K box).
 """
 import numpy as np
 import pytest

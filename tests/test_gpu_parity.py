@@ -210,8 +210,10 @@ def test_verify_accept(torch_cuda, fmt):
 
 @pytest.mark.parametrize("R,P", [(1, 1), (3, 1), (1, 33), (5, 40), (9, 7)])
 def test_verify_accept_shapes(torch_cuda, R, P):
-    """Ragged request counts and draft lengths (one warp covers 32 positions;
-    P > 32 takes a second ballot)."""
+    """Ragged request counts and draft lengths: single-position requests,
+    P above a warp's 32 lanes, and request counts that leave the last merge
+    blocks of a request in different waves (each row's block lowers its
+    request's first-miss word with an order-free atomicMin)."""
     from invariant_output_head_gb300 import Head
     torch = torch_cuda
     case = synth.small_float(62 + P, 300, 136, R * P)

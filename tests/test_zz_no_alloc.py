@@ -6,9 +6,11 @@ allocate, a latency-critical path that cannot take the synchronisation an
 allocation implies). ``detlm_greedy_noalloc`` serves them: its workspace is a
 static device array inside the library. This file checks, through the C ABI,
 that two calls in a row give the same results as the handle-based
-``detlm_head_greedy`` (the tolerance is the one every float parity test uses),
-that a batch too large for the static array is refused before any GPU work,
-and that later calls leave the device's free memory unchanged.
+``detlm_head_greedy`` (bit for bit, since the kernels and their parameters are
+the same; against the oracle within the tolerance every float parity test
+uses), that the largest batch the static array holds gives the handle path's
+bits too while one more row is refused before any GPU work, and that later
+calls leave the device's free memory unchanged.
 
 The file is named to be collected last.
 """
@@ -65,6 +67,8 @@ def test_noalloc_matches_handle_path_two_calls(env, fmt):
         torch.cuda.synchronize()
         assert int(host(err)[0]) == 0
         assert (host(tok) == host(t_ref)).all()
+        assert (host(lg).view(np.uint32) == host(l_ref).view(np.uint32)).all()
+        assert (host(gap).view(np.uint32) == host(g_ref).view(np.uint32)).all()
         e = LOGIT_RTOL * A[r0:r0 + B]
         assert (np.abs(host(lg).astype(np.float64) - host(l_ref)) <= e).all()
         assert (np.abs(host(lg).astype(np.float64) - z_ref[r0:r0 + B]) <= e).all()
@@ -73,12 +77,54 @@ def test_noalloc_matches_handle_path_two_calls(env, fmt):
     head.close()
 
 
+def _max_rows(V):
+    """Largest B the static array holds: the error word's 256 bytes and three
+    record arrays of 4 * ceil(V / 128) * B bytes, each rounded up to 256."""
+    n_vt = (V + 127) // 128
+
+    def need(B):
+        return 256 + 3 * ((4 * n_vt * B + 255) // 256 * 256)
+    B = (8 << 20) // (12 * n_vt)
+    while need(B) > (8 << 20):
+        B -= 1
+    while need(B + 1) <= (8 << 20):
+        B += 1
+    return B
+
+
+def test_noalloc_largest_batch_bitwise(env):
+    """V = 32000: the largest batch that fits (several 256-row column tiles)
+    gives the handle path's bits; one row more is refused."""
+    torch, lib, b = env
+    V, d = 32000, 64
+    Bmax = _max_rows(V)
+    assert Bmax > 256
+    case = synth.small_float(4343, V, d, Bmax)
+    W = dev(case["W"], "bf16")
+    h = dev(case["h"], "bf16")
+    st, tok, gap, lg, err = _noalloc(lib, torch, W, V, d, b.DETLM_BF16, h, Bmax)
+    assert st == b.DETLM_OK, b.status_string(st)
+    head = b.Head(W, "bf16")
+    t_ref, g_ref, l_ref = head.greedy(h, with_logits=True)
+    torch.cuda.synchronize()
+    assert int(host(err)[0]) == 0
+    assert (host(tok) == host(t_ref)).all()
+    assert (host(gap).view(np.uint32) == host(g_ref).view(np.uint32)).all()
+    assert (host(lg).view(np.uint32) == host(l_ref).view(np.uint32)).all()
+    rows = np.array([0, 255, 256, Bmax - 1])
+    z_ref, A = oracle_float_rows(case["W"], case["h"][rows], "bf16")
+    assert (np.abs(host(lg)[rows].astype(np.float64) - z_ref) <= LOGIT_RTOL * A).all()
+    head.close()
+    h1 = torch.zeros((Bmax + 1, d), dtype=torch.bfloat16, device="cuda")
+    st, *_ = _noalloc(lib, torch, W, V, d, b.DETLM_BF16, h1, Bmax + 1)
+    assert st == b.DETLM_EINVAL
+
+
 def test_noalloc_refuses_oversized_batch_and_int8(env):
     torch, lib, b = env
     V, d = 32000, 64
     W = torch.zeros((V, d), dtype=torch.bfloat16, device="cuda")
-    n_vt = (V + 127) // 128
-    too_big = (8 << 20) // (3 * 4 * n_vt) + 1
+    too_big = _max_rows(V) + 1
     h = torch.zeros((too_big, d), dtype=torch.bfloat16, device="cuda")
     st, *_ = _noalloc(lib, torch, W, V, d, b.DETLM_BF16, h, too_big)
     assert st == b.DETLM_EINVAL
