@@ -110,8 +110,10 @@ int detlm_head_greedy(detlm_head_t* head, const void* h_dev, int64_t B,
  * targets_dev: int32 [B]; logp_dev: float [B]. B == 0 is a no-op. h_dev must
  * be 16-byte aligned; targets_dev and logp_dev 4-byte aligned. The log-sum-
  * exp runs in a fixed order per row (exact maximum and sum of exp(z - max)
- * per 256-entry vocabulary tile, tiles merged in an order set by V alone),
- * so logp_dev[n] is the same bits for any B and any co-rows.
+ * per 256-entry vocabulary tile, tiles merged in an order set by V alone:
+ * 128 leaves of contiguous tiles, each folded in ascending order, combined
+ * in a balanced binary tree), so logp_dev[n] is the same bits for any B and
+ * any co-rows.
  * INT8 heads return DETLM_EUNSUPPORTED. */
 int detlm_head_logprob(detlm_head_t* head, const void* h_dev,
                        const int32_t* targets_dev, int64_t B, float* logp_dev,
@@ -251,6 +253,90 @@ int detlm_head_debug(detlm_head_t* head, int flags, uint64_t timeout_ns);
  * (padded rows of h per MMA) a call with B rows uses. */
 int detlm_head_tiles(const detlm_head_t* head, int64_t B, int32_t* n_vtiles,
                      int32_t* n_cols);
+
+/* ------------------------------------------------------------------------
+ * Vocabulary-parallel heads: W split by rows over P devices (or P heads on
+ * one device), one 16-byte record per hidden row exchanged between them.
+ *
+ * "TandemLLM docs, 12 Exactness", section 12.2: the head's reduction order is
+ * fixed by the weight's shape, never by the row count; here it is also fixed
+ * independently of P. The greedy records merge exactly (value desc, index
+ * asc), and the log-sum-exp tree of detlm_head_logprob (128 leaves of
+ * contiguous 256-entry tiles, folded in ascending order, combined in a
+ * balanced binary tree) is cut on leaf boundaries, so shards + merge give the
+ * single head's token, gap and log-probability bit for bit for P = 1, 2, 4,
+ * ..., 128.
+ *
+ * A caller on P devices: each rank r creates its shard over its own rows
+ * W[v_begin:v_end] (detlm_shard_range), runs the *_shard call on the same
+ * hidden rows, all-gathers the B records of every rank in rank order into
+ * recs [P][B] (a P * B * 16-byte exchange instead of B * V logits), and runs
+ * the merge call (every rank gets the same result).
+ * ------------------------------------------------------------------------ */
+
+/* One hidden row's record from one shard (16 bytes, 16-byte aligned arrays).
+ *   greedy, BF16/FP16 head: m = the shard's best logit, i = the lowest global
+ *     vocabulary index attaining it, s = the runner-up value (s == m on a tie);
+ *   greedy, INT8 head: the same, with m and s int32 (m_i32, s_i32);
+ *   log-prob: m = the shard's largest logit, s = sum over the shard of
+ *     exp(z - m) (the root of the shard's subtree of the log-sum-exp tree),
+ *     i = 1 when the row's target lies in the shard (then zt is its logit),
+ *     else 0. */
+typedef struct {
+  union { float m; int32_t m_i32; };
+  int32_t i;
+  union { float s; int32_t s_i32; };
+  float zt;
+} detlm_shard_rec_t;
+
+/* Rows [*v_begin, *v_end) of a vocabulary of V that shard `rank` of P holds:
+ * with n = ceil(V / 256), the 256-entry tiles [floor(rank n / P),
+ * floor((rank + 1) n / P)) (the last clipped at V). P: a power of two,
+ * 1 <= P <= 128; 0 <= rank < P. A host computation (no GPU needed). A shard
+ * is empty when n < P; such a split is refused by detlm_head_create_shard. */
+int detlm_shard_range(int64_t V, int P, int rank, int64_t* v_begin,
+                      int64_t* v_end);
+
+/* A head over one shard: W_shard_dev [v_end - v_begin, d] holds rows
+ * [v_begin, v_end) of the full W (borrowed, as in detlm_head_create; same
+ * dtype and alignment rules). V is the full vocabulary. The shard head
+ * serves the *_shard calls only (the whole-head calls return
+ * DETLM_EUNSUPPORTED); detlm_head_reserve, detlm_head_check,
+ * detlm_head_time_next, detlm_head_debug and detlm_head_destroy apply. */
+int detlm_head_create_shard(detlm_head_t** out, const void* W_shard_dev,
+                            int64_t V, int64_t d, int dtype, int P, int rank);
+
+/* Greedy records of this shard for B hidden rows h_dev [B, d]:
+ * rec_dev [B] (device, 16-byte aligned). logits_dev (NULL to skip): the
+ * shard's fp32 (int32 for INT8) logits [B, v_end - v_begin], columns in the
+ * shard's own order. */
+int detlm_head_greedy_shard(detlm_head_t* head, const void* h_dev, int64_t B,
+                            detlm_shard_rec_t* rec_dev, void* logits_dev,
+                            cudaStream_t stream);
+
+/* Log-prob records of this shard (BF16/FP16 heads; INT8: DETLM_EUNSUPPORTED).
+ * targets_dev int32 [B]: global vocabulary ids. rec_dev [B]. */
+int detlm_head_logprob_shard(detlm_head_t* head, const void* h_dev,
+                             const int32_t* targets_dev, int64_t B,
+                             detlm_shard_rec_t* rec_dev, cudaStream_t stream);
+
+/* Token and gap from the P shards' greedy records recs_dev [P][B] (shard
+ * r's B records at recs_dev + r * B). dtype: the heads' dtype. token_dev
+ * int32 [B]; gap_dev float [B] in bf16 ulps (INT8: int32 [B], m - s), as
+ * detlm_head_greedy returns them. No handle: the call allocates nothing. */
+int detlm_merge_greedy_shards(const detlm_shard_rec_t* recs_dev, int P,
+                              int64_t B, int dtype, int32_t* token_dev,
+                              void* gap_dev, cudaStream_t stream);
+
+/* Log-probabilities from the P shards' log-prob records recs_dev [P][B]:
+ * logp = zt - (M + log S) with (M, S) the balanced-tree merge of the shards'
+ * (m, s), zt from the shard holding the target. V: the full vocabulary. A
+ * target outside [0, V) gives NaN and, when err_dev is not NULL, sets
+ * DETLM_ETARGET's bit (2) in *err_dev. */
+int detlm_merge_logprob_shards(const detlm_shard_rec_t* recs_dev, int P,
+                               int64_t B, int64_t V, const int32_t* targets_dev,
+                               float* logp_dev, int* err_dev,
+                               cudaStream_t stream);
 
 /* Greedy call that allocates no device memory at all (no counterpart in the
  * source pages; this is a deployment convenience).

@@ -16,6 +16,9 @@ from .binding import (  # noqa: F401
     detlm_status_string, detlm_greedy_noalloc, detlm_head_verify,
     detlm_head_greedy_gated, detlm_head_sample, detlm_quantize_rows,
     detlm_head_greedy_from_float, quantize_rows,
+    detlm_shard_range, detlm_head_create_shard, detlm_head_greedy_shard,
+    detlm_head_logprob_shard, detlm_merge_greedy_shards, detlm_merge_logprob_shards,
+    ShardHead, VocabParallelHead, merge_greedy, merge_logprob, gather_records,
     DETLM_BF16, DETLM_FP16, DETLM_INT8, DETLM_FP32, DETLM_OK, DETLM_EINVAL, DETLM_EUNSUPPORTED,
     DETLM_ECUDA, DETLM_ETIMEOUT, DETLM_ENOMEM, DETLM_ETARGET, DETLM_DEBUG_STALL,
 )

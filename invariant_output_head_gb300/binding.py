@@ -41,6 +41,12 @@ _SIGS = {
     "detlm_head_destroy": (None, [_vp]),
     "detlm_status_string": (ctypes.c_char_p, [_i32]),
     "detlm_greedy_noalloc": (_i32, [_vp, _i64, _i64, _i32, _vp, _i64, _vp, _vp, _vp, _vp, _vp]),
+    "detlm_shard_range": (_i32, [_i64, _i32, _i32, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
+    "detlm_head_create_shard": (_i32, [ctypes.POINTER(_vp), _vp, _i64, _i64, _i32, _i32, _i32]),
+    "detlm_head_greedy_shard": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp]),
+    "detlm_head_logprob_shard": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
+    "detlm_merge_greedy_shards": (_i32, [_vp, _i32, _i64, _i32, _vp, _vp, _vp]),
+    "detlm_merge_logprob_shards": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _vp, _vp]),
 }
 
 _lib = None
@@ -217,6 +223,44 @@ def detlm_greedy_noalloc(W_ptr, V, d, dtype, h_ptr, B, token_ptr, gap_ptr, logit
            "detlm_greedy_noalloc")
 
 
+def detlm_shard_range(V: int, P: int, rank: int):
+    """(v_begin, v_end): the vocabulary rows shard `rank` of P holds (host only)."""
+    a, b = _i64(), _i64()
+    _check(load_library().detlm_shard_range(V, P, rank, ctypes.byref(a), ctypes.byref(b)),
+           "detlm_shard_range")
+    return a.value, b.value
+
+
+def detlm_head_create_shard(W_ptr: int, V: int, d: int, dtype: int, P: int, rank: int) -> int:
+    out = _vp()
+    _check(load_library().detlm_head_create_shard(ctypes.byref(out), W_ptr, V, d, dtype, P, rank),
+           "detlm_head_create_shard")
+    return out.value
+
+
+def detlm_head_greedy_shard(handle, h_ptr, B, rec_ptr, logits_ptr, stream) -> None:
+    _check(load_library().detlm_head_greedy_shard(handle, h_ptr, B, rec_ptr, logits_ptr, stream),
+           "detlm_head_greedy_shard")
+
+
+def detlm_head_logprob_shard(handle, h_ptr, targets_ptr, B, rec_ptr, stream) -> None:
+    _check(load_library().detlm_head_logprob_shard(handle, h_ptr, targets_ptr, B, rec_ptr,
+                                                   stream),
+           "detlm_head_logprob_shard")
+
+
+def detlm_merge_greedy_shards(recs_ptr, P, B, dtype, token_ptr, gap_ptr, stream) -> None:
+    _check(load_library().detlm_merge_greedy_shards(recs_ptr, P, B, dtype, token_ptr, gap_ptr,
+                                                    stream),
+           "detlm_merge_greedy_shards")
+
+
+def detlm_merge_logprob_shards(recs_ptr, P, B, V, targets_ptr, logp_ptr, err_ptr, stream) -> None:
+    _check(load_library().detlm_merge_logprob_shards(recs_ptr, P, B, V, targets_ptr, logp_ptr,
+                                                     err_ptr, stream),
+           "detlm_merge_logprob_shards")
+
+
 # ---- torch convenience wrapper ------------------------------------------
 
 def _stream_ptr(stream) -> int:
@@ -370,3 +414,119 @@ class Head:
 
     def tiles(self, B: int):
         return detlm_head_tiles(self.handle, B)
+
+
+# ---- vocabulary-parallel heads -------------------------------------------
+
+SHARD_REC_INT32S = 4     # one detlm_shard_rec_t = 16 bytes = 4 int32 words
+
+
+class ShardHead(Head):
+    """Shard `rank` of P of a head split by vocabulary rows. W_shard holds the
+    rows detlm_shard_range(V, P, rank) of the full weight (V rows in all)."""
+
+    def __init__(self, W_shard, V: int, P: int, rank: int, dtype: str | None = None):
+        import torch
+        if dtype is None:
+            dtype = {torch.bfloat16: "bf16", torch.float16: "fp16",
+                     torch.int8: "int8"}[W_shard.dtype]
+        if not W_shard.is_cuda or not W_shard.is_contiguous() or W_shard.dim() != 2:
+            raise ValueError("W_shard must be a contiguous 2-D CUDA tensor")
+        v0, v1 = detlm_shard_range(V, P, rank)
+        if int(W_shard.shape[0]) != v1 - v0:
+            raise ValueError(f"shard {rank} of {P} holds rows [{v0}, {v1})")
+        self.W = W_shard
+        self.dtype = dtype
+        self.V, self.d = int(W_shard.shape[0]), int(W_shard.shape[1])
+        self.V_total, self.P, self.rank, self.v_begin, self.v_end = V, P, rank, v0, v1
+        self.handle = detlm_head_create_shard(W_shard.data_ptr(), V, self.d, DTYPES[dtype], P, rank)
+
+    def greedy_records(self, h, with_logits: bool = False, stream=None):
+        """Records int32 [B, 4] (detlm_shard_rec_t) and the shard's logits or None."""
+        import torch
+        self._check_h(h)
+        B = int(h.shape[0])
+        rec = torch.empty((B, SHARD_REC_INT32S), dtype=torch.int32, device=h.device)
+        gdt = torch.int32 if self.dtype == "int8" else torch.float32
+        logits = torch.empty((B, self.V), dtype=gdt, device=h.device) if with_logits else None
+        detlm_head_greedy_shard(self.handle, h.data_ptr(), B, rec.data_ptr(),
+                                logits.data_ptr() if logits is not None else None,
+                                _stream_ptr(stream))
+        return rec, logits
+
+    def logprob_records(self, h, targets, stream=None):
+        import torch
+        self._check_h(h)
+        B = int(h.shape[0])
+        if targets.dtype != torch.int32 or not targets.is_cuda or targets.numel() != B:
+            raise ValueError("targets must be an int32 CUDA tensor [B]")
+        rec = torch.empty((B, SHARD_REC_INT32S), dtype=torch.int32, device=h.device)
+        detlm_head_logprob_shard(self.handle, h.data_ptr(), targets.data_ptr(), B, rec.data_ptr(),
+                                 _stream_ptr(stream))
+        return rec
+
+
+def merge_greedy(recs, dtype: str, stream=None):
+    """recs int32 [P, B, 4] (shard-major) -> (token int32 [B], gap [B])."""
+    import torch
+    if recs.dtype != torch.int32 or recs.dim() != 3 or recs.shape[2] != SHARD_REC_INT32S:
+        raise ValueError("recs must be an int32 tensor [P, B, 4]")
+    recs = recs.contiguous()
+    P, B = int(recs.shape[0]), int(recs.shape[1])
+    token = torch.empty(B, dtype=torch.int32, device=recs.device)
+    gap = torch.empty(B, dtype=torch.int32 if dtype == "int8" else torch.float32,
+                      device=recs.device)
+    detlm_merge_greedy_shards(recs.data_ptr(), P, B, DTYPES[dtype], token.data_ptr(),
+                              gap.data_ptr(), _stream_ptr(stream))
+    return token, gap
+
+
+def merge_logprob(recs, V: int, targets, err=None, stream=None):
+    """recs int32 [P, B, 4] -> logp float32 [B]."""
+    import torch
+    if recs.dtype != torch.int32 or recs.dim() != 3 or recs.shape[2] != SHARD_REC_INT32S:
+        raise ValueError("recs must be an int32 tensor [P, B, 4]")
+    recs = recs.contiguous()
+    P, B = int(recs.shape[0]), int(recs.shape[1])
+    logp = torch.empty(B, dtype=torch.float32, device=recs.device)
+    detlm_merge_logprob_shards(recs.data_ptr(), P, B, V, targets.data_ptr(), logp.data_ptr(),
+                               err.data_ptr() if err is not None else None, _stream_ptr(stream))
+    return logp
+
+
+def gather_records(rec, group=None):
+    """All-gather one rank's records [B, 4] into [P, B, 4] in rank order (the
+    layout the merge calls read). torch.distributed provides the collective
+    (NCCL between GPUs, gloo on CPU tensors)."""
+    import torch
+    import torch.distributed as dist
+    P = dist.get_world_size(group)
+    B = int(rec.shape[0])
+    out = torch.empty((P * B,) + tuple(rec.shape[1:]), dtype=rec.dtype, device=rec.device)
+    dist.all_gather_into_tensor(out, rec.contiguous(), group=group)
+    return out.view((P, B) + tuple(rec.shape[1:]))
+
+
+class VocabParallelHead:
+    """The output head split by vocabulary over the ranks of a process group:
+    rank r holds W rows detlm_shard_range(V, P, r). A call runs this rank's
+    shard, all-gathers one 16-byte record per hidden row and merges them, so
+    every rank returns the single-device head's outputs bit for bit."""
+
+    def __init__(self, W_shard, V: int, group=None, dtype: str | None = None):
+        import torch.distributed as dist
+        self.group = group
+        P, r = dist.get_world_size(group), dist.get_rank(group)
+        self.shard = ShardHead(W_shard, V, P, r, dtype)
+
+    def greedy(self, h, stream=None):
+        rec, _ = self.shard.greedy_records(h, stream=stream)
+        return merge_greedy(gather_records(rec, self.group), self.shard.dtype, stream=stream)
+
+    def logprob(self, h, targets, stream=None):
+        rec = self.shard.logprob_records(h, targets, stream=stream)
+        return merge_logprob(gather_records(rec, self.group), self.shard.V_total, targets,
+                             stream=stream)
+
+    def close(self):
+        self.shard.close()

@@ -20,13 +20,18 @@
 #include "int8_kernels.cuh"
 #include "quant_kernels.cuh"
 #include "rows_kernels.cuh"
+#include "shard_kernels.cuh"
 
 using namespace detlm;
 
 struct detlm_head {
   int device = 0;
   int dtype = 0;
-  int64_t V = 0, d = 0;
+  int64_t V = 0, d = 0;      // V: rows of this head's W
+  // vocabulary shard r of P: this head's rows are [v_off, v_off + V) of a
+  // vocabulary of V_total (P = 1: the whole head)
+  int64_t v_off = 0, V_total = 0;
+  int P = 1, rank = 0;
   const void* W = nullptr;
   CUtensorMap tmW;
   int n_vt = 0, nk = 0, num_sms = 0;
@@ -150,7 +155,7 @@ int status_from_cuda(cudaError_t e) {
 }
 
 // workspace: rec_m, rec_i, rec_s, rec_b [B, n_vt] and zt [B], 256-byte
-// aligned parts
+// aligned parts, laid out for the allocated row count
 size_t ws_part(int64_t n) { return (static_cast<size_t>(n) * 4 + 255) & ~static_cast<size_t>(255); }
 size_t ws_bytes_for(const detlm_head* h, int64_t B) {
   return 4 * ws_part(static_cast<int64_t>(h->n_vt) * B) + ws_part(B);
@@ -174,9 +179,9 @@ int ensure_ws(detlm_head* h, int64_t B, cudaStream_t stream) {
 }
 
 struct WsView { float* m; int32_t* i; float* s; int32_t* b; float* zt; };
-WsView ws_view(const detlm_head* h, int64_t B) {
+WsView ws_view(const detlm_head* h) {
   uint8_t* b = static_cast<uint8_t*>(h->ws);
-  const size_t part = ws_part(static_cast<int64_t>(h->n_vt) * B);
+  const size_t part = ws_part(static_cast<int64_t>(h->n_vt) * h->ws_B);
   WsView w;
   w.m = reinterpret_cast<float*>(b);
   w.i = reinterpret_cast<int32_t*>(b + part);
@@ -319,10 +324,59 @@ cudaError_t launch_rows_kernel(detlm_head* h, const CUtensorMap& tmH, const Head
   return cudaLaunchKernelEx(&cfg, kern, h->tmW, tmH, p);
 }
 
+// 256-entry tiles of a vocabulary of V (the log-sum-exp records' tiles, and
+// the unit of the vocabulary shards)
+int64_t tiles256(int64_t V) { return (V + kRowsN - 1) / kRowsN; }
+
+// Rows [v_begin, v_end) of shard r of P: the 256-entry tiles of the leaves
+// [128 r / P, 128 (r + 1) / P) of the log-sum-exp tree, i.e. tiles
+// [floor(r n / P), floor((r + 1) n / P)) of the n = ceil(V / 256) tiles.
+void shard_rows(int64_t V, int P, int r, int64_t* v_begin, int64_t* v_end) {
+  const int64_t n = tiles256(V);
+  const int64_t t0 = r * n / P, t1 = (r + 1) * n / P;
+  *v_begin = t0 * kRowsN;
+  *v_end = t1 * kRowsN < V ? t1 * kRowsN : V;
+}
+
+// Instead of the merge: one 16-byte record per row for this shard
+// (shard_fold_kernel), launched as a dependent of the projection kernel.
+cudaError_t launch_shard_fold(const detlm_head* h, int mode, int64_t B, int n_vt, const float* rec_m,
+                              const int32_t* rec_i, const float* rec_s, const float* zt,
+                              const int32_t* targets, ShardRec* out, cudaStream_t stream) {
+  ShardFoldParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  fp.B = static_cast<int32_t>(B);
+  fp.n_vt = n_vt;
+  fp.mode = mode;
+  fp.n_tiles = static_cast<int32_t>(tiles256(h->V_total));
+  fp.leaf0 = h->rank * (kLeaves / h->P);
+  fp.n_leaves = kLeaves / h->P;
+  fp.t0 = static_cast<int32_t>(h->v_off / kRowsN);
+  fp.v_begin = static_cast<int32_t>(h->v_off);
+  fp.v_end = static_cast<int32_t>(h->v_off + h->V);
+  fp.rec_m = rec_m;
+  fp.rec_i = rec_i;
+  fp.rec_s = rec_s;
+  fp.zt = zt;
+  fp.targets = targets;
+  fp.out = out;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(B));
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, shard_fold_kernel, fp);
+}
+
 template <int MODE>
 int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* targets,
                  int32_t* token, float* gap, float* logits, float* logp, cudaStream_t stream,
-                 const ModeArgs* gate = nullptr) {
+                 const ModeArgs* gate = nullptr, ShardRec* shard_out = nullptr) {
   // the log-prob call runs on the rows kernel for every B (its records are
   // folded per row, in a fixed order, whatever B is)
   constexpr bool rows = MODE == MODE_LOGPROB;
@@ -333,7 +387,7 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
     return DETLM_EINVAL;
   int st = ensure_ws(h, B, stream);
   if (st != DETLM_OK) return st;
-  const WsView w = ws_view(h, B);
+  const WsView w = ws_view(h);
 
   HeadParams p;
   std::memset(&p, 0, sizeof(p));
@@ -369,6 +423,7 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   p.err = h->d_err;
   p.stall = h->stall;
   p.timeout_ns = h->timeout_ns;
+  p.v_off = static_cast<int32_t>(h->v_off);
   // the mode's own inputs (these members share storage)
   if constexpr (MODE == MODE_LOGPROB) {
     p.targets = targets;
@@ -386,7 +441,6 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
                            : smem_layout(N, p.stages, kExtraSmem).total + 1024;
   const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
   const int grid = static_cast<int>(units < h->num_sms ? units : h->num_sms);
-
   if (h->t_start) cudaEventRecord(h->t_start, stream);
   cudaError_t e;
   if constexpr (rows)
@@ -398,6 +452,9 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
     h->t_start = h->t_stop = nullptr;
   }
   if (e != cudaSuccess) return status_from_cuda(e);
+  if (shard_out != nullptr)
+    return status_from_cuda(launch_shard_fold(h, rows ? SHARD_LOGPROB : SHARD_GREEDY, B, p.n_vt,
+                                              w.m, w.i, w.s, w.zt, targets, shard_out, stream));
 
   MergeParams mp;
   std::memset(&mp, 0, sizeof(mp));
@@ -490,7 +547,7 @@ cudaError_t i8_to_f16(const void* in, void* out, size_t n, cudaStream_t stream) 
 }
 
 int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token, int32_t* gap,
-                     int32_t* logits, cudaStream_t stream) {
+                     int32_t* logits, cudaStream_t stream, ShardRec* shard_out = nullptr) {
   cudaError_t e;
   if (h->W16 == nullptr) {
     const size_t n = static_cast<size_t>(h->V) * h->d;
@@ -524,7 +581,7 @@ int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token
   if (!encode_2d(&tmH, DETLM_FP16, h->h16, h->d, B, static_cast<uint32_t>(N))) return DETLM_EINVAL;
   int st = ensure_ws(h, B, stream);
   if (st != DETLM_OK) return st;
-  const WsView w = ws_view(h, B);
+  const WsView w = ws_view(h);
 
   HeadParams p;
   std::memset(&p, 0, sizeof(p));
@@ -548,6 +605,7 @@ int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token
   p.err = h->d_err;
   p.stall = h->stall;
   p.timeout_ns = h->timeout_ns;
+  p.v_off = static_cast<int32_t>(h->v_off);
   const size_t smem = smem_layout(N, p.stages).total + 1024;
   const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
   const int grid = static_cast<int>(units < h->num_sms ? units : h->num_sms);
@@ -558,6 +616,9 @@ int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token
     h->t_start = h->t_stop = nullptr;
   }
   if (e != cudaSuccess) return status_from_cuda(e);
+  if (shard_out != nullptr)
+    return status_from_cuda(launch_shard_fold(h, SHARD_GREEDY_INT, B, p.n_vt, w.m, w.i, w.s,
+                                              nullptr, nullptr, shard_out, stream));
 
   Int8MergeParams mp;
   mp.B = p.B;
@@ -583,14 +644,14 @@ int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token
 }
 
 int launch_int8(detlm_head* h, const void* h_dev, int64_t B, int32_t* token, int32_t* gap,
-                int32_t* logits, cudaStream_t stream) {
-  if (B >= kI8WideB) return launch_int8_wide(h, h_dev, B, token, gap, logits, stream);
+                int32_t* logits, cudaStream_t stream, ShardRec* shard_out = nullptr) {
+  if (B >= kI8WideB) return launch_int8_wide(h, h_dev, B, token, gap, logits, stream, shard_out);
   const int N = int8_cols_for(B, h->d);
   CUtensorMap tmH;
   if (!encode_2d(&tmH, DETLM_INT8, h_dev, h->d, B, static_cast<uint32_t>(N))) return DETLM_EINVAL;
   int st = ensure_ws(h, B, stream);
   if (st != DETLM_OK) return st;
-  const WsView w = ws_view(h, B);
+  const WsView w = ws_view(h);
 
   Int8Params p;
   std::memset(&p, 0, sizeof(p));
@@ -617,6 +678,7 @@ int launch_int8(detlm_head* h, const void* h_dev, int64_t B, int32_t* token, int
   p.err = h->d_err;
   p.stall = h->stall;
   p.timeout_ns = h->timeout_ns;
+  p.v_off = static_cast<int32_t>(h->v_off);
 
   const size_t smem = int8_layout(N, p.stages).total + 1024;
   const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
@@ -628,6 +690,11 @@ int launch_int8(detlm_head* h, const void* h_dev, int64_t B, int32_t* token, int
     h->t_start = h->t_stop = nullptr;
   }
   if (e != cudaSuccess) return status_from_cuda(e);
+  if (shard_out != nullptr)
+    return status_from_cuda(launch_shard_fold(h, SHARD_GREEDY_INT, B, p.n_vt,
+                                              reinterpret_cast<const float*>(p.rec_m), p.rec_i,
+                                              reinterpret_cast<const float*>(p.rec_s), nullptr,
+                                              nullptr, shard_out, stream));
 
   Int8MergeParams mp;
   mp.B = p.B;
@@ -756,6 +823,7 @@ int detlm_head_create(detlm_head_t** out, const void* W_dev, int64_t V, int64_t 
   h->n_vt = static_cast<int>((V + kBM - 1) / kBM);
   h->nk = static_cast<int>((d * static_cast<int64_t>(elem_bytes(dtype)) + kRowBytes - 1) / kRowBytes);
   h->timeout_ns = kDefaultTimeoutNs;
+  h->V_total = V;
   if (!encode_2d(&h->tmW, dtype, W_dev, d, V, kBM)) {
     delete h;
     return DETLM_EINVAL;
@@ -774,6 +842,121 @@ int detlm_head_create(detlm_head_t** out, const void* W_dev, int64_t V, int64_t 
   return DETLM_OK;
 }
 
+int detlm_shard_range(int64_t V, int P, int rank, int64_t* v_begin, int64_t* v_end) {
+  if (v_begin == nullptr || v_end == nullptr) return DETLM_EINVAL;
+  if (V < 1 || V >= (int64_t{1} << 31)) return DETLM_EINVAL;
+  if (P < 1 || P > kLeaves || (P & (P - 1)) != 0 || rank < 0 || rank >= P) return DETLM_EINVAL;
+  shard_rows(V, P, rank, v_begin, v_end);
+  return DETLM_OK;
+}
+
+int detlm_head_create_shard(detlm_head_t** out, const void* W_shard_dev, int64_t V, int64_t d,
+                            int dtype, int P, int rank) {
+  if (out == nullptr) return DETLM_EINVAL;
+  *out = nullptr;
+  int64_t v0 = 0, v1 = 0;
+  const int st = detlm_shard_range(V, P, rank, &v0, &v1);
+  if (st != DETLM_OK) return st;
+  if (v1 <= v0) return DETLM_EINVAL;             // fewer 256-entry tiles than shards
+  detlm_head_t* h = nullptr;
+  const int c = detlm_head_create(&h, W_shard_dev, v1 - v0, d, dtype);
+  if (c != DETLM_OK) return c;
+  h->v_off = v0;
+  h->V_total = V;
+  h->P = P;
+  h->rank = rank;
+  *out = h;
+  return DETLM_OK;
+}
+
+int detlm_head_greedy_shard(detlm_head_t* h, const void* h_dev, int64_t B,
+                            detlm_shard_rec_t* rec_dev, void* logits_dev, cudaStream_t stream) {
+  if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
+  if (B == 0) return DETLM_OK;
+  if (h_dev == nullptr || !aligned(h_dev, 16)) return DETLM_EINVAL;
+  if (rec_dev == nullptr || !aligned(rec_dev, 16)) return DETLM_EINVAL;
+  if (logits_dev != nullptr && !aligned(logits_dev, 4)) return DETLM_EINVAL;
+  ShardRec* out = reinterpret_cast<ShardRec*>(rec_dev);
+  if (h->dtype == DETLM_INT8)
+    return launch_int8(h, h_dev, B, nullptr, nullptr, static_cast<int32_t*>(logits_dev), stream,
+                       out);
+  return launch_float<MODE_GREEDY>(h, h_dev, B, nullptr, nullptr, nullptr,
+                                   static_cast<float*>(logits_dev), nullptr, stream, nullptr, out);
+}
+
+int detlm_head_logprob_shard(detlm_head_t* h, const void* h_dev, const int32_t* targets_dev,
+                             int64_t B, detlm_shard_rec_t* rec_dev, cudaStream_t stream) {
+  if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
+  if (h->dtype == DETLM_INT8) return DETLM_EUNSUPPORTED;
+  if (B == 0) return DETLM_OK;
+  if (h_dev == nullptr || !aligned(h_dev, 16)) return DETLM_EINVAL;
+  if (targets_dev == nullptr || !aligned(targets_dev, 4)) return DETLM_EINVAL;
+  if (rec_dev == nullptr || !aligned(rec_dev, 16)) return DETLM_EINVAL;
+  return launch_float<MODE_LOGPROB>(h, h_dev, B, targets_dev, nullptr, nullptr, nullptr, nullptr,
+                                    stream, nullptr, reinterpret_cast<ShardRec*>(rec_dev));
+}
+
+namespace {
+cudaError_t launch_shard_merge(const ShardMergeParams& mp, int64_t B, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(B));
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, shard_merge_kernel, mp);
+}
+bool bad_P(int P) { return P < 1 || P > kLeaves || (P & (P - 1)) != 0; }
+}  // namespace
+
+int detlm_merge_greedy_shards(const detlm_shard_rec_t* recs_dev, int P, int64_t B, int dtype,
+                              int32_t* token_dev, void* gap_dev, cudaStream_t stream) {
+  if (bad_P(P) || bad_B(B)) return DETLM_EINVAL;
+  if (dtype != DETLM_BF16 && dtype != DETLM_FP16 && dtype != DETLM_INT8) return DETLM_EINVAL;
+  if (static_cast<int64_t>(P) * B >= (int64_t{1} << 31)) return DETLM_EINVAL;
+  if (B == 0) return DETLM_OK;
+  if (recs_dev == nullptr || !aligned(recs_dev, 16)) return DETLM_EINVAL;
+  if (token_dev == nullptr || !aligned(token_dev, 4)) return DETLM_EINVAL;
+  if (gap_dev == nullptr || !aligned(gap_dev, 4)) return DETLM_EINVAL;
+  ShardMergeParams mp;
+  std::memset(&mp, 0, sizeof(mp));
+  mp.P = P;
+  mp.B = static_cast<int32_t>(B);
+  mp.mode = dtype == DETLM_INT8 ? SHARD_GREEDY_INT : SHARD_GREEDY;
+  mp.recs = reinterpret_cast<const ShardRec*>(recs_dev);
+  mp.token = token_dev;
+  mp.gap = gap_dev;
+  return status_from_cuda(launch_shard_merge(mp, B, stream));
+}
+
+int detlm_merge_logprob_shards(const detlm_shard_rec_t* recs_dev, int P, int64_t B, int64_t V,
+                               const int32_t* targets_dev, float* logp_dev, int* err_dev,
+                               cudaStream_t stream) {
+  if (bad_P(P) || bad_B(B)) return DETLM_EINVAL;
+  if (V < 1 || V >= (int64_t{1} << 31)) return DETLM_EINVAL;
+  if (static_cast<int64_t>(P) * B >= (int64_t{1} << 31)) return DETLM_EINVAL;
+  if (B == 0) return DETLM_OK;
+  if (recs_dev == nullptr || !aligned(recs_dev, 16)) return DETLM_EINVAL;
+  if (targets_dev == nullptr || !aligned(targets_dev, 4)) return DETLM_EINVAL;
+  if (logp_dev == nullptr || !aligned(logp_dev, 4)) return DETLM_EINVAL;
+  if (err_dev != nullptr && !aligned(err_dev, 4)) return DETLM_EINVAL;
+  ShardMergeParams mp;
+  std::memset(&mp, 0, sizeof(mp));
+  mp.P = P;
+  mp.B = static_cast<int32_t>(B);
+  mp.V = static_cast<int32_t>(V);
+  mp.mode = SHARD_LOGPROB;
+  mp.recs = reinterpret_cast<const ShardRec*>(recs_dev);
+  mp.targets = targets_dev;
+  mp.logp = logp_dev;
+  mp.err = err_dev;
+  return status_from_cuda(launch_shard_merge(mp, B, stream));
+}
+
 int detlm_head_reserve(detlm_head_t* h, int64_t max_B) {
   if (h == nullptr || bad_B(max_B)) return DETLM_EINVAL;
   return ensure_ws(h, max_B, nullptr);
@@ -782,6 +965,7 @@ int detlm_head_reserve(detlm_head_t* h, int64_t max_B) {
 int detlm_head_greedy(detlm_head_t* h, const void* h_dev, int64_t B, int32_t* token_dev,
                       void* gap_dev, void* logits_dev, cudaStream_t stream) {
   if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
+  if (h->P > 1) return DETLM_EUNSUPPORTED;   // a vocabulary shard: the *_shard calls
   if (B == 0) return DETLM_OK;
   if (h_dev == nullptr || !aligned(h_dev, 16)) return DETLM_EINVAL;
   if (token_dev == nullptr || !aligned(token_dev, 4)) return DETLM_EINVAL;
@@ -797,6 +981,7 @@ int detlm_head_greedy(detlm_head_t* h, const void* h_dev, int64_t B, int32_t* to
 int detlm_head_logprob(detlm_head_t* h, const void* h_dev, const int32_t* targets_dev, int64_t B,
                        float* logp_dev, cudaStream_t stream) {
   if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
+  if (h->P > 1) return DETLM_EUNSUPPORTED;   // a vocabulary shard: the *_shard calls
   if (h->dtype == DETLM_INT8) return DETLM_EUNSUPPORTED;
   if (B == 0) return DETLM_OK;
   if (h_dev == nullptr || !aligned(h_dev, 16)) return DETLM_EINVAL;
@@ -810,6 +995,7 @@ int detlm_head_greedy_gated(detlm_head_t* h, const void* h_dev, int64_t B, float
                             int32_t* token_dev, float* gap_dev, float* logits_dev,
                             int32_t* base_token_dev, float* margin_dev, cudaStream_t stream) {
   if (h == nullptr || bad_B(B) || std::isnan(tau)) return DETLM_EINVAL;
+  if (h->P > 1) return DETLM_EUNSUPPORTED;   // a vocabulary shard: the *_shard calls
   if (h->dtype == DETLM_INT8) return DETLM_EUNSUPPORTED;
   if (B == 0) return DETLM_OK;
   if (h_dev == nullptr || !aligned(h_dev, 16)) return DETLM_EINVAL;
@@ -830,6 +1016,7 @@ int detlm_head_sample(detlm_head_t* h, const void* h_dev, int64_t B, float tempe
                       const uint64_t* seeds_dev, const uint64_t* positions_dev, int32_t* token_dev,
                       float* score_gap_dev, float* logits_dev, cudaStream_t stream) {
   if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
+  if (h->P > 1) return DETLM_EUNSUPPORTED;   // a vocabulary shard: the *_shard calls
   if (!(temperature > 0.0f) || !std::isfinite(temperature)) return DETLM_EINVAL;
   if (h->dtype == DETLM_INT8) return DETLM_EUNSUPPORTED;
   if (B == 0) return DETLM_OK;
@@ -865,6 +1052,7 @@ int detlm_head_greedy_from_float(detlm_head_t* h, const void* x_dev, int x_dtype
                                  int32_t* token_dev, int32_t* gap_dev, int32_t* logits_dev,
                                  int32_t* mult_dev, int32_t* shift_dev, cudaStream_t stream) {
   if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
+  if (h->P > 1) return DETLM_EUNSUPPORTED;   // a vocabulary shard: the *_shard calls
   if (h->dtype != DETLM_INT8) return DETLM_EUNSUPPORTED;
   if (x_dtype != DETLM_BF16 && x_dtype != DETLM_FP16 && x_dtype != DETLM_FP32) return DETLM_EINVAL;
   if (B == 0) return DETLM_OK;
@@ -905,6 +1093,7 @@ int detlm_head_verify(detlm_head_t* h, const void* h_dev, int64_t n_req, int64_t
                       const int32_t* drafts_dev, int32_t* token_dev, void* gap_dev,
                       void* logits_dev, int32_t* accepted_dev, cudaStream_t stream) {
   if (h == nullptr || n_req < 0 || P < 1) return DETLM_EINVAL;
+  if (h->P > 1) return DETLM_EUNSUPPORTED;   // a vocabulary shard: the *_shard calls
   if (n_req > 0 && P > (INT32_MAX - 1) / n_req) return DETLM_EINVAL;
   if (n_req == 0) return DETLM_OK;
   if (drafts_dev == nullptr || !aligned(drafts_dev, 4)) return DETLM_EINVAL;
@@ -924,6 +1113,7 @@ int detlm_head_verify(detlm_head_t* h, const void* h_dev, int64_t n_req, int64_t
 int detlm_head_greedy_host(detlm_head_t* h, const void* h_host, int64_t B, int32_t* token_host,
                            void* gap_host, void* logits_host, cudaStream_t stream) {
   if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
+  if (h->P > 1) return DETLM_EUNSUPPORTED;   // a vocabulary shard: the *_shard calls
   if (B == 0) return DETLM_OK;
   if (h_host == nullptr || token_host == nullptr || gap_host == nullptr) return DETLM_EINVAL;
   const size_t hb = static_cast<size_t>(B) * h->d * elem_bytes(h->dtype);
@@ -951,6 +1141,7 @@ int detlm_head_greedy_host(detlm_head_t* h, const void* h_host, int64_t B, int32
 int detlm_head_logprob_host(detlm_head_t* h, const void* h_host, const int32_t* targets_host,
                             int64_t B, float* logp_host, cudaStream_t stream) {
   if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
+  if (h->P > 1) return DETLM_EUNSUPPORTED;   // a vocabulary shard: the *_shard calls
   if (h->dtype == DETLM_INT8) return DETLM_EUNSUPPORTED;
   if (B == 0) return DETLM_OK;
   if (h_host == nullptr || targets_host == nullptr || logp_host == nullptr) return DETLM_EINVAL;

@@ -37,10 +37,12 @@
 //
 // Kernel 2 (merge_kernel): one 128-thread block per hidden row folds the
 // n_vt tile records in a fixed order that depends on V only: thread g folds
-// tiles g, g+128, g+256, ... in ascending order, then the 128 partial
-// results combine in a balanced binary tree over g (pairs g^1, g^2, ...,
-// g^64). No atomics take part in any logit, token, gap or log-probability
-// (the speculative-verify fold's atomicMin is order-free).
+// its leaf of the tree -- the greedy records g, g+128, g+256, ... (an exact
+// fold, any order gives the same bits), the log-sum-exp records of the
+// contiguous tiles [g n_vt / 128, (g+1) n_vt / 128) -- in ascending order,
+// then the 128 partial results combine in a balanced binary tree over g
+// (pairs g^1, g^2, ..., g^64). No atomics take part in any logit, token, gap
+// or log-probability (the speculative-verify fold's atomicMin is order-free).
 //
 // Both reductions are written so that a row's bits do not depend on its
 // position in the tile or on B: the greedy record is exact (a function of
@@ -85,7 +87,7 @@ enum : int { ERR_TIMEOUT = 1, ERR_TARGET = 2 };
 // N = 256 log-prob kernel ran 12 % slower on GB300 (same registers and code
 // otherwise). Mode-specific pointers share storage.
 struct HeadParams {
-  int32_t V, d, B;
+  int32_t V, d, B;          // V: vocabulary rows of this head's W
   int32_t N;            // hidden rows per unit (MMA N), multiple of 16, <= kMaxN
   int32_t n_vt, n_nt;   // vocabulary tiles, hidden-row tiles
   int32_t nk;           // K blocks of 128 bytes
@@ -115,6 +117,7 @@ struct HeadParams {
     int32_t round_fp16;       // gated: 1 rounds logits to fp16, 0 to bf16
     float temperature;        // sample: T > 0
   };
+  int32_t v_off;            // vocabulary index of this head's first W row
 };
 static_assert(sizeof(HeadParams) <= 128, "kernel parameter struct above 128 bytes");
 
@@ -486,25 +489,15 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
-    }
-    for (int b = 0; b < p.n_slots; ++b) {
-      mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), EW);
-    }
-    mbar_init(never_bar, 1);
-    mbar_init(drain_bar, static_cast<uint32_t>(NWAY));
-    *abort_flag = 0;
+    // this thread is the TMA producer: W is read-only for the life of the
+    // head, so the W boxes of the first S stages are requested first --
+    // right after their full barriers exist, before the other barriers, the
+    // tensor-memory allocation and the wait for the previous kernels on the
+    // stream; the hidden rows (which a previous kernel may write) only after
+    // that wait
+    for (int s = 0; s < S; ++s) mbar_init(full_bar(s), 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmW);
-    tma_prefetch_desc(&tmH);
-    // this thread is the TMA producer: W is read-only for the life of the
-    // head, so the W boxes of the first S stages are requested now, before
-    // the tensor-memory allocation and before waiting for the previous
-    // kernels on the stream; the hidden rows (which a previous kernel may
-    // write) only after that wait
     const uint64_t pol_w = policy_evict_first();
     const int pre = pre_stages(), spu = (p.nk + KPS - 1) / KPS;
     for (int j = 0; j < pre; ++j) {
@@ -517,6 +510,16 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
         tma_load_2d(sA(j) + b * kBM * kRowBytes, &tmW, (kb0 + b) * kElems, vt * kBM,
                     full_bar(j), pol_w);
     }
+    for (int s = 0; s < S; ++s) mbar_init(empty_bar(s), 1);
+    for (int b = 0; b < p.n_slots; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), EW);
+    }
+    mbar_init(never_bar, 1);
+    mbar_init(drain_bar, static_cast<uint32_t>(NWAY));
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmH);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), p.tmem_cols);
@@ -729,6 +732,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       const int v = vt * kBM + row;
       const bool vok = v < p.V;
       const int n0 = nt * N;
+      const int vg0 = p.v_off + vt * kBM + q * 32;   // vocabulary index of this warp's row 0
       if constexpr (MODE == MODE_SAMPLE) {
         // the unit's column keys, once per unit (ordered before the reads by
         // this barrier, after the previous unit's reads by the one above)
@@ -769,7 +773,8 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
             float x = -INFINITY;
             if (vok && n0 + c < p.B)
               x = sample_score(xp[lane * kXpStride + i], p.temperature, skey[c], skey[N + c],
-                               skey[2 * N + c], skey[3 * N + c], static_cast<uint32_t>(v));
+                               skey[2 * N + c], skey[3 * N + c],
+                               static_cast<uint32_t>(p.v_off + v));
             xp[lane * kXpStride + i] = x;
           }
         } else {
@@ -778,14 +783,14 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
         }
         __syncwarp();
         if constexpr (MODE == MODE_INT) {
-          const ITop2 t = xp_itop2(reinterpret_cast<const int32_t*>(xp), lane, vt * kBM + q * 32);
+          const ITop2 t = xp_itop2(reinterpret_cast<const int32_t*>(xp), lane, vg0);
           if (lane < 16) {
             reinterpret_cast<int32_t*>(red_m)[q * N + c0 + lane] = t.m;
             red_i[q * N + c0 + lane] = t.i;
             reinterpret_cast<int32_t*>(red_s)[q * N + c0 + lane] = t.s;
           }
         } else if constexpr (MODE == MODE_GREEDY || MODE == MODE_SAMPLE) {
-          const Top2 t = xp_top2(xp, lane, vt * kBM + q * 32);
+          const Top2 t = xp_top2(xp, lane, vg0);
           if (lane < 16) {
             red_m[q * N + c0 + lane] = t.m;
             red_i[q * N + c0 + lane] = t.i;
@@ -794,7 +799,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
         } else {
           static_assert(MODE == MODE_GATED, "the log-prob call runs on head_rows_kernel");
           int32_t i16;
-          const Top2 t = xp_gated(xp, lane, vt * kBM + q * 32, p.round_fp16 != 0, i16);
+          const Top2 t = xp_gated(xp, lane, vg0, p.round_fp16 != 0, i16);
           if (lane < 16) {
             red_m[q * N + c0 + lane] = t.m;
             red_i[q * N + c0 + lane] = t.i;
@@ -884,6 +889,34 @@ __device__ __forceinline__ T block_tree128(T x, M merge_fn, T* smem4) {
 constexpr int kMergeThreads = 128;
 constexpr int kMergeBatch = 8;     // records loaded per thread before folding
 
+// The log-sum-exp tree over a row's tile records: 128 leaves, leaf g holding
+// the tiles [leaf_lo(g, n), leaf_lo(g + 1, n)) of the n tiles, folded in
+// ascending order; the leaves combine in a balanced binary tree (block_tree128).
+// The shape is a function of n alone. A run of whole leaves is a run of whole
+// tiles, so a head cut into P = 2, 4, ..., 128 vocabulary shards on leaf
+// boundaries (shard r: leaves [128 r / P, 128 (r + 1) / P)) computes subtrees
+// of this very tree, and combining the shards' roots in a balanced tree gives
+// the same bits (shard_kernels.cuh).
+constexpr int kLeaves = kMergeThreads;
+__host__ __device__ inline int leaf_lo(int g, int n) {
+  return static_cast<int>((static_cast<int64_t>(g) * n) / kLeaves);
+}
+
+// Fold of tiles [t0, t1) of one row's (m, S) records, in ascending order,
+// starting from the identity (a no-op of lse_merge, bit for bit).
+__device__ __forceinline__ Lse lse_fold_range(const float* rm, const float* rs, int t0, int t1) {
+  Lse acc{-INFINITY, 0.0f};
+  for (int t = t0; t < t1; t += kMergeBatch) {
+    Lse r[kMergeBatch];
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j)
+      r[j] = t + j < t1 ? Lse{rm[t + j], rs[t + j]} : Lse{-INFINITY, 0.0f};
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) acc = lse_merge(acc, r[j]);
+  }
+  return acc;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
   grid_dep_launch(); // the next call's kernel 1 may start (it prefetches only W)
@@ -954,17 +987,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     }
   } else {
     __shared__ Lse part[4];
-    Lse acc{-INFINITY, 0.0f};
-    for (int t0 = g; t0 < p.n_vt; t0 += kMergeThreads * kMergeBatch) {
-      Lse r[kMergeBatch];
-#pragma unroll
-      for (int j = 0; j < kMergeBatch; ++j) {
-        const int t = t0 + j * kMergeThreads;
-        r[j] = t < p.n_vt ? Lse{p.rec_m[base + t], p.rec_s[base + t]} : Lse{-INFINITY, 0.0f};
-      }
-#pragma unroll
-      for (int j = 0; j < kMergeBatch; ++j) acc = lse_merge(acc, r[j]);
-    }
+    const Lse acc = lse_fold_range(p.rec_m + base, p.rec_s + base, leaf_lo(g, p.n_vt),
+                                   leaf_lo(g + 1, p.n_vt));
     const Lse tot = block_tree128(acc, lse_merge, part);
     if (g == 0) {
       const int tg = p.targets[n];

@@ -67,7 +67,7 @@ __host__ __device__ inline int int8_cols_for(int64_t B, int64_t /*d*/) {
 }
 
 struct Int8Params {
-  int32_t V, d, B;
+  int32_t V, d, B;           // V: vocabulary rows of this head's W
   int32_t N, n_vt, n_nt, nk, n_chunks;
   int32_t stages;            // int8 ring depth
   uint32_t idesc;
@@ -78,6 +78,7 @@ struct Int8Params {
   int* err;
   int32_t stall;
   uint64_t timeout_ns;
+  int32_t v_off;             // vocabulary index of this head's first W row
 };
 static_assert(sizeof(Int8Params) <= 128, "kernel parameter struct above 128 bytes");
 
@@ -238,8 +239,24 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   };
 
   if (threadIdx.x == 0) {
+    // this thread is the TMA producer: W is read-only for the head's life,
+    // so the W boxes of the first S stages are requested first -- right
+    // after their full barriers exist, before the other barriers, the
+    // tensor-memory allocation and the wait for the previous kernels on the
+    // stream; the hidden rows (which a previous kernel may write) only after
+    // that wait
+    for (int s = 0; s < S; ++s) mbar_init(full(s), 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmW);
+    const uint64_t pol_w = policy_evict_first();
+    const int pre = pre_stages();
+    for (int j = 0; j < pre; ++j) {
+      const int u = blockIdx.x + (j / p.nk) * gridDim.x;
+      const int vt = u / p.n_nt, kb = j - (j / p.nk) * p.nk;
+      mbar_expect_tx(full(j), L.tx);
+      tma_load_2d(base + j * L.stage, &tmW, kb * kRowBytes, vt * kBM, full(j), pol_w);
+    }
     for (int s = 0; s < S; ++s) {
-      mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
       mbar_init(conv(s), kI8ConvWarps);
     }
@@ -249,21 +266,7 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     mbar_init(drain_bar, 2);
     *abort_flag = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmH);
-    // this thread is the TMA producer: W is read-only for the head's life,
-    // so the W boxes of the first S stages are requested now, before the
-    // tensor-memory allocation and before waiting for the previous kernels
-    // on the stream; the hidden rows (which a previous kernel may write)
-    // only after that wait
-    const uint64_t pol_w = policy_evict_first();
-    const int pre = pre_stages();
-    for (int j = 0; j < pre; ++j) {
-      const int u = blockIdx.x + (j / p.nk) * gridDim.x;
-      const int vt = u / p.n_nt, kb = j - (j / p.nk) * p.nk;
-      mbar_expect_tx(full(j), L.tx);
-      tma_load_2d(base + j * L.stage, &tmW, kb * kRowBytes, vt * kBM, full(j), pol_w);
-    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), 512u);
@@ -475,7 +478,7 @@ int8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
 #pragma unroll
         for (int i = 0; i < 16; ++i) xp[lane * kXpStride + i] = vok ? acc[bb][i] : INT32_MIN;
         __syncwarp();
-        const ITop2 t = xp_itop2(xp, lane, vt * kBM + q * 32);
+        const ITop2 t = xp_itop2(xp, lane, p.v_off + vt * kBM + q * 32);
         if (lane < 16) {
           red_m[q * N + c0 + lane] = t.m;
           red_i[q * N + c0 + lane] = t.i;

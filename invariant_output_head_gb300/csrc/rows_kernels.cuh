@@ -301,8 +301,9 @@ head_rows_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
       if (row_ok) {
         // the target's logit, if it lies in this half: a select chain over
         // the 16-entry blocks, then over the block (no register is indexed
-        // at run time)
-        const int tl = p.targets[n] - vb;
+        // at run time); targets are vocabulary indices of the whole head,
+        // this head's rows start at v_off
+        const int tl = p.targets[n] - p.v_off - vb;
         if (tl >= 0 && tl < 128) {
           const int tb = tl >> 4, ti = tl & 15;
           float sel[16];
