@@ -230,6 +230,51 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": n}
 
 
+def instruction_peaks(dev, n_sms: int) -> dict:
+    """What the integer head's wide path is measured against beside the bf16
+    peak: the dense rate of the instruction it runs on (tcgen05 kind::f16,
+    fp16 operands, M = 128, N = 256; the library's probe kernel, one CTA per
+    SM, no loads), and torch._int_mm on 8192^3 int8 as the library
+    reference for an int8 x int8 -> int32 product."""
+    import ctypes
+    import torch
+    out = {}
+    lib_path = os.path.join(ROOT, "invariant_output_head_gb300", "_lib", "libdetlm_peak.so")
+    try:
+        lib = ctypes.CDLL(lib_path)
+        lib.detlm_mma_f16_peak.restype = ctypes.c_int
+        lib.detlm_mma_f16_peak.argtypes = [ctypes.c_int, ctypes.c_int,
+                                           ctypes.POINTER(ctypes.c_double)]
+        vals = []
+        for _ in range(3):
+            tf = ctypes.c_double()
+            if lib.detlm_mma_f16_peak(n_sms, 40000, ctypes.byref(tf)) == 0:
+                vals.append(tf.value)
+        out["mma_f16_dense_tflops"] = round(max(vals), 1) if vals else None
+    except OSError as e:
+        out["mma_f16_dense_tflops"] = None
+        out["mma_f16_note"] = f"probe library not loaded: {e}"
+    try:
+        n = 8192
+        a = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=dev)
+        b = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=dev)
+        torch._int_mm(a, b)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(10):
+            torch._int_mm(a, b)
+        e1.record()
+        torch.cuda.synchronize()
+        sec = e0.elapsed_time(e1) / 1e3 / 10
+        out["torch_int_mm_8192_tops"] = round(2.0 * n ** 3 / sec / 1e12, 1)
+        del a, b
+    except Exception as e:   # noqa: BLE001 - a reference figure, reported either way
+        out["torch_int_mm_8192_tops"] = None
+        out["torch_int_mm_note"] = f"{type(e).__name__}: {str(e)[:160]}"
+    return out
+
+
 def max_over_ranks(x: float, world: int) -> float:
     """Max of a host scalar over all ranks (NCCL on GPUs, gloo on CPUs)."""
     if world <= 1:
@@ -577,6 +622,11 @@ def run_ours(args, rank, world, local_rank):
     }
     if by_B is not None:
         res["roofline"]["per_B"] = by_B
+    if fmt == "int8" and spec["bound"] == "tensor" and rank == 0:
+        ip = instruction_peaks(dev, torch.cuda.get_device_properties(dev).multi_processor_count)
+        if ip.get("mma_f16_dense_tflops"):
+            ip["frac_of_mma_f16_dense"] = round(achieved / ip["mma_f16_dense_tflops"], 4)
+        res["roofline"]["instruction_peaks"] = ip
     if rank == 0 and not args.profile:
         res["e2e"] = run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream)
         res["cpu_baseline"] = cpu_baseline(args.workload, c, budget_s=args.cpu_seconds,
@@ -599,10 +649,13 @@ def gpu_row_decisions(snap, calls, mode):
 
 def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
     """Same metric end to end: pinned host inputs are copied in and the
-    results copied out on every call. The greedy and log-prob calls go
-    through their host-buffer entry points; the gated and verify calls, which
-    have none, through their device entry points between explicit copies on
-    the same stream."""
+    results copied out on every call, and every step ends when its results
+    are in host memory. The greedy and log-prob calls go through their
+    asynchronous host-buffer entry points (one pinned result buffer set per
+    call; the step ends with detlm_head_check on each head it used); the
+    other calls, which have no host-buffer form, through their device entry
+    points between explicit copies on the same stream, the step ending with a
+    stream synchronization."""
     import torch
     from invariant_output_head_gb300 import binding as bd
     fmt, V = c["dtype"], c["V"]
@@ -616,6 +669,16 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
     gap = torch.empty(maxB, dtype=torch.int32).pin_memory()
     lg = torch.empty((maxB, V), dtype=torch.int32).pin_memory() if greedy else None
     lp = torch.empty(maxB, dtype=torch.float32).pin_memory()
+    # the asynchronous calls: a result buffer set of their own per call
+    res_bufs = []
+    if mode in ("greedy", "logprob"):
+        for _, B in calls:
+            if mode == "greedy":
+                res_bufs.append((torch.empty(B, dtype=torch.int32).pin_memory(),
+                                 torch.empty(B, dtype=torch.int32).pin_memory(),
+                                 torch.empty((B, V), dtype=torch.int32).pin_memory()))
+            else:
+                res_bufs.append((torch.empty(B, dtype=torch.float32).pin_memory(),))
     tg = torch.from_numpy(c["targets"]).pin_memory() if not greedy else None
     extra = torch.empty(2 * maxB, dtype=torch.int32).pin_memory()   # base+margin / accepted
     sp = stream.cuda_stream
@@ -640,15 +703,18 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
             sd_dev = torch.empty((2, sd_host.shape[1]), dtype=torch.int64, device=dev)
 
     def one_step(i):
+        used = {}
         for j, (r0, B) in enumerate(calls):
             hd = heads[(i * len(calls) + j) % len(heads)]
+            used[id(hd)] = hd
             hp = h_host.data_ptr() + r0 * d * esz
             if mode == "greedy":
-                bd.detlm_head_greedy_host(hd.handle, hp, B, tok.data_ptr(), gap.data_ptr(),
-                                          lg.data_ptr(), sp)
+                rt, rg, rl = res_bufs[j]
+                bd.detlm_head_greedy_host_async(hd.handle, hp, B, rt.data_ptr(), rg.data_ptr(),
+                                                rl.data_ptr(), sp)
             elif mode == "logprob":
-                bd.detlm_head_logprob_host(hd.handle, hp, tg.data_ptr() + r0 * 4, B,
-                                           lp.data_ptr(), sp)
+                bd.detlm_head_logprob_host_async(hd.handle, hp, tg.data_ptr() + r0 * 4, B,
+                                                 res_bufs[j][0].data_ptr(), sp)
             elif mode == "int8f":
                 with torch.cuda.stream(stream):
                     x_dev[:B].copy_(x_host[r0:r0 + B], non_blocking=True)
@@ -686,6 +752,12 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
                     lg[:B].view(torch.float32).copy_(o_dev[2][:B], non_blocking=True)
                     if n_extra:
                         extra[:n_extra].copy_(o_dev[3][:n_extra], non_blocking=True)
+        # the step's results are in host memory when the step ends
+        if mode in ("greedy", "logprob"):
+            for hd in used.values():
+                assert hd.check() == 0
+        else:
+            stream.synchronize()
     for i in range(3):
         one_step(i)
     torch.cuda.synchronize()
@@ -701,7 +773,8 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
     d2h = sum(4 * B if mode == "logprob" else 8 * B + 4 * B * V for _, B in calls)
     d2h += sum(8 * B if mode == "gated" else (4 * (B // 16) if mode == "verify" else 0)
                for _, B in calls)
-    api = {"greedy": "detlm_head_greedy_host", "logprob": "detlm_head_logprob_host",
+    api = {"greedy": "detlm_head_greedy_host_async (+ detlm_head_check per step)",
+           "logprob": "detlm_head_logprob_host_async (+ detlm_head_check per step)",
            "gated": "detlm_head_greedy_gated + pinned copies on the call's stream",
            "verify": "detlm_head_verify + pinned copies on the call's stream",
            "sample": "detlm_head_sample + pinned copies on the call's stream",

@@ -77,7 +77,10 @@ int detlm_head_create(detlm_head_t** out, const void* W_dev, int64_t V,
 
 /* Grow the workspace so that calls with up to max_B rows allocate nothing.
  * Optional: calls grow it on demand (a synchronous allocation). Call it
- * before capturing calls into a CUDA graph. */
+ * before capturing calls into a CUDA graph. For an INT8 head, max_B >= 256
+ * also makes what its calls of 256 rows or more run on: an fp16 copy of W
+ * (2 * V * d bytes, converted once, exactly, and kept until destroy) and an
+ * fp16 staging buffer for max_B hidden rows (2 * max_B * d bytes). */
 int detlm_head_reserve(detlm_head_t* head, int64_t max_B);
 
 /* Greedy decision for B hidden rows h_dev [B, d].
@@ -231,9 +234,32 @@ int detlm_head_logprob_host(detlm_head_t* head, const void* h_host,
                             const int32_t* targets_host, int64_t B,
                             float* logp_host, cudaStream_t stream);
 
-/* Wait for the stream, read and clear the handle's device error word.
- * DETLM_ETIMEOUT if a kernel's bounded wait ran out (its outputs are then
- * undefined), else DETLM_ETARGET if a target id was out of range, else OK. */
+/* Asynchronous forms of the two host-buffer calls, for a caller that issues
+ * many calls and reads the results once: they enqueue the copy of h (and
+ * targets) to the device, the call, and the copies of the results back to
+ * the given host buffers, and return without waiting. Results are in the
+ * host buffers after detlm_head_check returns; until then the caller keeps
+ * every buffer of every pending call alive and unchanged. The kernels run on
+ * `stream`. Result buffers the device can address (pinned host memory from
+ * cudaHostAlloc or cudaHostRegister, which is mapped on unified-addressing
+ * systems) are written by the kernels directly; otherwise the results go to
+ * two alternating device slots and are copied back on a stream of the
+ * handle's own, so one call's copy overlaps the next call's kernels. Copies
+ * from or to pageable memory make the call wait for them. Device staging is
+ * owned by the handle and grows on demand (growth waits for the pending
+ * calls). */
+int detlm_head_greedy_host_async(detlm_head_t* head, const void* h_host,
+                                 int64_t B, int32_t* token_host, void* gap_host,
+                                 void* logits_host, cudaStream_t stream);
+int detlm_head_logprob_host_async(detlm_head_t* head, const void* h_host,
+                                  const int32_t* targets_host, int64_t B,
+                                  float* logp_host, cudaStream_t stream);
+
+/* Wait for the stream and for the copies of the handle's pending
+ * asynchronous host-buffer calls, read and clear the handle's device error
+ * word. DETLM_ETIMEOUT if a kernel's bounded wait ran out (its outputs are
+ * then undefined), else DETLM_ETARGET if a target id was out of range, else
+ * OK. */
 int detlm_head_check(detlm_head_t* head, cudaStream_t stream);
 
 /* Record start/stop around the projection kernel of the NEXT call only (one

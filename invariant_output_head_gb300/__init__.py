@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     Head, DetlmError, load_library, library_path, status_string,
     detlm_head_create, detlm_head_reserve, detlm_head_greedy, detlm_head_logprob,
     detlm_head_greedy_host, detlm_head_logprob_host, detlm_head_check,
+    detlm_head_greedy_host_async, detlm_head_logprob_host_async,
     detlm_head_time_next, detlm_head_debug, detlm_head_tiles, detlm_head_destroy,
     detlm_status_string, detlm_greedy_noalloc, detlm_head_verify,
     detlm_head_greedy_gated, detlm_head_sample, detlm_quantize_rows,

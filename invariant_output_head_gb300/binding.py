@@ -33,6 +33,8 @@ _SIGS = {
     "detlm_head_greedy_from_float": (_i32, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     "detlm_head_greedy_host": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp]),
     "detlm_head_logprob_host": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
+    "detlm_head_greedy_host_async": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _vp]),
+    "detlm_head_logprob_host_async": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
     "detlm_head_check": (_i32, [_vp, _vp]),
     "detlm_head_time_next": (_i32, [_vp, _vp, _vp]),
     "detlm_head_debug": (_i32, [_vp, _i32, _u64]),
@@ -183,6 +185,19 @@ def detlm_head_logprob_host(handle, h_ptr, targets_ptr, B, logp_ptr, stream) -> 
     _check(load_library().detlm_head_logprob_host(handle, h_ptr, targets_ptr, B,
                                                   logp_ptr, stream),
            "detlm_head_logprob_host")
+
+
+def detlm_head_greedy_host_async(handle, h_ptr, B, token_ptr, gap_ptr, logits_ptr,
+                                 stream) -> None:
+    _check(load_library().detlm_head_greedy_host_async(handle, h_ptr, B, token_ptr, gap_ptr,
+                                                       logits_ptr, stream),
+           "detlm_head_greedy_host_async")
+
+
+def detlm_head_logprob_host_async(handle, h_ptr, targets_ptr, B, logp_ptr, stream) -> None:
+    _check(load_library().detlm_head_logprob_host_async(handle, h_ptr, targets_ptr, B,
+                                                        logp_ptr, stream),
+           "detlm_head_logprob_host_async")
 
 
 def detlm_head_check(handle, stream) -> int:

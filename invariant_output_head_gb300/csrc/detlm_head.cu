@@ -13,6 +13,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "detlm_head.h"
@@ -38,12 +39,27 @@ struct detlm_head {
   int rows_pairs = 0;        // CTA pairs of the rows kernel that fit at once (0: not asked yet)
   int* d_err = nullptr;
   int* err_host = nullptr;   // pinned word the error word is read into
+  // where the GPU has native atomics on host memory (Grace with NVLink-C2C),
+  // the error word itself is a mapped pinned host word: d_err is its device
+  // address and the check reads it without a copy
+  int* err_mapped = nullptr;
   // split-V record workspace
   void* ws = nullptr;
   int64_t ws_B = 0;
   // device staging for the *_host calls
   void* stage = nullptr;
   size_t stage_bytes = 0;
+  // the *_host_async calls: the hidden rows staged on the call's stream, the
+  // outputs in two alternating slots copied to the host on the handle's own
+  // copy stream (so a call's device-to-host copy overlaps the next call's
+  // kernels); done[k]: slot k's kernels finished, freed[k]: its copy did
+  void* a_in = nullptr;
+  size_t a_in_bytes = 0;
+  void* a_out[2] = {nullptr, nullptr};
+  size_t a_out_bytes = 0;
+  int a_next = 0;
+  cudaStream_t a_copy = nullptr;
+  cudaEvent_t a_done[2] = {nullptr, nullptr}, a_freed[2] = {nullptr, nullptr};
   // integer head, wide batches: fp16 copy of W (made at the first such call)
   // and the call's hidden rows in fp16
   void* W16 = nullptr;
@@ -217,21 +233,40 @@ int ensure_vws(detlm_head* h, int64_t R, cudaStream_t stream) {
   return DETLM_OK;
 }
 
+// One-time set-up of a kernel on the current device: its opt-in dynamic
+// shared memory (the most any launch asks for) and, where want_regs > 0, a
+// check of the register count its register split assumes. Later launches on
+// the device skip these runtime calls (a bit per device; up to 64 devices,
+// beyond that the set-up runs on every launch).
+template <auto KERN>
+cudaError_t prepare_kernel(int want_regs) {
+  static std::atomic<uint64_t> ready{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 64;
+  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (bit != 0 && (ready.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  if (want_regs > 0) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, KERN);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != want_regs) return cudaErrorInvalidConfiguration;
+  }
+  cudaError_t e = cudaFuncSetAttribute(KERN, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemLimit);
+  if (e != cudaSuccess) return e;
+  ready.fetch_or(bit, std::memory_order_release);
+  return cudaSuccess;
+}
+
 // Launch kernel 1 for N = 16 * nblk as a programmatic dependent of the
 // previous kernel on the stream (its prologue overlaps that kernel's tail).
 template <int MODE, int NBLK>
 cudaError_t launch_gemm_n(const CUtensorMap& tmW, const CUtensorMap& tmH, const HeadParams& p,
                           int grid, size_t smem, cudaStream_t stream) {
   auto kern = head_gemm_kernel<MODE, NBLK>;
-  if constexpr (threads_for(16 * NBLK) == 384) {
-    // the kernel's register split assumes exactly this launch budget
-    cudaFuncAttributes fa;
-    cudaError_t e0 = cudaFuncGetAttributes(&fa, kern);
-    if (e0 != cudaSuccess) return e0;
-    if (fa.numRegs != kRegsLaunchWide) return cudaErrorInvalidConfiguration;
-  }
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  // the wide kernel's register split assumes exactly its launch budget
+  cudaError_t e = prepare_kernel<head_gemm_kernel<MODE, NBLK>>(
+      threads_for(16 * NBLK) == 384 ? kRegsLaunchWide : 0);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
@@ -290,11 +325,7 @@ int rows_stages() {
 cudaError_t launch_rows_kernel(detlm_head* h, const CUtensorMap& tmH, const HeadParams& p,
                                int64_t units, size_t smem, cudaStream_t stream) {
   auto kern = head_rows_kernel;
-  cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs != kRegsLaunchWide) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = prepare_kernel<head_rows_kernel>(kRegsLaunchWide);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
@@ -499,9 +530,7 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
 template <int N>
 cudaError_t launch_int8_t(const CUtensorMap& tmW, const CUtensorMap& tmH, const Int8Params& p,
                           int grid, size_t smem, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(int8_gemm_kernel<N>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = prepare_kernel<int8_gemm_kernel<N>>(0);
   if (e != cudaSuccess) return e;
   // a programmatic dependent of the previous kernel on the stream (its
   // prologue and W prefetch overlap that kernel's tail)
@@ -546,8 +575,10 @@ cudaError_t i8_to_f16(const void* in, void* out, size_t n, cudaStream_t stream) 
   return cudaGetLastError();
 }
 
-int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token, int32_t* gap,
-                     int32_t* logits, cudaStream_t stream, ShardRec* shard_out = nullptr) {
+// The wide integer path's buffers: the fp16 copy of W (2 V d bytes, made
+// once and kept until destroy) and the fp16 staging of B hidden rows. Made by
+// detlm_head_reserve when max_B >= kI8WideB, else by the first such call.
+int ensure_wide(detlm_head* h, int64_t B, cudaStream_t stream) {
   cudaError_t e;
   if (h->W16 == nullptr) {
     const size_t n = static_cast<size_t>(h->V) * h->d;
@@ -574,6 +605,14 @@ int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token
     if (e != cudaSuccess) return status_from_cuda(e);
     h->h16_bytes = hb;
   }
+  return DETLM_OK;
+}
+
+int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token, int32_t* gap,
+                     int32_t* logits, cudaStream_t stream, ShardRec* shard_out = nullptr) {
+  cudaError_t e;
+  const int sw = ensure_wide(h, B, stream);
+  if (sw != DETLM_OK) return sw;
   e = i8_to_f16(h_dev, h->h16, static_cast<size_t>(B) * h->d, stream);
   if (e != cudaSuccess) return status_from_cuda(e);
   const int N = cols_for(B);
@@ -720,6 +759,18 @@ int launch_int8(detlm_head* h, const void* h_dev, int64_t B, int32_t* token, int
 }
 
 int read_err(detlm_head* h, cudaStream_t stream) {
+  if (h->err_mapped != nullptr) {
+    // the word lives in host memory: once the stream is idle no kernel of
+    // this handle can write it, and the next ones see the host's clear
+    const cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return status_from_cuda(e);
+    volatile int* w = h->err_mapped;
+    const int hv = *w;
+    if (hv != 0) *w = 0;
+    if (hv & ERR_TIMEOUT) return DETLM_ETIMEOUT;
+    if (hv & ERR_TARGET) return DETLM_ETARGET;
+    return DETLM_OK;
+  }
   // into a pinned word: a copy to pageable memory costs an extra staging step
   cudaError_t e = cudaMemcpyAsync(h->err_host, h->d_err, sizeof(int), cudaMemcpyDeviceToHost, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
@@ -751,6 +802,97 @@ int ensure_stage(detlm_head* h, size_t bytes, cudaStream_t stream) {
 }
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Copy n16 16-byte words of hidden rows from a buffer the device can read
+// (pinned host memory) into the handle's staging, as a programmatic
+// dependent of the previous call's merge: it waits for that kernel (and so
+// for the previous projection, the last reader of the staging) before
+// writing, and the next projection, launched as its dependent, requests its
+// first W boxes while this copy runs.
+__global__ void __launch_bounds__(256) stage_rows_kernel(const uint4* __restrict__ src,
+                                                         uint4* __restrict__ dst, size_t n16) {
+  grid_dep_wait();
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    dst[i] = src[i];
+  __syncthreads();
+  grid_dep_launch();
+}
+
+cudaError_t launch_stage_rows(const void* src_dev, void* dst, size_t bytes, cudaStream_t stream) {
+  const size_t n16 = bytes / 16;
+  size_t blocks = (n16 + 255) / 256;
+  if (blocks > 1024) blocks = 1024;
+  if (blocks == 0) blocks = 1;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, stage_rows_kernel, static_cast<const uint4*>(src_dev),
+                            static_cast<uint4*>(dst), n16);
+}
+
+// The device address of a caller's buffer if kernels can write it directly
+// (device or managed memory, or pinned host memory mapped into the device's
+// address space, as cudaHostAlloc and cudaHostRegister give it), else null.
+void* device_address(void* p) {
+  if (p == nullptr) return nullptr;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();   // not a CUDA-known pointer: clear the sticky-free error
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return p;
+  if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr) return a.devicePointer;
+  return nullptr;
+}
+
+// Staging of the asynchronous host-buffer calls: the copy stream and its
+// events on first use; the buffers grown to hold in_bytes of rows and
+// out_bytes of outputs per slot (growth waits for every pending call).
+int ensure_async(detlm_head* h, size_t in_bytes, size_t out_bytes, cudaStream_t stream) {
+  cudaError_t e = cudaSuccess;
+  if (h->a_copy == nullptr) {
+    e = cudaStreamCreateWithFlags(&h->a_copy, cudaStreamNonBlocking);
+    for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+      e = cudaEventCreateWithFlags(&h->a_done[k], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->a_freed[k], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return status_from_cuda(e);
+  }
+  if (in_bytes > h->a_in_bytes || out_bytes > h->a_out_bytes) {
+    e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->a_copy);
+    if (e != cudaSuccess) return status_from_cuda(e);
+  }
+  if (in_bytes > h->a_in_bytes) {
+    if (h->a_in) cudaFree(h->a_in);
+    h->a_in = nullptr;
+    h->a_in_bytes = 0;
+    e = cudaMalloc(&h->a_in, in_bytes);
+    if (e != cudaSuccess) return status_from_cuda(e);
+    h->a_in_bytes = in_bytes;
+  }
+  if (out_bytes > h->a_out_bytes) {
+    for (int k = 0; k < 2; ++k) {
+      if (h->a_out[k]) cudaFree(h->a_out[k]);
+      h->a_out[k] = nullptr;
+    }
+    h->a_out_bytes = 0;
+    for (int k = 0; k < 2; ++k) {
+      e = cudaMalloc(&h->a_out[k], out_bytes);
+      if (e != cudaSuccess) return status_from_cuda(e);
+    }
+    h->a_out_bytes = out_bytes;
+  }
+  return DETLM_OK;
+}
 
 bool bad_B(int64_t B) { return B < 0 || B >= (int64_t{1} << 31); }
 
@@ -828,12 +970,23 @@ int detlm_head_create(detlm_head_t** out, const void* W_dev, int64_t V, int64_t 
     delete h;
     return DETLM_EINVAL;
   }
-  e = cudaMalloc(&h->d_err, sizeof(int));
-  if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
+  int host_atomics = 0;
+  cudaDeviceGetAttribute(&host_atomics, cudaDevAttrHostNativeAtomicSupported, dev);
+  if (host_atomics) {
+    e = cudaHostAlloc(reinterpret_cast<void**>(&h->err_mapped), sizeof(int), cudaHostAllocMapped);
+    if (e == cudaSuccess) {
+      *h->err_mapped = 0;
+      e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->d_err), h->err_mapped, 0);
+    }
+  } else {
+    e = cudaMalloc(&h->d_err, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
+  }
   if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&h->err_host), sizeof(int),
                                           cudaHostAllocDefault);
   if (e != cudaSuccess) {
-    if (h->d_err) cudaFree(h->d_err);
+    if (h->err_mapped) cudaFreeHost(h->err_mapped);
+    else if (h->d_err) cudaFree(h->d_err);
     if (h->err_host) cudaFreeHost(h->err_host);
     delete h;
     return status_from_cuda(e);
@@ -959,7 +1112,12 @@ int detlm_merge_logprob_shards(const detlm_shard_rec_t* recs_dev, int P, int64_t
 
 int detlm_head_reserve(detlm_head_t* h, int64_t max_B) {
   if (h == nullptr || bad_B(max_B)) return DETLM_EINVAL;
-  return ensure_ws(h, max_B, nullptr);
+  int st = ensure_ws(h, max_B, nullptr);
+  if (st == DETLM_OK && h->dtype == DETLM_INT8 && max_B >= kI8WideB) {
+    st = ensure_wide(h, max_B, nullptr);
+    if (st == DETLM_OK) st = status_from_cuda(cudaStreamSynchronize(nullptr));
+  }
+  return st;
 }
 
 int detlm_head_greedy(detlm_head_t* h, const void* h_dev, int64_t B, int32_t* token_dev,
@@ -1163,8 +1321,109 @@ int detlm_head_logprob_host(detlm_head_t* h, const void* h_host, const int32_t* 
   return read_err(h, stream);
 }
 
+int detlm_head_greedy_host_async(detlm_head_t* h, const void* h_host, int64_t B,
+                                 int32_t* token_host, void* gap_host, void* logits_host,
+                                 cudaStream_t stream) {
+  if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
+  if (h->P > 1) return DETLM_EUNSUPPORTED;   // a vocabulary shard: the *_shard calls
+  if (B == 0) return DETLM_OK;
+  if (h_host == nullptr || token_host == nullptr || gap_host == nullptr) return DETLM_EINVAL;
+  const size_t hb = static_cast<size_t>(B) * h->d * elem_bytes(h->dtype);
+  const size_t ob = static_cast<size_t>(B) * 4;
+  const size_t lb = logits_host ? static_cast<size_t>(B) * h->V * 4 : 0;
+  // results straight into the caller's buffers where the device can write
+  // them (pinned host memory): no staging, no copy back
+  void* tok_d = device_address(token_host);
+  void* gap_d = device_address(gap_host);
+  void* log_d = device_address(logits_host);
+  const bool direct = tok_d != nullptr && gap_d != nullptr &&
+                      (logits_host == nullptr || log_d != nullptr) &&
+                      aligned(tok_d, 4) && aligned(gap_d, 4) && (log_d == nullptr || aligned(log_d, 4));
+  int st = ensure_async(h, round256(hb), direct ? 0 : 2 * round256(ob) + round256(lb), stream);
+  if (st != DETLM_OK) return st;
+  if (direct) {
+    // rows the device can read (pinned, 16-byte aligned: row bytes are a
+    // multiple of 16) are staged by a kernel that chains with the previous
+    // call's kernels; other rows by a copy
+    const void* in_d = aligned(h_host, 16) ? device_address(const_cast<void*>(h_host)) : nullptr;
+    const cudaError_t e = in_d != nullptr
+                              ? launch_stage_rows(in_d, h->a_in, hb, stream)
+                              : cudaMemcpyAsync(h->a_in, h_host, hb, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return status_from_cuda(e);
+    return detlm_head_greedy(h, h->a_in, B, static_cast<int32_t*>(tok_d), gap_d, log_d, stream);
+  }
+  const int k = h->a_next;
+  uint8_t* o = static_cast<uint8_t*>(h->a_out[k]);
+  int32_t* dtok = reinterpret_cast<int32_t*>(o);
+  void* dgap = o + round256(ob);
+  void* dlog = logits_host ? o + 2 * round256(ob) : nullptr;
+  // the slot's previous copy to the host must be done before it is reused
+  cudaError_t e = cudaStreamWaitEvent(stream, h->a_freed[k], 0);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(h->a_in, h_host, hb, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return status_from_cuda(e);
+  st = detlm_head_greedy(h, h->a_in, B, dtok, dgap, dlog, stream);
+  if (st != DETLM_OK) return st;
+  e = cudaEventRecord(h->a_done[k], stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->a_copy, h->a_done[k], 0);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(token_host, dtok, ob, cudaMemcpyDeviceToHost, h->a_copy);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(gap_host, dgap, ob, cudaMemcpyDeviceToHost, h->a_copy);
+  if (e == cudaSuccess && logits_host)
+    e = cudaMemcpyAsync(logits_host, dlog, lb, cudaMemcpyDeviceToHost, h->a_copy);
+  if (e == cudaSuccess) e = cudaEventRecord(h->a_freed[k], h->a_copy);
+  if (e != cudaSuccess) return status_from_cuda(e);
+  h->a_next = k ^ 1;
+  return DETLM_OK;
+}
+
+int detlm_head_logprob_host_async(detlm_head_t* h, const void* h_host, const int32_t* targets_host,
+                                  int64_t B, float* logp_host, cudaStream_t stream) {
+  if (h == nullptr || bad_B(B)) return DETLM_EINVAL;
+  if (h->P > 1) return DETLM_EUNSUPPORTED;   // a vocabulary shard: the *_shard calls
+  if (h->dtype == DETLM_INT8) return DETLM_EUNSUPPORTED;
+  if (B == 0) return DETLM_OK;
+  if (h_host == nullptr || targets_host == nullptr || logp_host == nullptr) return DETLM_EINVAL;
+  const size_t hb = static_cast<size_t>(B) * h->d * elem_bytes(h->dtype);
+  const size_t ob = static_cast<size_t>(B) * 4;
+  void* lp_d = device_address(logp_host);
+  const bool direct = lp_d != nullptr && aligned(lp_d, 4);
+  int st = ensure_async(h, round256(hb) + round256(ob), direct ? 0 : round256(ob), stream);
+  if (st != DETLM_OK) return st;
+  if (direct) {
+    uint8_t* in = static_cast<uint8_t*>(h->a_in);
+    int32_t* dt = reinterpret_cast<int32_t*>(in + round256(hb));
+    cudaError_t e = cudaMemcpyAsync(in, h_host, hb, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dt, targets_host, ob, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return status_from_cuda(e);
+    return detlm_head_logprob(h, in, dt, B, static_cast<float*>(lp_d), stream);
+  }
+  const int k = h->a_next;
+  float* dlp = static_cast<float*>(h->a_out[k]);
+  uint8_t* in = static_cast<uint8_t*>(h->a_in);
+  int32_t* dt = reinterpret_cast<int32_t*>(in + round256(hb));
+  cudaError_t e = cudaStreamWaitEvent(stream, h->a_freed[k], 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(in, h_host, hb, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(dt, targets_host, ob, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return status_from_cuda(e);
+  st = detlm_head_logprob(h, in, dt, B, dlp, stream);
+  if (st != DETLM_OK) return st;
+  e = cudaEventRecord(h->a_done[k], stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->a_copy, h->a_done[k], 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(logp_host, dlp, ob, cudaMemcpyDeviceToHost, h->a_copy);
+  if (e == cudaSuccess) e = cudaEventRecord(h->a_freed[k], h->a_copy);
+  if (e != cudaSuccess) return status_from_cuda(e);
+  h->a_next = k ^ 1;
+  return DETLM_OK;
+}
+
 int detlm_head_check(detlm_head_t* h, cudaStream_t stream) {
   if (h == nullptr) return DETLM_EINVAL;
+  if (h->a_copy != nullptr) {
+    // the asynchronous host-buffer calls' copies to the host
+    const cudaError_t e = cudaStreamSynchronize(h->a_copy);
+    if (e != cudaSuccess) return status_from_cuda(e);
+  }
   return read_err(h, stream);
 }
 
@@ -1191,13 +1450,24 @@ int detlm_head_tiles(const detlm_head_t* h, int64_t B, int32_t* n_vtiles, int32_
 
 void detlm_head_destroy(detlm_head_t* h) {
   if (h == nullptr) return;
+  if (h->a_copy) {
+    cudaStreamSynchronize(h->a_copy);
+    cudaStreamDestroy(h->a_copy);
+  }
+  for (int k = 0; k < 2; ++k) {
+    if (h->a_done[k]) cudaEventDestroy(h->a_done[k]);
+    if (h->a_freed[k]) cudaEventDestroy(h->a_freed[k]);
+    if (h->a_out[k]) cudaFree(h->a_out[k]);
+  }
+  if (h->a_in) cudaFree(h->a_in);
   if (h->ws) cudaFree(h->ws);
   if (h->vws) cudaFree(h->vws);
   if (h->q8) cudaFree(h->q8);
   if (h->W16) cudaFree(h->W16);
   if (h->h16) cudaFree(h->h16);
   if (h->stage) cudaFree(h->stage);
-  if (h->d_err) cudaFree(h->d_err);
+  if (h->err_mapped) cudaFreeHost(h->err_mapped);
+  else if (h->d_err) cudaFree(h->d_err);
   if (h->err_host) cudaFreeHost(h->err_host);
   delete h;
 }

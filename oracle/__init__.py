@@ -12,7 +12,9 @@ Everything is computed exactly or in float64 with numpy:
   float64; logits by a float64 matrix product; the per-entry error base
   ``A = |h|·|W|ᵀ`` for the tolerance ``1e-6·A``;
 * the integer head: exact int64 matrix product (every partial sum is far
-  below 2^63), cross-checked on samples with Python big-integer dots;
+  below 2^63), cross-checked on samples with Python big-integer dots; for
+  large row counts the same exact integers through a float64 product (every
+  partial sum is an integer below 2^53);
 * greedy token (lowest index among the maxima), runner-up value of the
   multiset, top-2 gap in bf16 ulps of the winning logit, logsumexp and the
   log-probability of a target;
@@ -31,7 +33,7 @@ closed forms, invariants, and planted-mistake checks). Nothing is marked
 """
 from .head import (  # noqa: F401
     decode_bf16, decode_fp16, decode_fp32, decode_int8, decode,
-    logits_float, logits_int, bigint_dot,
+    logits_float, logits_int, logits_int_f64, bigint_dot,
     ulp_bf16, top2, greedy, greedy_int, gap_from_top2_f32,
     logsumexp, logprob,
     head_greedy, head_logprob, verify_accept,

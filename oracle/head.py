@@ -146,6 +146,23 @@ def logits_int(W: np.ndarray, h: np.ndarray) -> np.ndarray:
     return np.asarray(h, dtype=np.int64) @ np.asarray(W, dtype=np.int64).T
 
 
+def logits_int_f64(W: np.ndarray, h: np.ndarray) -> np.ndarray:
+    """The same exact integer logits through a float64 matrix product ([DetLLM]).
+
+    Every product of two int8 values is an integer of magnitude <= 2^14, and
+    every partial sum of d of them, in any order or grouping, is an integer of
+    magnitude <= d * 2^14 < 2^53 (d < 2^39): each float64 addition (or fused
+    multiply-add) is then exact, so the result is the exact integer whatever
+    order the matrix product takes -- the float64 product is used only for
+    its speed on large row counts.
+    """
+    d = np.asarray(W).shape[1]
+    if d * 128 * 128 >= 2**53:
+        raise ValueError("partial sums could exceed 2^53")
+    z = np.asarray(h, dtype=np.float64) @ np.asarray(W, dtype=np.float64).T
+    return z.astype(np.int64)
+
+
 def bigint_dot(w_row, h_row) -> int:
     """One logit by Python big-integer arithmetic (no overflow possible)."""
     return sum(int(a) * int(b) for a, b in zip(w_row.tolist(), h_row.tolist()))

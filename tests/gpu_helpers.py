@@ -9,6 +9,11 @@ import oracle
 # fp32 logits of the float heads: |z_gpu - z_ref| <= 1e-6 * sum_k |w_k h_k|
 LOGIT_RTOL = 1e-6
 
+# Every parity check's rows and its listed exceptions (decisions that differ
+# from the oracle's inside the tolerance), printed at the end of the session
+# by the terminal-summary hook in conftest.py: listed, not hidden.
+PARITY_REPORT = []
+
 
 def dev(arr: np.ndarray, fmt: str):
     import torch
@@ -80,6 +85,7 @@ def check_float_greedy(z_ref, A, tok_g, gap_g, z_g=None, label=""):
                       z_ref[n, t] - z_ref[n, tg], e[n, t] + e[n, tg])
         exceptions.append({"row": n, "oracle": t, "gpu": tg,
                            "gap_ulp": float(gap_ref[n])})
+    PARITY_REPORT.append((label, B, exceptions))
     if z_ref.shape[1] >= 2:
         ulp = oracle.ulp_bf16(m_ref)
         emax = e.max(axis=1)
@@ -127,10 +133,12 @@ def check_sample(z_ref, A, T, seeds, positions, tok_g, gap_g, label=""):
             assert sc[n, t] - sc[n, tg] <= e[n, t] + e[n, tg], (
                 label, "sampled token differs outside the bound", n, t, tg,
                 sc[n, t] - sc[n, tg], e[n, t] + e[n, tg])
-            listed.append({"row": n, "oracle": t, "gpu": tg})
+            listed.append({"row": n, "oracle": t, "gpu": tg,
+                           "gap_score": float(sc[n, t] - sc[n, tg])})
         if z_ref.shape[1] >= 2 and gap_g is not None and tg == t:
             srt = np.argsort(-sc[n], kind="stable")
             bound = e[n, srt[0]] + 2 * e[n, srt[1:3]].max() + 2.0 ** -24 * abs(float(gap_g[n]))
             assert abs(float(gap_g[n]) - (ref["m"][n] - ref["s"][n])) <= bound, (
                 label, "score gap", n, gap_g[n], ref["m"][n] - ref["s"][n], bound)
+    PARITY_REPORT.append((label, z_ref.shape[0], listed))
     return listed

@@ -294,6 +294,29 @@ def pin_int_head(o):
     assert int(out["token"][0]) == 7 and int(out["gap"][0]) == 0
     assert o.bigint_dot(W[3], h[2]) == sum(int(a) * int(b) for a, b in
                                             zip(W[3].tolist(), h[2].tolist()))
+    # the float64 product gives the same integers: random rows, and the
+    # extremes (sums of 16384 products of +-128, |z| = 2^28, where a float32
+    # sum would have rounded)
+    for z64 in (o.logits_int_f64(W, h),):
+        assert z64.dtype == np.int64
+        for n in range(B):
+            ex = [sum(int(a) * int(b) for a, b in zip(W[v].tolist(), h[n].tolist()))
+                  for v in range(V)]
+            assert [int(x) for x in z64[n]] == ex, n
+    d = 16384
+    We = np.full((2, d), -128, np.int8)
+    We[1] = 127
+    he = np.full((2, d), -128, np.int8)
+    he[1] = 127
+    he[1, -1] = -128
+    ze = o.logits_int_f64(We, he)
+    for n in range(2):
+        for v in range(2):
+            assert int(ze[n, v]) == o.bigint_dot(We[v], he[n])
+    assert int(ze[0, 0]) == 2**28
+    # 127^2 (d - 1) - 127 * 128 = 264,225,151: odd and above 2^24, so no
+    # float32 holds it
+    assert int(ze[1, 1]) == 127 * 127 * (d - 1) - 127 * 128 == 264_225_151
 
 
 def pin_invariants(o):

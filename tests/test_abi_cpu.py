@@ -112,3 +112,30 @@ def test_package_has_no_cpu_fallback():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "numpy" not in text or f == "build.py", f
+
+
+def test_shard_calls_reject_bad_arguments_on_the_host(lib):
+    from invariant_output_head_gb300 import binding as b
+    buf = ctypes.create_string_buffer(64)
+    assert lib.detlm_head_greedy_shard(None, buf, 1, buf, None, None) == b.DETLM_EINVAL
+    assert lib.detlm_head_logprob_shard(None, buf, buf, 1, buf, None) == b.DETLM_EINVAL
+    for P in (0, 3, 256):
+        assert lib.detlm_merge_greedy_shards(buf, P, 1, b.DETLM_BF16, buf, buf, None) == \
+            b.DETLM_EINVAL
+        assert lib.detlm_merge_logprob_shards(buf, P, 1, 100, buf, buf, None, None) == \
+            b.DETLM_EINVAL
+    assert lib.detlm_merge_greedy_shards(buf, 2, 1, 7, buf, buf, None) == b.DETLM_EINVAL
+    assert lib.detlm_merge_logprob_shards(buf, 2, 1, 0, buf, buf, None, None) == b.DETLM_EINVAL
+    assert lib.detlm_merge_greedy_shards(None, 2, 1, b.DETLM_BF16, buf, buf, None) == \
+        b.DETLM_EINVAL
+    assert lib.detlm_merge_greedy_shards(buf, 2, 0, b.DETLM_BF16, None, None, None) == b.DETLM_OK
+    out = ctypes.c_void_p(0)
+    assert lib.detlm_head_create_shard(ctypes.byref(out), buf, 1000, 64, b.DETLM_BF16, 3, 0) == \
+        b.DETLM_EINVAL
+
+
+def test_peak_probe_library_loads_and_exports_its_entry_point():
+    from invariant_output_head_gb300 import build
+    build.build()
+    probe = ctypes.CDLL(build.PEAK_LIB)
+    assert hasattr(probe, "detlm_mma_f16_peak")

@@ -135,6 +135,48 @@ def test_host_buffer_calls_match_device_calls(env):
     assert (lh.view(np.uint32) == host(lp).view(np.uint32)).all()
 
 
+def test_async_host_buffer_calls_match_device_calls(env):
+    """Many asynchronous host-buffer calls of changing batch size (one result
+    buffer set per call, pinned or pageable), one check at the end: every
+    call's results equal the device call's bit for bit, whether the kernels
+    wrote them to pinned host memory directly or they were staged and copied
+    back while the next call ran."""
+    torch, b = env
+    V, d = 900, 256
+    case = synth.small_float(16, V, d, 40)
+    head = b.Head(dev(case["W"], "bf16"), "bf16")
+    hd = dev(case["h"], "bf16")
+    td = dev(case["targets"], "int32")
+    t, g, z = (host(x) for x in head.greedy(hd, with_logits=True))
+    lp = host(head.logprob(hd, td))
+    h_pin = torch.from_numpy(np.ascontiguousarray(case["h"]).view(np.int16)).pin_memory()
+    tg_pin = torch.from_numpy(case["targets"]).pin_memory()
+    s = torch.cuda.current_stream().cuda_stream
+    calls = [(0, 1), (1, 7), (8, 40 - 8), (3, 5), (0, 40), (39, 1)]
+    outs = []
+    for k, (r0, B) in enumerate(calls):
+        # pinned result buffers (written by the kernels directly) and, every
+        # other call, pageable ones (staged on the device, copied back)
+        alloc = ((lambda *a, **kw: torch.empty(*a, **kw).pin_memory()) if k % 2 == 0
+                 else (lambda *a, **kw: torch.empty(*a, **kw)))
+        o = (alloc(B, dtype=torch.int32), alloc(B, dtype=torch.float32),
+             alloc((B, V), dtype=torch.float32), alloc(B, dtype=torch.float32))
+        hp = h_pin.data_ptr() + r0 * d * 2
+        b.detlm_head_greedy_host_async(head.handle, hp, B, o[0].data_ptr(), o[1].data_ptr(),
+                                       o[2].data_ptr(), s)
+        b.detlm_head_logprob_host_async(head.handle, hp, tg_pin.data_ptr() + 4 * r0, B,
+                                        o[3].data_ptr(), s)
+        outs.append(o)
+    assert head.check() == 0
+    for (r0, B), o in zip(calls, outs):
+        sl = slice(r0, r0 + B)
+        assert (o[0].numpy() == t[sl]).all()
+        assert (o[1].numpy().view(np.uint32) == g[sl].view(np.uint32)).all()
+        assert (o[2].numpy().view(np.uint32) == z[sl].view(np.uint32)).all()
+        assert (o[3].numpy().view(np.uint32) == lp[sl].view(np.uint32)).all()
+    head.close()
+
+
 def test_reserved_workspace_and_tiles(env):
     torch, b = env
     case = synth.small_float(7, 1000, 128, 300)

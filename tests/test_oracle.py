@@ -47,6 +47,9 @@ MUTANTS = {
     "int_narrow_accumulator": ("return np.asarray(h, dtype=np.int64) @ np.asarray(W, dtype=np.int64).T",
                                "return (np.asarray(h, dtype=np.int64) @ np.asarray(W, dtype=np.int64).T).astype(np.int16).astype(np.int64)"),
     "int_gap_reversed": ("        gap = m - s\n", "        gap = s - m\n"),
+    "int_f64_narrowed": ("    return z.astype(np.int64)\n", "    return z.astype(np.float32).astype(np.int64)\n"),
+    "int_f64_transposed": ("    z = np.asarray(h, dtype=np.float64) @ np.asarray(W, dtype=np.float64).T\n",
+                           "    z = (np.asarray(W, dtype=np.float64) @ np.asarray(h, dtype=np.float64).T).T[:, ::-1]\n"),
     "verify_accept_counts_all_matches": ("        while a < P and drafts[r, a] == tokens[r, a]:\n            a += 1",
                                          "        a = int((drafts[r] == tokens[r]).sum())"),
     "verify_accept_off_by_one": ("        out[r] = a\n", "        out[r] = min(a + 1, P)\n"),
