@@ -398,6 +398,8 @@ int detlm_greedy_noalloc(const void* W_dev, int64_t V, int64_t d, int dtype,
                          float* gap_dev, float* logits_dev, int* err_dev,
                          cudaStream_t stream);
 
+/* Release the handle: waits for the device (the handle's work may still run
+ * on any stream), then frees everything the handle owns. W is not freed. */
 void detlm_head_destroy(detlm_head_t* head);
 
 const char* detlm_status_string(int status);

@@ -1450,6 +1450,11 @@ int detlm_head_tiles(const detlm_head_t* h, int64_t B, int32_t* n_vtiles, int32_
 
 void detlm_head_destroy(detlm_head_t* h) {
   if (h == nullptr) return;
+  // the handle's kernels and copies may still run on any stream: let them
+  // finish before their memory (device, and mapped host memory that the
+  // kernels write) is released
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
   if (h->a_copy) {
     cudaStreamSynchronize(h->a_copy);
     cudaStreamDestroy(h->a_copy);
