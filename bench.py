@@ -124,6 +124,8 @@ KERNEL_SOURCES = {
     "head_gemm_kernel": ("detlm_head.cu", "head_kernels.cuh", "ptx.cuh"),
     "head_rows_kernel": ("detlm_head.cu", "head_kernels.cuh", "ptx.cuh", "rows_kernels.cuh"),
     "int8_gemm_kernel": ("detlm_head.cu", "head_kernels.cuh", "int8_kernels.cuh", "ptx.cuh"),
+    "head_pair_kernel": ("detlm_head.cu", "head_kernels.cuh", "pair_kernels.cuh", "ptx.cuh",
+                         "rows_kernels.cuh"),
 }
 
 
@@ -140,11 +142,19 @@ def kernel_source_hash(kernel: str) -> str:
 
 
 def projection_kernel(workload: str, batch: int) -> str:
-    """Name of the call's projection kernel (the one the roofline covers)."""
-    if WORKLOADS[workload]["fmt"] == "int8" and batch < 256:
-        return "int8_gemm_kernel"
-    if workload == "logprob":
+    """Name of the call's projection kernel (the one the roofline covers): the
+    integer head's streaming kernel below 256 rows; the log-prob kernel; the
+    pair kernel for greedy calls (plain, verify, integer) of more than 128
+    rows; the one-CTA kernel otherwise (and for the gated and sampling
+    calls)."""
+    spec = WORKLOADS[workload]
+    rows = spec.get("B", batch)
+    if spec["fmt"] == "int8":
+        return "int8_gemm_kernel" if batch < 256 else "head_pair_kernel"
+    if spec["mode"] == "logprob":
         return "head_rows_kernel"
+    if spec["mode"] in ("greedy", "verify") and rows > 128:
+        return "head_pair_kernel"
     return "head_gemm_kernel"
 
 

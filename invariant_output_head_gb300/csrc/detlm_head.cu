@@ -21,6 +21,7 @@
 #include "int8_kernels.cuh"
 #include "quant_kernels.cuh"
 #include "rows_kernels.cuh"
+#include "pair_kernels.cuh"
 #include "shard_kernels.cuh"
 
 using namespace detlm;
@@ -37,6 +38,7 @@ struct detlm_head {
   CUtensorMap tmW;
   int n_vt = 0, nk = 0, num_sms = 0;
   int rows_pairs = 0;        // CTA pairs of the rows kernel that fit at once (0: not asked yet)
+  int wide_pairs = 0;        // the same for the wide greedy kernel
   int* d_err = nullptr;
   int* err_host = nullptr;   // pinned word the error word is read into
   // where the GPU has native atomics on host memory (Grace with NVLink-C2C),
@@ -355,6 +357,53 @@ cudaError_t launch_rows_kernel(detlm_head* h, const CUtensorMap& tmH, const Head
   return cudaLaunchKernelEx(&cfg, kern, h->tmW, tmH, p);
 }
 
+// Stages of the wide greedy pair kernel: as many 32 KB stages as shared
+// memory holds.
+int pair_stages() {
+  const PairLayout L1 = pair_layout(1);
+  const uint32_t fixed = L1.total - L1.stage_bytes + 2u * kPairMaxStages * 8u + 1024u;
+  int s = static_cast<int>((kSmemLimit - fixed) / L1.stage_bytes);
+  return s > kPairMaxStages ? kPairMaxStages : s;
+}
+
+// The wide greedy pair kernel's launch: clusters of two CTAs, as many pairs
+// as fit on the GPU at once up to one per unit, a programmatic dependent of
+// the previous kernel.
+template <int MODE>
+cudaError_t launch_pair_kernel(detlm_head* h, const CUtensorMap& tmW, const CUtensorMap& tmH,
+                               const HeadParams& p, int64_t units, size_t smem,
+                               cudaStream_t stream) {
+  auto kern = head_pair_kernel<MODE>;
+  cudaError_t e = prepare_kernel<head_pair_kernel<MODE>>(kRegsLaunchWide);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.blockDim = dim3(kPairThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  if (h->wide_pairs == 0) {
+    cfg.gridDim = dim3(static_cast<unsigned>(h->num_sms & ~1));
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters <= 0) return cudaErrorInvalidConfiguration;
+    h->wide_pairs = clusters < h->num_sms / 2 ? clusters : h->num_sms / 2;
+  }
+  const int64_t pairs = units < h->wide_pairs ? units : h->wide_pairs;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, tmW, tmH, p);
+}
+
 // 256-entry tiles of a vocabulary of V (the log-sum-exp records' tiles, and
 // the unit of the vocabulary shards)
 int64_t tiles256(int64_t V) { return (V + kRowsN - 1) / kRowsN; }
@@ -412,9 +461,12 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   // folded per row, in a fixed order, whatever B is)
   constexpr bool rows = MODE == MODE_LOGPROB;
   const int N = rows ? kRowsN : cols_for(B);
+  // greedy calls of more than 128 rows: the pair kernel (W on the MMA's M
+  // axis over two CTAs; the same logits bit for bit)
+  const bool wide = MODE == MODE_GREEDY && N == kPairN;
   CUtensorMap tmH;
-  if (!encode_2d(&tmH, h->dtype, h_dev, h->d, B, rows ? static_cast<uint32_t>(kRowsHalf)
-                                                      : static_cast<uint32_t>(N)))
+  if (!encode_2d(&tmH, h->dtype, h_dev, h->d, B, (rows || wide) ? static_cast<uint32_t>(kRowsHalf)
+                                                                 : static_cast<uint32_t>(N)))
     return DETLM_EINVAL;
   int st = ensure_ws(h, B, stream);
   if (st != DETLM_OK) return st;
@@ -438,6 +490,15 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
     p.n_issuers = 1;
     p.tmem_cols = 512;
     p.idesc = idesc_f16(h->dtype == DETLM_BF16 ? 1u : 0u, kRowsM, kRowsN);
+  } else if (wide) {
+    // units: two 128-row vocabulary tiles x 256 hidden rows (one CTA pair)
+    p.n_vt = h->n_vt;
+    p.n_nt = static_cast<int32_t>((B + kPairN - 1) / kPairN);
+    p.n_slots = 2;
+    p.stages = pair_stages();
+    p.n_issuers = 1;
+    p.tmem_cols = 512;
+    p.idesc = idesc_f16(h->dtype == DETLM_BF16 ? 1u : 0u, 2 * kBM, kPairN);
   } else {
     p.n_vt = h->n_vt;
     p.n_nt = static_cast<int32_t>((B + N - 1) / N);
@@ -468,16 +529,24 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
     p.temperature = gate->temperature;
   }
 
-  const size_t smem = rows ? rows_layout(p.stages).total + 1024
-                           : smem_layout(N, p.stages, kExtraSmem).total + 1024;
-  const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
+  const size_t smem = rows   ? rows_layout(p.stages).total + 1024
+                     : wide ? pair_layout(p.stages).total + 1024
+                            : smem_layout(N, p.stages, kExtraSmem).total + 1024;
+  const int64_t units = wide ? static_cast<int64_t>((p.n_vt + 1) / 2) * p.n_nt
+                             : static_cast<int64_t>(p.n_vt) * p.n_nt;
   const int grid = static_cast<int>(units < h->num_sms ? units : h->num_sms);
   if (h->t_start) cudaEventRecord(h->t_start, stream);
   cudaError_t e;
-  if constexpr (rows)
+  if constexpr (rows) {
     e = launch_rows_kernel(h, tmH, p, units, smem, stream);
-  else
+  } else if constexpr (MODE == MODE_GREEDY) {
+    if (wide)
+      e = launch_pair_kernel<MODE_GREEDY>(h, h->tmW, tmH, p, units, smem, stream);
+    else
+      e = launch_gemm<MODE>(h->tmW, tmH, p, grid, smem, stream);
+  } else {
     e = launch_gemm<MODE>(h->tmW, tmH, p, grid, smem, stream);
+  }
   if (h->t_stop) {
     cudaEventRecord(h->t_stop, stream);
     h->t_start = h->t_stop = nullptr;
@@ -615,9 +684,11 @@ int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token
   if (sw != DETLM_OK) return sw;
   e = i8_to_f16(h_dev, h->h16, static_cast<size_t>(B) * h->d, stream);
   if (e != cudaSuccess) return status_from_cuda(e);
-  const int N = cols_for(B);
+  // the pair kernel (W on the MMA's M axis over two CTAs), as the float
+  // heads' calls of more than 128 rows
   CUtensorMap tmH;
-  if (!encode_2d(&tmH, DETLM_FP16, h->h16, h->d, B, static_cast<uint32_t>(N))) return DETLM_EINVAL;
+  if (!encode_2d(&tmH, DETLM_FP16, h->h16, h->d, B, static_cast<uint32_t>(kRowsHalf)))
+    return DETLM_EINVAL;
   int st = ensure_ws(h, B, stream);
   if (st != DETLM_OK) return st;
   const WsView w = ws_view(h);
@@ -627,16 +698,16 @@ int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token
   p.V = static_cast<int32_t>(h->V);
   p.d = static_cast<int32_t>(h->d);
   p.B = static_cast<int32_t>(B);
-  p.N = N;
+  p.N = kPairN;
   p.n_vt = h->n_vt;
-  p.n_nt = static_cast<int32_t>((B + N - 1) / N);
+  p.n_nt = static_cast<int32_t>((B + kPairN - 1) / kPairN);
   p.nk = static_cast<int32_t>((h->d * 2 + kRowBytes - 1) / kRowBytes);
   p.n_chunks = static_cast<int32_t>((h->d + kChunkK - 1) / kChunkK);
-  p.n_slots = slots_for(N);
-  p.stages = stages_for(N);
-  p.n_issuers = issuers_for(N, p.stages, &p.n_slots);
-  p.tmem_cols = tmem_cols_for(p.n_slots * N);
-  p.idesc = idesc_f16(0u, kBM, static_cast<uint32_t>(N));
+  p.n_slots = 2;
+  p.stages = pair_stages();
+  p.n_issuers = 1;
+  p.tmem_cols = 512;
+  p.idesc = idesc_f16(0u, 2 * kBM, kPairN);
   p.logits = reinterpret_cast<float*>(logits);
   p.rec_m = w.m;
   p.rec_i = w.i;
@@ -645,11 +716,10 @@ int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token
   p.stall = h->stall;
   p.timeout_ns = h->timeout_ns;
   p.v_off = static_cast<int32_t>(h->v_off);
-  const size_t smem = smem_layout(N, p.stages).total + 1024;
-  const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
-  const int grid = static_cast<int>(units < h->num_sms ? units : h->num_sms);
+  const size_t smem = pair_layout(p.stages).total + 1024;
+  const int64_t units = static_cast<int64_t>((p.n_vt + 1) / 2) * p.n_nt;
   if (h->t_start) cudaEventRecord(h->t_start, stream);
-  e = launch_gemm<MODE_INT>(h->tmW16, tmH, p, grid, smem, stream);
+  e = launch_pair_kernel<MODE_INT>(h, h->tmW16, tmH, p, units, smem, stream);
   if (h->t_stop) {
     cudaEventRecord(h->t_stop, stream);
     h->t_start = h->t_stop = nullptr;

@@ -1,0 +1,399 @@
+// pair_kernels.cuh -- the wide greedy projection (more than 128 hidden rows)
+// on CTA pairs, with W on the tensor core's M axis.
+//
+// Kernel 1c (head_pair_kernel): the same logits as head_gemm_kernel -- the
+// same K chunks, the same fp32 round-to-nearest (integer head: int32) fold
+// of the chunk sums -- computed by clusters of two CTAs with
+// tcgen05.mma.cta_group::2. A unit is 256 vocabulary rows (two 128-row tiles,
+// one per CTA; the MMA's M axis) x 256 hidden rows (N). Each CTA loads its own
+// W tile box and its own half of the hidden-row box (128 of the 256 rows) per
+// 64-element K step: 32 KB of shared memory written per CTA and step instead
+// of the 48 KB a one-CTA 128 x 256 unit needs, and the tensor core reads half
+// of B from each CTA. On GB300 the one-CTA kernel at N = 256 is bound by
+// shared-memory bandwidth (its TMA fill plus the MMA's operand reads run near
+// 100 bytes per clock per SM, and the 128 x 256 x 16 MMAs take ~112 ns
+// instead of 65), which the pair layout relieves.
+//
+// Each CTA finds its 128 vocabulary rows x 256 hidden-row columns of the
+// product in its own tensor memory (lane = vocabulary row), so the epilogue
+// is head_gemm_kernel's: fp32 logits stored with a warp's lanes on
+// consecutive vocabulary entries (128-byte coalesced stores), then per
+// 16-column block a shared-memory transpose fold, the four lane quarters
+// merged in a fixed order, one record per (hidden row, 128-row tile). The
+// tensor core's result for an element depends neither on the operand roles
+// nor on the pair mode (checked bit for bit on GB300 with standalone
+// probes), so the logits are head_gemm_kernel's bit for bit, and the greedy
+// record is exact.
+//
+// The pair protocol is the log-prob kernel's (rows_kernels.cuh): the leader
+// issues every MMA; both producers' loads complete on the leader's stage
+// barrier; MMA commits arrive on both CTAs' barriers (multicast); a chunk's
+// accumulator slot goes back to the MMA when the eight epilogue warps of both
+// CTAs have arrived on the leader's slot-empty barrier. Every wait is bounded.
+#pragma once
+#include "head_kernels.cuh"
+#include "rows_kernels.cuh"
+
+namespace detlm {
+
+constexpr int kPairThreads = 384;
+constexpr int kPairMaxStages = 7;
+constexpr int kPairN = 256;         // hidden rows per unit (MMA N)
+constexpr int kPairWarps = 8;       // epilogue warps 4 .. 11, 128 columns each
+
+struct PairLayout {
+  uint32_t a_bytes, b_bytes, stage_bytes, ctrl_off, red_off, xp_off, total;
+};
+
+// Stage s: this CTA's W tile box [128 rows x 128 B] (operand A) then its half
+// of the hidden-row box [128 rows x 128 B] (operand B), both 128-byte
+// swizzled; then the barriers, the per-quarter column results (3 words x 4
+// quarters x 256 columns) and the epilogue warps' transpose areas.
+__host__ __device__ inline PairLayout pair_layout(int stages) {
+  PairLayout L;
+  L.a_bytes = kBM * kRowBytes;
+  L.b_bytes = kRowsHalf * kRowBytes;
+  L.stage_bytes = L.a_bytes + L.b_bytes;
+  L.ctrl_off = static_cast<uint32_t>(stages) * L.stage_bytes;
+  // full[S], empty[S], slot_full[2], slot_empty[2], never, drain; then the
+  // TMEM address holder and the abort flag
+  L.red_off = L.ctrl_off + (2u * stages + 6u) * 8u + 16u;
+  L.xp_off = L.red_off + 3u * 4u * kPairN * 4u;
+  L.total = L.xp_off + kPairWarps * kXpWords * 4u;
+  return L;
+}
+
+// p.n_vt: 128-row vocabulary tiles (the records' tiles); a unit covers tiles
+// 2 vp and 2 vp + 1 (the second may lie past V: its rows read as zeros and
+// it writes nothing). p.n_nt: 256-row hidden tiles.
+template <int MODE>
+__global__ void __launch_bounds__(kPairThreads, 1)
+head_pair_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
+                 const HeadParams p) {
+  static_assert(MODE == MODE_GREEDY || MODE == MODE_INT, "mode");
+  constexpr int N = kPairN;
+  constexpr int WBLK = 8;                          // 16-column blocks per epilogue warp
+  constexpr int ET = 32 * kPairWarps;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = p.stages;
+  const PairLayout L = pair_layout(S);
+  const uint32_t rank = cluster_rank();            // 0: leader, 1: peer
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int n_pairs = static_cast<int>(gridDim.x >> 1);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.ctrl_off);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+  const uint32_t never_bar = bar0 + 8u * (2 * S + 4);
+  const uint32_t drain_bar = bar0 + 8u * (2 * S + 5);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.ctrl_off + (2 * S + 6) * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  float* red_m = reinterpret_cast<float*>(smem + L.red_off);
+  int32_t* red_i = reinterpret_cast<int32_t*>(red_m + 4 * N);
+  float* red_s = reinterpret_cast<float*>(red_i + 4 * N);
+  float* xpose = reinterpret_cast<float*>(smem + L.xp_off);
+  const uint32_t smem_base = smem_u32(smem);
+  auto sA = [&](int s) { return smem_base + static_cast<uint32_t>(s) * L.stage_bytes; };
+  auto sB = [&](int s) { return sA(s) + L.a_bytes; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);       // the leader's arrival (+ both CTAs' loads)
+      mbar_init(empty_bar(s), 1);      // the leader's MMA commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);       // the leader's MMA commit
+      mbar_init(acce_bar(b), 2 * kPairWarps);   // eight epilogue warps of each CTA
+    }
+    mbar_init(never_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmH);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_holder), 512u);
+    tmem_relinquish_pair();
+  }
+  // both CTAs' barriers are initialised before any load or arrival of the
+  // other CTA can reach them
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int n_vp = (p.n_vt + 1) >> 1;   // 256-row vocabulary units
+  const int n_units = n_vp * p.n_nt;
+  const int kElems = kRowBytes / 2;     // 16-bit elements per 128-byte box row
+  const int spu = p.nk;                 // one K box per stage
+  const int half = static_cast<int>(rank) * kRowsHalf;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegsWg0Wide));
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_h = policy_evict_last();
+      const bool leader = rank == 0;
+      // W is read-only for the head's life: the W boxes of the first S
+      // stages are requested before waiting for the previous kernels on the
+      // stream; the hidden rows (which a previous kernel may write) after.
+      const int n_my = (n_units - pair + n_pairs - 1) / n_pairs;
+      const int pre = min(S, n_my > 0 ? n_my * spu : 0);
+      for (int j = 0; j < pre; ++j) {
+        const int u = pair + (j / spu) * n_pairs;
+        const int vp = u / p.n_nt, kb = j - (j / spu) * spu;
+        if (leader) mbar_expect_tx(full_bar(j), 2u * L.stage_bytes);
+        tma_load_2d_pair(sA(j), &tmW, kb * kElems, vp * (2 * kBM) + half,
+                         cluster_addr(full_bar(j), 0), pol_w);
+      }
+      grid_dep_wait();
+      uint32_t stage = 0, phase = 0, outstanding = 0, out_par = 0;
+      bool ok = true;
+      int j = 0;
+      for (int u = pair; u < n_units && ok; u += n_pairs) {
+        const int vp = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
+        for (int kb = 0; kb < spu; ++kb, ++j) {
+          const uint32_t fb = cluster_addr(full_bar(stage), 0);
+          if (j < pre) {
+            tma_load_2d_pair(sB(stage), &tmH, kb * kElems, nt * N + half, fb, pol_h);
+            if (leader) mbar_arrive(full_bar(stage));
+          } else {
+            if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) { ok = false; break; }
+            if (leader) mbar_arrive_expect_tx(full_bar(stage), 2u * L.stage_bytes);
+            tma_load_2d_pair(sA(stage), &tmW, kb * kElems, vp * (2 * kBM) + half, fb, pol_w);
+            tma_load_2d_pair(sB(stage), &tmH, kb * kElems, nt * N + half, fb, pol_h);
+          }
+          outstanding |= 1u << stage;
+          out_par = (out_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(p.err, ERR_TIMEOUT);
+        if (leader) {
+          // the armed stages complete once both CTAs' loads have landed
+          const int zero = 0;
+          for (int s = 0; s < S; ++s)
+            if ((outstanding >> s) & 1u) mbar_wait(full_bar(s), (out_par >> s) & 1u, &zero, p.timeout_ns);
+        } else {
+          // the peer's loads complete on the leader's barriers: give the
+          // ones in flight time to land before this CTA may leave
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < kPairSettleNs) __nanosleep(1000);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegsWg0Wide));
+    if (lane == 0 && rank == 0) {
+      uint32_t stage = 0, phase = 0, slot = 0, sph = 0;
+      bool ok = true;
+      if (p.stall) ok = mbar_wait(never_bar, 0, abort_flag, p.timeout_ns);
+      for (int u = pair; u < n_units && ok; u += n_pairs) {
+        for (int c = 0; c < p.n_chunks && ok; ++c) {
+          if (!mbar_wait(acce_bar(slot), sph ^ 1u, abort_flag, p.timeout_ns)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + slot * static_cast<uint32_t>(N);
+#pragma unroll
+          for (int sc = 0; sc < kBlocksPerChunk; ++sc) {
+            const int kb = c * kBlocksPerChunk + sc;
+            if (kb >= p.nk) break;
+            if (!mbar_wait(full_bar(stage), phase, abort_flag, p.timeout_ns)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t da = sdesc_sw128(sA(stage));
+            const uint64_t db = sdesc_sw128(sB(stage));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)   // K = 16 per MMA: 32 bytes = 2 descriptor units
+              mma_f16_pair(d_tmem, da + 2u * k, db + 2u * k, p.idesc, !(sc == 0 && k == 0));
+            mma_commit_pair(empty_bar(stage), 3);
+            if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+          }
+          if (!ok) break;
+          mma_commit_pair(accf_bar(slot), 3);
+          if (++slot == 2u) { slot = 0; sph ^= 1u; }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(p.err, ERR_TIMEOUT);
+      }
+      mma_commit_pair(drain_bar, 1);
+      const int zero = 0;
+      mbar_wait(drain_bar, 0, &zero, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // warps 2 and 3: no role, fewer registers
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegsWg0Wide));
+  } else {
+    // --------------------------------------------------------- epilogue
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(kRegsEpiWide));
+    grid_dep_wait();          // outputs and records: only after the previous kernels
+    const int q = warp & 3;                    // TMEM lane quarter
+    const int g = (warp - 4) >> 2;             // column half (hidden rows 128 g ..)
+    const int et = threadIdx.x - 128;          // 0 .. ET-1
+    const int row = q * 32 + lane;             // vocabulary row within this CTA's tile
+    const uint32_t tlane = static_cast<uint32_t>(q * 32) << 16;
+    float* xp = xpose + (warp - 4) * kXpWords;
+    uint32_t slot = 0, sph = 0;
+    bool failed = false;
+    using Acc = typename std::conditional<MODE == MODE_INT, int32_t, float>::type;
+    for (int u = pair; u < n_units; u += n_pairs) {
+      const int vp = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
+      Acc acc[WBLK][16];
+      for (int c = 0; c < p.n_chunks; ++c) {
+        const uint32_t cur = slot, cph = sph;
+        if (++slot == 2u) { slot = 0; sph ^= 1u; }
+        if (!failed && !mbar_wait(accf_bar(cur), cph, abort_flag, p.timeout_ns)) {
+          failed = true;
+          *abort_flag = 1;
+        }
+        if (failed) continue;
+        tc_fence_after();
+        const uint32_t sbase = tmem_base + tlane + cur * static_cast<uint32_t>(N) +
+                               static_cast<uint32_t>(g * WBLK * 16);
+        // two groups of four 16-column loads, one wait each (a wait per
+        // load leaves the drain latency-bound)
+#pragma unroll
+        for (int h4 = 0; h4 < 2; ++h4) {
+          uint32_t rr[4][16];
+#pragma unroll
+          for (int b4 = 0; b4 < 4; ++b4) tmem_ld16(sbase + (h4 * 4 + b4) * 16, rr[b4]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int b4 = 0; b4 < 4; ++b4) {
+            const int bb = h4 * 4 + b4;
+            if constexpr (MODE == MODE_INT) {
+              // exact integer chunk sums (|sum| <= 128 * 2^14 = 2^21): adding
+              // 1.5 * 2^23 is exact and leaves the integer in the low
+              // mantissa bits; int32 fold
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int32_t x =
+                    __float_as_int(__fadd_rn(__uint_as_float(rr[b4][i]), 12582912.0f)) - 0x4B400000;
+                acc[bb][i] = (c == 0) ? x : acc[bb][i] + x;
+              }
+            } else if (c == 0) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) acc[bb][i] = __uint_as_float(rr[b4][i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) acc[bb][i] = __fadd_rn(acc[bb][i], __uint_as_float(rr[b4][i]));
+            }
+          }
+        }
+        tc_fence_before();   // slot fully read: hand it back to the leader's MMA warp
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0) mbar_arrive(acce_bar(cur));
+          else mbar_arrive_remote(cluster_addr(acce_bar(cur), 0));
+        }
+      }
+      if (epi_bar_or<ET>(failed || *abort_flag)) {
+        if (et == 0) { *abort_flag = 1; atomicOr(p.err, ERR_TIMEOUT); }
+        break;
+      }
+      const int tile = 2 * vp + static_cast<int>(rank);   // this CTA's 128-row tile
+      const bool tile_ok = tile < p.n_vt;
+      const int v = tile * kBM + row;
+      const bool vok = tile_ok && v < p.V;
+      const int n0 = nt * N;
+      const int vg0 = p.v_off + tile * kBM + q * 32;      // vocabulary index of this warp's row 0
+#pragma unroll
+      for (int bb = 0; bb < WBLK; ++bb) {
+        const int c0 = (g * WBLK + bb) * 16;
+        if (p.logits != nullptr && vok) {
+          Acc* lg = reinterpret_cast<Acc*>(p.logits);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int n = n0 + c0 + i;
+            if (n < p.B) lg[static_cast<size_t>(n) * p.V + v] = acc[bb][i];
+          }
+        }
+        if constexpr (MODE == MODE_INT) {
+          int32_t* xpi = reinterpret_cast<int32_t*>(xp);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) xpi[lane * kXpStride + i] = vok ? acc[bb][i] : INT32_MIN;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) xp[lane * kXpStride + i] = vok ? acc[bb][i] : -INFINITY;
+        }
+        __syncwarp();
+        if constexpr (MODE == MODE_INT) {
+          const ITop2 t = xp_itop2(reinterpret_cast<const int32_t*>(xp), lane, vg0);
+          if (lane < 16) {
+            reinterpret_cast<int32_t*>(red_m)[q * N + c0 + lane] = t.m;
+            red_i[q * N + c0 + lane] = t.i;
+            reinterpret_cast<int32_t*>(red_s)[q * N + c0 + lane] = t.s;
+          }
+        } else {
+          const Top2 t = xp_top2(xp, lane, vg0);
+          if (lane < 16) {
+            red_m[q * N + c0 + lane] = t.m;
+            red_i[q * N + c0 + lane] = t.i;
+            red_s[q * N + c0 + lane] = t.s;
+          }
+        }
+        __syncwarp();
+      }
+      named_bar_sync(1, ET);
+      // fixed combination of the four 32-row quarters: (q0 . q1) . (q2 . q3)
+      if (tile_ok) {
+        for (int c = et; c < N; c += ET) {
+          const int n = n0 + c;
+          if (n >= p.B) continue;
+          const size_t o = static_cast<size_t>(n) * p.n_vt + tile;   // records [B][n_vt]
+          if constexpr (MODE == MODE_INT) {
+            const int32_t* rm = reinterpret_cast<const int32_t*>(red_m);
+            const int32_t* rs = reinterpret_cast<const int32_t*>(red_s);
+            ITop2 t[4];
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) t[qq] = ITop2{rm[qq * N + c], red_i[qq * N + c], rs[qq * N + c]};
+            const ITop2 r = itop2_merge(itop2_merge(t[0], t[1]), itop2_merge(t[2], t[3]));
+            reinterpret_cast<int32_t*>(p.rec_m)[o] = r.m;
+            p.rec_i[o] = r.i;
+            reinterpret_cast<int32_t*>(p.rec_s)[o] = r.s;
+          } else {
+            Top2 t[4];
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq)
+              t[qq] = Top2{red_m[qq * N + c], red_i[qq * N + c], red_s[qq * N + c]};
+            const Top2 r = top2_merge(top2_merge(t[0], t[1]), top2_merge(t[2], t[3]));
+            p.rec_m[o] = r.m;
+            p.rec_i[o] = r.i;
+            p.rec_s[o] = r.s;
+          }
+        }
+      }
+      named_bar_sync(1, ET);
+    }
+    if (failed && et == 0) atomicOr(p.err, ERR_TIMEOUT);
+  }
+
+  // neither CTA leaves (or frees its tensor memory) before the leader's MMAs
+  // and both CTAs' remote arrivals are done
+  tc_fence_before();
+  cluster_sync();
+  // the merge kernel may be scheduled now (at the end: waiting merge blocks
+  // would share the SMs' issue slots with this kernel for its whole run)
+  grid_dep_launch();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, 512u);
+  }
+}
+
+}  // namespace detlm

@@ -8,10 +8,12 @@ import bench
 
 def test_projection_kernel_per_workload():
     assert bench.projection_kernel("pr1", 1) == "head_gemm_kernel"
-    assert bench.projection_kernel("spec", 256) == "head_gemm_kernel"
+    assert bench.projection_kernel("spec", 256) == "head_pair_kernel"
+    assert bench.projection_kernel("verify", 256) == "head_pair_kernel"
+    assert bench.projection_kernel("gated", 1) == "head_gemm_kernel"
     assert bench.projection_kernel("logprob", 8192) == "head_rows_kernel"
     assert bench.projection_kernel("int8", 1) == "int8_gemm_kernel"
-    assert bench.projection_kernel("int8", 512) == "head_gemm_kernel"   # fp16 copies, wide path
+    assert bench.projection_kernel("int8", 512) == "head_pair_kernel"   # fp16 copies, wide path
     for kernel in {bench.projection_kernel(w, b) for w in bench.WORKLOADS for b in (1, 512)}:
         assert kernel in bench.KERNEL_SOURCES
 
