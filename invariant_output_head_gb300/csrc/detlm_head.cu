@@ -360,10 +360,25 @@ cudaError_t launch_rows_kernel(detlm_head* h, const CUtensorMap& tmH, const Head
 // Stages of the wide greedy pair kernel: as many 32 KB stages as shared
 // memory holds.
 int pair_stages() {
-  const PairLayout L1 = pair_layout(1);
-  const uint32_t fixed = L1.total - L1.stage_bytes + 2u * kPairMaxStages * 8u + 1024u;
-  int s = static_cast<int>((kSmemLimit - fixed) / L1.stage_bytes);
-  return s > kPairMaxStages ? kPairMaxStages : s;
+  int s = kPairMaxStages;
+  while (s > 2 && pair_layout(s).total + 1024u > kSmemLimit) --s;
+  return s;
+}
+
+// The pair kernel's logits tensor map: [B][V] 4-byte elements, box 16 x 32
+// (a warp's staging buffer), 64-byte swizzle. Needs 16-byte aligned rows:
+// V a multiple of 4 and a 16-byte aligned base; otherwise the kernel stores
+// the logits with plain stores (returns false).
+bool encode_logits(CUtensorMap* m, const void* logits, int64_t V, int64_t B, bool int32) {
+  if (logits == nullptr || (V & 3) != 0 || !aligned(logits, 16)) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(V) * 4u};
+  cuuint32_t box[2] = {16u, 32u};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, int32 ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                  const_cast<void*>(logits), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // The wide greedy pair kernel's launch: clusters of two CTAs, as many pairs
@@ -371,8 +386,8 @@ int pair_stages() {
 // the previous kernel.
 template <int MODE>
 cudaError_t launch_pair_kernel(detlm_head* h, const CUtensorMap& tmW, const CUtensorMap& tmH,
-                               const HeadParams& p, int64_t units, size_t smem,
-                               cudaStream_t stream) {
+                               const CUtensorMap& tmL, const HeadParams& p, int64_t units,
+                               size_t smem, cudaStream_t stream) {
   auto kern = head_pair_kernel<MODE>;
   cudaError_t e = prepare_kernel<head_pair_kernel<MODE>>(kRegsLaunchWide);
   if (e != cudaSuccess) return e;
@@ -401,7 +416,7 @@ cudaError_t launch_pair_kernel(detlm_head* h, const CUtensorMap& tmW, const CUte
   const int64_t pairs = units < h->wide_pairs ? units : h->wide_pairs;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, tmW, tmH, p);
+  return cudaLaunchKernelEx(&cfg, kern, tmW, tmH, tmL, p);
 }
 
 // 256-entry tiles of a vocabulary of V (the log-sum-exp records' tiles, and
@@ -535,13 +550,15 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   const int64_t units = wide ? static_cast<int64_t>((p.n_vt + 1) / 2) * p.n_nt
                              : static_cast<int64_t>(p.n_vt) * p.n_nt;
   const int grid = static_cast<int>(units < h->num_sms ? units : h->num_sms);
+  CUtensorMap tmL = tmH;   // the pair kernel's logits map; not read unless valid
+  if (wide) p.tma_logits = encode_logits(&tmL, logits, h->V, B, false) ? 1 : 0;
   if (h->t_start) cudaEventRecord(h->t_start, stream);
   cudaError_t e;
   if constexpr (rows) {
     e = launch_rows_kernel(h, tmH, p, units, smem, stream);
   } else if constexpr (MODE == MODE_GREEDY) {
     if (wide)
-      e = launch_pair_kernel<MODE_GREEDY>(h, h->tmW, tmH, p, units, smem, stream);
+      e = launch_pair_kernel<MODE_GREEDY>(h, h->tmW, tmH, tmL, p, units, smem, stream);
     else
       e = launch_gemm<MODE>(h->tmW, tmH, p, grid, smem, stream);
   } else {
@@ -718,8 +735,10 @@ int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token
   p.v_off = static_cast<int32_t>(h->v_off);
   const size_t smem = pair_layout(p.stages).total + 1024;
   const int64_t units = static_cast<int64_t>((p.n_vt + 1) / 2) * p.n_nt;
+  CUtensorMap tmL = tmH;   // not read unless the logits map is valid
+  p.tma_logits = encode_logits(&tmL, logits, h->V, B, true) ? 1 : 0;
   if (h->t_start) cudaEventRecord(h->t_start, stream);
-  e = launch_pair_kernel<MODE_INT>(h, h->tmW16, tmH, p, units, smem, stream);
+  e = launch_pair_kernel<MODE_INT>(h, h->tmW16, tmH, tmL, p, units, smem, stream);
   if (h->t_stop) {
     cudaEventRecord(h->t_stop, stream);
     h->t_start = h->t_stop = nullptr;

@@ -116,6 +116,7 @@ struct HeadParams {
   union {
     int32_t round_fp16;       // gated: 1 rounds logits to fp16, 0 to bf16
     float temperature;        // sample: T > 0
+    int32_t tma_logits;       // pair kernel: 1 = logits leave through the logits tensor map
   };
   int32_t v_off;            // vocabulary index of this head's first W row
 };

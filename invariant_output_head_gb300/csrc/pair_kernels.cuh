@@ -1,29 +1,31 @@
 // pair_kernels.cuh -- the wide greedy projection (more than 128 hidden rows)
-// on CTA pairs, with W on the tensor core's M axis.
+// on CTA pairs.
 //
 // Kernel 1c (head_pair_kernel): the same logits as head_gemm_kernel -- the
 // same K chunks, the same fp32 round-to-nearest (integer head: int32) fold
 // of the chunk sums -- computed by clusters of two CTAs with
-// tcgen05.mma.cta_group::2. A unit is 256 vocabulary rows (two 128-row tiles,
-// one per CTA; the MMA's M axis) x 256 hidden rows (N). Each CTA loads its own
-// W tile box and its own half of the hidden-row box (128 of the 256 rows) per
-// 64-element K step: 32 KB of shared memory written per CTA and step instead
-// of the 48 KB a one-CTA 128 x 256 unit needs, and the tensor core reads half
-// of B from each CTA. On GB300 the one-CTA kernel at N = 256 is bound by
+// tcgen05.mma.cta_group::2. A unit is 256 vocabulary rows x 256 hidden rows.
+// Per 64-element K step each CTA loads 128 hidden rows (its half of the MMA's
+// M = 256 operand) and 128 vocabulary rows (its half of the N = 256
+// operand): 32 KB of shared memory written per CTA and step instead of the
+// 48 KB a one-CTA 128 x 256 unit needs, and the tensor core reads half of the
+// N operand from each CTA. On GB300 the one-CTA kernel at N = 256 is bound by
 // shared-memory bandwidth (its TMA fill plus the MMA's operand reads run near
 // 100 bytes per clock per SM, and the 128 x 256 x 16 MMAs take ~112 ns
 // instead of 65), which the pair layout relieves.
 //
-// Each CTA finds its 128 vocabulary rows x 256 hidden-row columns of the
-// product in its own tensor memory (lane = vocabulary row), so the epilogue
-// is head_gemm_kernel's: fp32 logits stored with a warp's lanes on
-// consecutive vocabulary entries (128-byte coalesced stores), then per
-// 16-column block a shared-memory transpose fold, the four lane quarters
-// merged in a fixed order, one record per (hidden row, 128-row tile). The
-// tensor core's result for an element depends neither on the operand roles
-// nor on the pair mode (checked bit for bit on GB300 with standalone
-// probes), so the logits are head_gemm_kernel's bit for bit, and the greedy
-// record is exact.
+// Here the hidden rows are the MMA's M axis: tensor-memory lane = hidden row,
+// column = vocabulary row. Each epilogue thread therefore owns one hidden row
+// and 128 consecutive vocabulary entries (one 128-row tile of W), and folds
+// its tile record (max, lowest index, runner-up) in registers, in ascending
+// vocabulary order, with no exchange between threads; the per-unit work after
+// the last chunk is short enough to run while the MMA fills both accumulator
+// slots with the next unit's first chunks. fp32 logits leave through a small
+// per-warp transpose in shared memory, so that a warp's stores cover whole
+// 64-byte runs of a hidden row's logits. The tensor core's result for an
+// element depends neither on the operand roles nor on the pair mode (checked
+// bit for bit on GB300 with standalone probes), so the logits are
+// head_gemm_kernel's bit for bit, and the greedy record is exact.
 //
 // The pair protocol is the log-prob kernel's (rows_kernels.cuh): the leader
 // issues every MMA; both producers' loads complete on the leader's stage
@@ -41,35 +43,42 @@ constexpr int kPairMaxStages = 7;
 constexpr int kPairN = 256;         // hidden rows per unit (MMA N)
 constexpr int kPairWarps = 8;       // epilogue warps 4 .. 11, 128 columns each
 
+// Logits staging: per epilogue warp two buffers of 32 hidden rows x 16
+// logits (64-byte rows, 64-byte swizzle: 16-byte chunk c of row r sits at
+// chunk c ^ ((r >> 1) & 3), so a warp's row-per-lane writes and the 8-row
+// reads below are both free of bank conflicts).
+constexpr uint32_t kPairStageBuf = 32 * 16 * 4;
+constexpr uint32_t kPairXsBytes = 2 * kPairStageBuf;
+
 struct PairLayout {
-  uint32_t a_bytes, b_bytes, stage_bytes, ctrl_off, red_off, xp_off, total;
+  uint32_t a_bytes, b_bytes, stage_bytes, ctrl_off, xs_off, total;
 };
 
-// Stage s: this CTA's W tile box [128 rows x 128 B] (operand A) then its half
-// of the hidden-row box [128 rows x 128 B] (operand B), both 128-byte
-// swizzled; then the barriers, the per-quarter column results (3 words x 4
-// quarters x 256 columns) and the epilogue warps' transpose areas.
+// Stage s: this CTA's 128 hidden rows [128 rows x 128 B] (operand A) then its
+// 128 vocabulary rows [128 rows x 128 B] (its half of operand B), both
+// 128-byte swizzled; then the barriers and the epilogue warps' logits
+// staging buffers (1024-byte aligned: the swizzle pattern repeats every 512
+// bytes).
 __host__ __device__ inline PairLayout pair_layout(int stages) {
   PairLayout L;
-  L.a_bytes = kBM * kRowBytes;
-  L.b_bytes = kRowsHalf * kRowBytes;
+  L.a_bytes = kRowsHalf * kRowBytes;
+  L.b_bytes = kBM * kRowBytes;
   L.stage_bytes = L.a_bytes + L.b_bytes;
   L.ctrl_off = static_cast<uint32_t>(stages) * L.stage_bytes;
   // full[S], empty[S], slot_full[2], slot_empty[2], never, drain; then the
   // TMEM address holder and the abort flag
-  L.red_off = L.ctrl_off + (2u * stages + 6u) * 8u + 16u;
-  L.xp_off = L.red_off + 3u * 4u * kPairN * 4u;
-  L.total = L.xp_off + kPairWarps * kXpWords * 4u;
+  L.xs_off = (L.ctrl_off + (2u * stages + 6u) * 8u + 16u + 1023u) & ~1023u;
+  L.total = L.xs_off + kPairWarps * kPairXsBytes;
   return L;
 }
 
 // p.n_vt: 128-row vocabulary tiles (the records' tiles); a unit covers tiles
 // 2 vp and 2 vp + 1 (the second may lie past V: its rows read as zeros and
-// it writes nothing). p.n_nt: 256-row hidden tiles.
+// no record of it is written). p.n_nt: 256-row hidden tiles.
 template <int MODE>
 __global__ void __launch_bounds__(kPairThreads, 1)
 head_pair_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
-                 const HeadParams p) {
+                 const __grid_constant__ CUtensorMap tmL, const HeadParams p) {
   static_assert(MODE == MODE_GREEDY || MODE == MODE_INT, "mode");
   constexpr int N = kPairN;
   constexpr int WBLK = 8;                          // 16-column blocks per epilogue warp
@@ -95,10 +104,7 @@ head_pair_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 5);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.ctrl_off + (2 * S + 6) * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  float* red_m = reinterpret_cast<float*>(smem + L.red_off);
-  int32_t* red_i = reinterpret_cast<int32_t*>(red_m + 4 * N);
-  float* red_s = reinterpret_cast<float*>(red_i + 4 * N);
-  float* xpose = reinterpret_cast<float*>(smem + L.xp_off);
+  uint8_t* xsall = smem + L.xs_off;
   const uint32_t smem_base = smem_u32(smem);
   auto sA = [&](int s) { return smem_base + static_cast<uint32_t>(s) * L.stage_bytes; };
   auto sB = [&](int s) { return sA(s) + L.a_bytes; };
@@ -120,6 +126,7 @@ head_pair_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmH);
+    if (p.tma_logits) tma_prefetch_desc(&tmL);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_holder), 512u);
@@ -153,7 +160,7 @@ head_pair_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         const int u = pair + (j / spu) * n_pairs;
         const int vp = u / p.n_nt, kb = j - (j / spu) * spu;
         if (leader) mbar_expect_tx(full_bar(j), 2u * L.stage_bytes);
-        tma_load_2d_pair(sA(j), &tmW, kb * kElems, vp * (2 * kBM) + half,
+        tma_load_2d_pair(sB(j), &tmW, kb * kElems, vp * (2 * kBM) + half,
                          cluster_addr(full_bar(j), 0), pol_w);
       }
       grid_dep_wait();
@@ -165,13 +172,13 @@ head_pair_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         for (int kb = 0; kb < spu; ++kb, ++j) {
           const uint32_t fb = cluster_addr(full_bar(stage), 0);
           if (j < pre) {
-            tma_load_2d_pair(sB(stage), &tmH, kb * kElems, nt * N + half, fb, pol_h);
+            tma_load_2d_pair(sA(stage), &tmH, kb * kElems, nt * N + half, fb, pol_h);
             if (leader) mbar_arrive(full_bar(stage));
           } else {
             if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns)) { ok = false; break; }
             if (leader) mbar_arrive_expect_tx(full_bar(stage), 2u * L.stage_bytes);
-            tma_load_2d_pair(sA(stage), &tmW, kb * kElems, vp * (2 * kBM) + half, fb, pol_w);
-            tma_load_2d_pair(sB(stage), &tmH, kb * kElems, nt * N + half, fb, pol_h);
+            tma_load_2d_pair(sB(stage), &tmW, kb * kElems, vp * (2 * kBM) + half, fb, pol_w);
+            tma_load_2d_pair(sA(stage), &tmH, kb * kElems, nt * N + half, fb, pol_h);
           }
           outstanding |= 1u << stage;
           out_par = (out_par & ~(1u << stage)) | (phase << stage);
@@ -242,12 +249,16 @@ head_pair_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     // --------------------------------------------------------- epilogue
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(kRegsEpiWide));
     grid_dep_wait();          // outputs and records: only after the previous kernels
-    const int q = warp & 3;                    // TMEM lane quarter
-    const int g = (warp - 4) >> 2;             // column half (hidden rows 128 g ..)
+    const int q = warp & 3;                    // TMEM lane quarter: hidden rows 32 q ..
+    const int g = (warp - 4) >> 2;             // column half: the unit's tile 2 vp + g
     const int et = threadIdx.x - 128;          // 0 .. ET-1
-    const int row = q * 32 + lane;             // vocabulary row within this CTA's tile
     const uint32_t tlane = static_cast<uint32_t>(q * 32) << 16;
-    float* xp = xpose + (warp - 4) * kXpWords;
+    uint8_t* xs = xsall + (warp - 4) * kPairXsBytes;
+    const uint32_t xs_u32 = smem_u32(xs);
+    const bool tma_lg = p.tma_logits != 0;
+    // without the tensor map (rows not 16-byte aligned): plain stores
+    const bool vec = (p.V & 3) == 0 && (reinterpret_cast<uintptr_t>(p.logits) & 15u) == 0;
+    uint32_t nbuf = 0;                         // staging buffers used so far
     uint32_t slot = 0, sph = 0;
     bool failed = false;
     using Acc = typename std::conditional<MODE == MODE_INT, int32_t, float>::type;
@@ -306,81 +317,123 @@ head_pair_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         if (et == 0) { *abort_flag = 1; atomicOr(p.err, ERR_TIMEOUT); }
         break;
       }
-      const int tile = 2 * vp + static_cast<int>(rank);   // this CTA's 128-row tile
-      const bool tile_ok = tile < p.n_vt;
-      const int v = tile * kBM + row;
-      const bool vok = tile_ok && v < p.V;
-      const int n0 = nt * N;
-      const int vg0 = p.v_off + tile * kBM + q * 32;      // vocabulary index of this warp's row 0
+      const int tile = 2 * vp + g;                     // this warp's 128-row vocabulary tile
+      const int vt0 = tile * kBM;                      // its first vocabulary row (this head)
+      const int lim = p.V - vt0;                       // its rows below V (<= 0: none)
+      const int nw0 = nt * N + static_cast<int>(rank) * kRowsHalf + q * 32;   // warp's row 0
+      const int n = nw0 + lane;                        // this thread's hidden row
+      if (p.logits != nullptr && lim > 0) {
+        // per 16-column block the warp's 32 rows x 16 logits go to a staging
+        // buffer (row = lane); the tensor map's store (clipped at B and V)
+        // then runs asynchronously while the warp drains the next unit, or,
+        // without it, each store instruction writes 8 rows x 64 bytes
+        const int rl = lane & 7, cc = lane >> 3;
 #pragma unroll
-      for (int bb = 0; bb < WBLK; ++bb) {
-        const int c0 = (g * WBLK + bb) * 16;
-        if (p.logits != nullptr && vok) {
-          Acc* lg = reinterpret_cast<Acc*>(p.logits);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int n = n0 + c0 + i;
-            if (n < p.B) lg[static_cast<size_t>(n) * p.V + v] = acc[bb][i];
+        for (int bb = 0; bb < WBLK; ++bb) {
+          // blocks wholly past V or B store nothing (warp-uniform)
+          if (vt0 + bb * 16 >= p.V || nw0 >= p.B) continue;
+          const uint32_t buf = nbuf & 1u;
+          if (tma_lg && nbuf >= 2) {
+            if (lane == 0) bulk_wait_group_read<1>();   // this buffer's previous store has read it
+            __syncwarp();
           }
-        }
-        if constexpr (MODE == MODE_INT) {
-          int32_t* xpi = reinterpret_cast<int32_t*>(xp);
+          uint8_t* sb = xs + buf * kPairStageBuf;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) xpi[lane * kXpStride + i] = vok ? acc[bb][i] : INT32_MIN;
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) xp[lane * kXpStride + i] = vok ? acc[bb][i] : -INFINITY;
-        }
-        __syncwarp();
-        if constexpr (MODE == MODE_INT) {
-          const ITop2 t = xp_itop2(reinterpret_cast<const int32_t*>(xp), lane, vg0);
-          if (lane < 16) {
-            reinterpret_cast<int32_t*>(red_m)[q * N + c0 + lane] = t.m;
-            red_i[q * N + c0 + lane] = t.i;
-            reinterpret_cast<int32_t*>(red_s)[q * N + c0 + lane] = t.s;
+          for (int k = 0; k < 4; ++k) {
+            uint4 w;
+            if constexpr (MODE == MODE_INT) {
+              w = make_uint4(acc[bb][4 * k], acc[bb][4 * k + 1], acc[bb][4 * k + 2], acc[bb][4 * k + 3]);
+            } else {
+              w = make_uint4(__float_as_uint(acc[bb][4 * k]), __float_as_uint(acc[bb][4 * k + 1]),
+                             __float_as_uint(acc[bb][4 * k + 2]), __float_as_uint(acc[bb][4 * k + 3]));
+            }
+            *reinterpret_cast<uint4*>(sb + lane * 64 + 16 * (k ^ ((lane >> 1) & 3))) = w;
           }
-        } else {
-          const Top2 t = xp_top2(xp, lane, vg0);
-          if (lane < 16) {
-            red_m[q * N + c0 + lane] = t.m;
-            red_i[q * N + c0 + lane] = t.i;
-            red_s[q * N + c0 + lane] = t.s;
-          }
-        }
-        __syncwarp();
-      }
-      named_bar_sync(1, ET);
-      // fixed combination of the four 32-row quarters: (q0 . q1) . (q2 . q3)
-      if (tile_ok) {
-        for (int c = et; c < N; c += ET) {
-          const int n = n0 + c;
-          if (n >= p.B) continue;
-          const size_t o = static_cast<size_t>(n) * p.n_vt + tile;   // records [B][n_vt]
-          if constexpr (MODE == MODE_INT) {
-            const int32_t* rm = reinterpret_cast<const int32_t*>(red_m);
-            const int32_t* rs = reinterpret_cast<const int32_t*>(red_s);
-            ITop2 t[4];
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) t[qq] = ITop2{rm[qq * N + c], red_i[qq * N + c], rs[qq * N + c]};
-            const ITop2 r = itop2_merge(itop2_merge(t[0], t[1]), itop2_merge(t[2], t[3]));
-            reinterpret_cast<int32_t*>(p.rec_m)[o] = r.m;
-            p.rec_i[o] = r.i;
-            reinterpret_cast<int32_t*>(p.rec_s)[o] = r.s;
+          if (tma_lg) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmL, xs_u32 + buf * kPairStageBuf, vt0 + bb * 16, nw0);
+              bulk_commit_group();
+            }
+            ++nbuf;
           } else {
-            Top2 t[4];
+            __syncwarp();
+            uint32_t* lg = reinterpret_cast<uint32_t*>(p.logits);
+            const int v = vt0 + bb * 16 + 4 * cc;        // first of this lane's four columns
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq)
-              t[qq] = Top2{red_m[qq * N + c], red_i[qq * N + c], red_s[qq * N + c]};
-            const Top2 r = top2_merge(top2_merge(t[0], t[1]), top2_merge(t[2], t[3]));
-            p.rec_m[o] = r.m;
-            p.rec_i[o] = r.i;
-            p.rec_s[o] = r.s;
+            for (int r8 = 0; r8 < 4; ++r8) {
+              const int r = r8 * 8 + rl;
+              const uint4 w =
+                  *reinterpret_cast<const uint4*>(sb + r * 64 + 16 * (cc ^ ((r >> 1) & 3)));
+              const int nr = nw0 + r;
+              if (nr < p.B) {
+                uint32_t* dst = lg + static_cast<size_t>(nr) * p.V + v;
+                if (vec && v + 3 < p.V) {
+                  *reinterpret_cast<uint4*>(dst) = w;
+                } else {
+                  if (v < p.V) dst[0] = w.x;
+                  if (v + 1 < p.V) dst[1] = w.y;
+                  if (v + 2 < p.V) dst[2] = w.z;
+                  if (v + 3 < p.V) dst[3] = w.w;
+                }
+              }
+            }
+            __syncwarp();
           }
         }
       }
-      named_bar_sync(1, ET);
+      if (lim > 0 && n < p.B) {
+        // this row's record of the tile: ascending vocabulary order, a strict
+        // comparison keeps the lowest index of the maximum; rows at or past V
+        // (only in the last tile) count as -inf / INT32_MIN
+        const int vg0 = p.v_off + vt0;
+        const size_t o = static_cast<size_t>(n) * p.n_vt + tile;   // records [B][n_vt]
+        auto fold = [&](auto ragged) {
+          constexpr bool kRagged = decltype(ragged)::value;
+          if constexpr (MODE == MODE_INT) {
+            ITop2 t{INT32_MIN, INT32_MAX, INT32_MIN};
+#pragma unroll
+            for (int bb = 0; bb < WBLK; ++bb)
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int j = bb * 16 + i;
+                const int32_t x = (!kRagged || j < lim) ? acc[bb][i] : INT32_MIN;
+                const bool gt = x > t.m;
+                t.s = gt ? t.m : max(t.s, x);
+                t.i = gt ? vg0 + j : t.i;
+                t.m = gt ? x : t.m;
+              }
+            reinterpret_cast<int32_t*>(p.rec_m)[o] = t.m;
+            p.rec_i[o] = t.i;
+            reinterpret_cast<int32_t*>(p.rec_s)[o] = t.s;
+          } else {
+            Top2 t{-INFINITY, INT32_MAX, -INFINITY};
+#pragma unroll
+            for (int bb = 0; bb < WBLK; ++bb)
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int j = bb * 16 + i;
+                const float x = (!kRagged || j < lim) ? acc[bb][i] : -INFINITY;
+                const bool gt = x > t.m;
+                t.s = gt ? t.m : fmaxf(t.s, x);
+                t.i = gt ? vg0 + j : t.i;
+                t.m = gt ? x : t.m;
+              }
+            p.rec_m[o] = t.m;
+            p.rec_i[o] = t.i;
+            p.rec_s[o] = t.s;
+          }
+        };
+        if (lim >= kBM) fold(std::false_type{});
+        else fold(std::true_type{});
+      }
     }
     if (failed && et == 0) atomicOr(p.err, ERR_TIMEOUT);
+    // the logits stores are complete before the CTA (and its shared memory)
+    // goes away
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
   }
 
   // neither CTA leaves (or frees its tensor memory) before the leader's MMAs
