@@ -616,6 +616,16 @@ def run_ours(args, rank, world, local_rank):
                      "hbm_achieved_gbs": round(hbm_achieved, 1),
                      "hbm_frac_of_measured": round(hbm_achieved / peaks["hbm_gbs"], 4),
                      "hbm_frac_of_spec_8tbs": round(hbm_achieved / spec_hbm, 4),
+                     # the launch's lower bounds: its algorithmic bytes at the
+                     # measured copy bandwidth, its flops at the burst tensor
+                     # peak; the larger one is the binding roofline
+                     "roofline_us": {"hbm": round(by_launch / (peaks["hbm_gbs"] * 1e9) * 1e6, 2),
+                                     "tensor": round(fl_launch / (peaks["bf16_tflops"] * 1e12) * 1e6, 2)},
+                     "binding": "hbm" if by_launch / peaks["hbm_gbs"] >= fl_launch / (peaks["bf16_tflops"] * 1e3)
+                                else "tensor",
+                     "frac_of_binding_roofline": round(
+                         max(by_launch / (peaks["hbm_gbs"] * 1e9),
+                             fl_launch / (peaks["bf16_tflops"] * 1e12)) / kernel_s, 4),
                      "steady_us_per_call": round(steady_call_s * 1e6, 2),
                      "steady_frac": round(steady_frac, 4),
                      "note": "achieved/frac: the projection kernel alone, median over a "

@@ -366,11 +366,19 @@ int pair_stages() {
 }
 
 // The pair kernel's logits tensor map: [B][V] 4-byte elements, box 16 x 32
-// (a warp's staging buffer), 64-byte swizzle. Needs 16-byte aligned rows:
-// V a multiple of 4 and a 16-byte aligned base; otherwise the kernel stores
+// (a warp's staging buffer), 64-byte swizzle. Used for logits in device
+// memory with 16-byte aligned rows (V a multiple of 4, a 16-byte aligned
+// base); otherwise (host memory the kernel writes through its mapping, such
+// as the asynchronous host-buffer calls' pinned buffers) the kernel stores
 // the logits with plain stores (returns false).
 bool encode_logits(CUtensorMap* m, const void* logits, int64_t V, int64_t B, bool int32) {
   if (logits == nullptr || (V & 3) != 0 || !aligned(logits, 16)) return false;
+  cudaPointerAttributes pa;
+  if (cudaPointerGetAttributes(&pa, logits) != cudaSuccess) {
+    cudaGetLastError();   // clear the error the query recorded
+    return false;
+  }
+  if (pa.type != cudaMemoryTypeDevice) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(B)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(V) * 4u};
   cuuint32_t box[2] = {16u, 32u};

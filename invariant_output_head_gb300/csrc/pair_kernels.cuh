@@ -218,6 +218,8 @@ head_pair_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
           for (int sc = 0; sc < kBlocksPerChunk; ++sc) {
             const int kb = c * kBlocksPerChunk + sc;
             if (kb >= p.nk) break;
+            // each stage's MMAs go out as soon as its loads have landed
+            // (waiting for both stages of a chunk first measured slower)
             if (!mbar_wait(full_bar(stage), phase, abort_flag, p.timeout_ns)) { ok = false; break; }
             tc_fence_after();
             const uint64_t da = sdesc_sw128(sA(stage));

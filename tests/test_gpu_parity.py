@@ -243,3 +243,49 @@ def test_verify_accept_call_sequence(torch_cuda):
         head.greedy(h[:7])
         assert (host(acc) == oracle.verify_accept(t_ref[:n].reshape(R, P), drafts)).all(), (R, P)
     assert head.check() == 0
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "int8"])
+def test_pair_kernel_logits_store_paths(torch_cuda, fmt):
+    """Calls of more than 128 rows run on the CTA-pair kernel, whose logits go
+    out through a tensor map when they are device memory with 16-byte aligned
+    rows, and through plain stores otherwise (an unaligned logits pointer,
+    pinned host memory written through its mapping). Every path gives the
+    same bits, equal to the oracle's integer logits for the int8 head."""
+    from invariant_output_head_gb300 import Head, binding
+    torch = torch_cuda
+    V, d, B = 1000, 256, 300 if fmt == "int8" else 200
+    if fmt == "int8":
+        case = synth.small_int8(611, V, d, B, n_ties=2)
+    else:
+        case = synth.small_float(611, V, d, B, fmt=fmt, n_ties=2)
+    head = Head(dev(case["W"], fmt), fmt)
+    h = dev(case["h"], fmt)
+    tok, gap, z = (host(x) for x in head.greedy(h, with_logits=True))
+    assert head.check() == 0
+    s = torch.cuda.current_stream().cuda_stream
+    # device logits starting 4 bytes into a buffer: rows not 16-byte aligned
+    buf = torch.zeros(B * V + 1, dtype=torch.int32, device="cuda")
+    tk = torch.empty(B, dtype=torch.int32, device="cuda")
+    gp = torch.empty(B, dtype=torch.int32 if fmt == "int8" else torch.float32, device="cuda")
+    binding.detlm_head_greedy(head.handle, h.data_ptr(), B, tk.data_ptr(), gp.data_ptr(),
+                              buf.data_ptr() + 4, s)
+    assert head.check() == 0
+    zu = host(buf)[1:].reshape(B, V).view(z.dtype)
+    assert (zu.view(np.uint32) == z.view(np.uint32)).all()
+    assert (host(tk) == tok).all()
+    # pinned host result buffers, written by the kernels directly
+    h_pin = torch.from_numpy(np.ascontiguousarray(case["h"]).view(
+        np.int8 if fmt == "int8" else np.int16)).pin_memory()
+    o_tok = torch.empty(B, dtype=torch.int32).pin_memory()
+    o_gap = torch.empty(B, dtype=gp.dtype).pin_memory()
+    o_log = torch.empty((B, V), dtype=torch.int32 if fmt == "int8" else torch.float32).pin_memory()
+    binding.detlm_head_greedy_host_async(head.handle, h_pin.data_ptr(), B, o_tok.data_ptr(),
+                                         o_gap.data_ptr(), o_log.data_ptr(), s)
+    assert head.check() == 0
+    assert (o_log.numpy().view(np.uint32) == z.view(np.uint32)).all()
+    assert (o_tok.numpy() == tok).all()
+    assert (o_gap.numpy().view(np.uint32) == gap.view(np.uint32)).all()
+    if fmt == "int8":
+        assert (z.astype(np.int64) == oracle.logits_int(case["W"], case["h"])).all()
+    head.close()
