@@ -148,11 +148,13 @@ def projection_kernel(workload: str, batch: int) -> str:
     rows; the one-CTA kernel otherwise (and for the gated and sampling
     calls)."""
     spec = WORKLOADS[workload]
-    rows = spec.get("B", batch)
     if spec["fmt"] == "int8":
         return "int8_gemm_kernel" if batch < 256 else "head_pair_kernel"
     if spec["mode"] == "logprob":
         return "head_rows_kernel"
+    # --batch sets the integer workloads' rows only; the decode workloads make
+    # calls of one row (the sweep: at most 64)
+    rows = spec.get("B", 1)
     if spec["mode"] in ("greedy", "verify") and rows > 128:
         return "head_pair_kernel"
     return "head_gemm_kernel"

@@ -148,7 +148,10 @@ head_pair_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     // ------------------------------------------------------ TMA producer
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegsWg0Wide));
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
+      // W streams through once (evict first) unless several hidden-row tiles
+      // share each W tile: their units run on neighbouring pairs at about
+      // the same time, and the second reads it from L2
+      const uint64_t pol_w = p.n_nt > 1 ? policy_evict_normal() : policy_evict_first();
       const uint64_t pol_h = policy_evict_last();
       const bool leader = rank == 0;
       // W is read-only for the head's life: the W boxes of the first S

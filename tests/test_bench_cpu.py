@@ -8,6 +8,8 @@ import bench
 
 def test_projection_kernel_per_workload():
     assert bench.projection_kernel("pr1", 1) == "head_gemm_kernel"
+    assert bench.projection_kernel("pr1", 512) == "head_gemm_kernel"     # --batch: int8 only
+    assert bench.projection_kernel("sweep", 512) == "head_gemm_kernel"
     assert bench.projection_kernel("spec", 256) == "head_pair_kernel"
     assert bench.projection_kernel("verify", 256) == "head_pair_kernel"
     assert bench.projection_kernel("gated", 1) == "head_gemm_kernel"

@@ -69,6 +69,35 @@ def test_stalled_logprob_pair_kernel_times_out_and_recovers(env):
     assert (np.abs(lp.astype(np.float64) - lp_ref) <= tol).all()
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "int8"])
+def test_stalled_wide_greedy_pair_kernel_times_out_and_recovers(env, fmt):
+    """Greedy calls of more than 128 rows (integer: 256 or more) run on CTA
+    pairs: the stalled leader's MMA warp gives up, both CTAs' waits run out,
+    the loads already issued land before either CTA leaves, and the next
+    call (logits through the tensor-map stores) is right."""
+    torch, b = env
+    B = 300
+    if fmt == "int8":
+        case = synth.small_int8(6, 1000, 256, B)
+    else:
+        case = synth.small_float(6, 1000, 256, B)
+    head = b.Head(dev(case["W"], fmt), fmt)
+    h = dev(case["h"], fmt)
+    b.detlm_head_debug(head.handle, b.DETLM_DEBUG_STALL, 20_000_000)
+    head.greedy(h, with_logits=True)
+    torch.cuda.synchronize()
+    assert head.check() == b.DETLM_ETIMEOUT
+    b.detlm_head_debug(head.handle, 0, 0)
+    t, g, z = head.greedy(h, with_logits=True)
+    assert head.check() == b.DETLM_OK
+    if fmt == "int8":
+        assert (host(z).astype(np.int64) == oracle.logits_int(case["W"], case["h"])).all()
+    else:
+        z_ref, A = oracle_float_rows(case["W"], case["h"][:32], fmt)
+        check_float_greedy(z_ref, A, host(t)[:32], host(g)[:32], host(z)[:32], label="pair stall")
+    head.close()
+
+
 def test_out_of_range_target_gives_nan_and_status(env):
     torch, b = env
     case = synth.small_float(4, 500, 128, 6)
