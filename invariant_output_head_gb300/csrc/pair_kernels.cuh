@@ -297,17 +297,22 @@ head_pair_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
               // 1.5 * 2^23 is exact and leaves the integer in the low
               // mantissa bits; int32 fold
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int32_t x =
-                    __float_as_int(__fadd_rn(__uint_as_float(rr[b4][i]), 12582912.0f)) - 0x4B400000;
-                acc[bb][i] = (c == 0) ? x : acc[bb][i] + x;
+              for (int i = 0; i < 16; i += 2) {
+                float f0 = __uint_as_float(rr[b4][i]), f1 = __uint_as_float(rr[b4][i + 1]);
+                add2_rn(f0, f1, 12582912.0f, 12582912.0f);
+                const int32_t x0 = __float_as_int(f0) - 0x4B400000;
+                const int32_t x1 = __float_as_int(f1) - 0x4B400000;
+                acc[bb][i] = (c == 0) ? x0 : acc[bb][i] + x0;
+                acc[bb][i + 1] = (c == 0) ? x1 : acc[bb][i + 1] + x1;
               }
             } else if (c == 0) {
 #pragma unroll
               for (int i = 0; i < 16; ++i) acc[bb][i] = __uint_as_float(rr[b4][i]);
             } else {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) acc[bb][i] = __fadd_rn(acc[bb][i], __uint_as_float(rr[b4][i]));
+              for (int i = 0; i < 16; i += 2)
+                add2_rn(acc[bb][i], acc[bb][i + 1], __uint_as_float(rr[b4][i]),
+                        __uint_as_float(rr[b4][i + 1]));
             }
           }
         }

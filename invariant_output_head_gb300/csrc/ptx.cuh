@@ -278,6 +278,18 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask)
       :: "r"(bar), "h"(cta_mask) : "memory");
 }
 
+// Two independent fp32 additions a0 += b0, a1 += b1, each rounded to
+// nearest even: one packed instruction on this GPU, the same bits as two
+// add.rn.f32 (the tensor-memory drains issue half as many adds).
+__device__ __forceinline__ void add2_rn(float& a0, float& a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 x, y;\n\t"
+      "mov.b64 x, {%0, %1};\n\t"
+      "mov.b64 y, {%2, %3};\n\t"
+      "add.rn.f32x2 x, x, y;\n\t"
+      "mov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1));
+}
+
 // 2^x by the special-function unit (ex2.approx.ftz: relative error about
 // 2^-22, results below 2^-126 flushed to zero).
 __device__ __forceinline__ float exp2_approx(float x) {

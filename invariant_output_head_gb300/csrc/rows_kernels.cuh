@@ -279,7 +279,9 @@ head_rows_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                 for (int i = 0; i < 16; ++i) acc[bb][i] = __uint_as_float(rr[b4][i]);
               } else {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[bb][i] = __fadd_rn(acc[bb][i], __uint_as_float(rr[b4][i]));
+                for (int i = 0; i < 16; i += 2)
+                  add2_rn(acc[bb][i], acc[bb][i + 1], __uint_as_float(rr[b4][i]),
+                          __uint_as_float(rr[b4][i + 1]));
               }
             }
           }
