@@ -484,8 +484,8 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   // folded per row, in a fixed order, whatever B is)
   constexpr bool rows = MODE == MODE_LOGPROB;
   const int N = rows ? kRowsN : cols_for(B);
-  // greedy calls of more than 128 rows: the pair kernel (W on the MMA's M
-  // axis over two CTAs; the same logits bit for bit)
+  // greedy calls of more than 128 rows: the pair kernel (CTA pairs, hidden
+  // rows on the MMA's M axis; the same logits bit for bit)
   const bool wide = MODE == MODE_GREEDY && N == kPairN;
   CUtensorMap tmH;
   if (!encode_2d(&tmH, h->dtype, h_dev, h->d, B, (rows || wide) ? static_cast<uint32_t>(kRowsHalf)
@@ -709,8 +709,8 @@ int launch_int8_wide(detlm_head* h, const void* h_dev, int64_t B, int32_t* token
   if (sw != DETLM_OK) return sw;
   e = i8_to_f16(h_dev, h->h16, static_cast<size_t>(B) * h->d, stream);
   if (e != cudaSuccess) return status_from_cuda(e);
-  // the pair kernel (W on the MMA's M axis over two CTAs), as the float
-  // heads' calls of more than 128 rows
+  // the pair kernel (CTA pairs, hidden rows on the MMA's M axis), as the
+  // float heads' calls of more than 128 rows
   CUtensorMap tmH;
   if (!encode_2d(&tmH, DETLM_FP16, h->h16, h->d, B, static_cast<uint32_t>(kRowsHalf)))
     return DETLM_EINVAL;
