@@ -442,6 +442,8 @@ template <int MODE, int NBLK>
 __global__ void __launch_bounds__(threads_for(16 * NBLK), 1)
 head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                  const __grid_constant__ CUtensorMap tmH, const HeadParams p) {
+  static_assert(MODE == MODE_GREEDY || MODE == MODE_GATED || MODE == MODE_SAMPLE,
+                "log-prob runs on head_rows_kernel, the integer wide path on head_pair_kernel");
   constexpr int N = 16 * NBLK;
   constexpr int EW = epi_warps_for(N);          // epilogue warps
   constexpr int ET = 32 * EW;                   // epilogue threads
@@ -687,8 +689,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
     bool failed = false;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       const int vt = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
-      using Acc = typename std::conditional<MODE == MODE_INT, int32_t, float>::type;
-      Acc acc[WBLK][16];
+      float acc[WBLK][16];
       for (int c = 0; c < p.n_chunks; ++c) {
         const uint32_t cur = slot, cph = sph;
         if (++slot == static_cast<uint32_t>(p.n_slots)) { slot = 0; sph ^= 1u; }
@@ -700,26 +701,27 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
         tc_fence_after();
         const uint32_t sbase = tmem_base + tlane + cur * static_cast<uint32_t>(N) +
                                static_cast<uint32_t>(g * WBLK * 16);
+        // groups of up to four 16-column loads, one wait each; the chunk
+        // sums are added with packed round-to-nearest fp32 adds
+        constexpr int kG = WBLK < 4 ? WBLK : 4;
 #pragma unroll
-        for (int bb = 0; bb < WBLK; ++bb) {
-          uint32_t r[16];
-          tmem_ld16(sbase + bb * 16, r);
+        for (int b0 = 0; b0 < WBLK; b0 += kG) {
+          uint32_t r[kG][16];
+#pragma unroll
+          for (int k = 0; k < kG; ++k) tmem_ld16(sbase + (b0 + k) * 16, r[k]);
           tmem_wait_ld();
-          if constexpr (MODE == MODE_INT) {   // exact integer chunk sums, int32 fold
-            // |chunk sum| <= 128 * 2^14 = 2^21: adding 1.5 * 2^23 is exact and
-            // leaves the integer in the low mantissa bits (cheaper than cvt)
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int32_t x =
-                  __float_as_int(__fadd_rn(__uint_as_float(r[i]), 12582912.0f)) - 0x4B400000;
-              acc[bb][i] = (c == 0) ? x : acc[bb][i] + x;
+          for (int k = 0; k < kG; ++k) {
+            const int bb = b0 + k;
+            if (c == 0) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) acc[bb][i] = __uint_as_float(r[k][i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; i += 2)
+                add2_rn(acc[bb][i], acc[bb][i + 1], __uint_as_float(r[k][i]),
+                        __uint_as_float(r[k][i + 1]));
             }
-          } else if (c == 0) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) acc[bb][i] = __uint_as_float(r[i]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) acc[bb][i] = __fadd_rn(acc[bb][i], __uint_as_float(r[i]));
           }
         }
         tc_fence_before();   // slot fully read: hand it back to the MMA warp
@@ -752,18 +754,13 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       for (int bb = 0; bb < WBLK; ++bb) {
         const int c0 = (g * WBLK + bb) * 16;
         if (p.logits != nullptr && vok) {
-          Acc* lg = reinterpret_cast<Acc*>(p.logits);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int n = n0 + c0 + i;
-            if (n < p.B) lg[static_cast<size_t>(n) * p.V + v] = acc[bb][i];
+            if (n < p.B) p.logits[static_cast<size_t>(n) * p.V + v] = acc[bb][i];
           }
         }
-        if constexpr (MODE == MODE_INT) {
-          int32_t* xpi = reinterpret_cast<int32_t*>(xp);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) xpi[lane * kXpStride + i] = vok ? acc[bb][i] : INT32_MIN;
-        } else if constexpr (MODE == MODE_SAMPLE) {
+        if constexpr (MODE == MODE_SAMPLE) {
           // logits to this lane's transpose row first, then the scores in
           // place (a rolled loop: the noise is long code)
 #pragma unroll
@@ -783,14 +780,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
           for (int i = 0; i < 16; ++i) xp[lane * kXpStride + i] = vok ? acc[bb][i] : -INFINITY;
         }
         __syncwarp();
-        if constexpr (MODE == MODE_INT) {
-          const ITop2 t = xp_itop2(reinterpret_cast<const int32_t*>(xp), lane, vg0);
-          if (lane < 16) {
-            reinterpret_cast<int32_t*>(red_m)[q * N + c0 + lane] = t.m;
-            red_i[q * N + c0 + lane] = t.i;
-            reinterpret_cast<int32_t*>(red_s)[q * N + c0 + lane] = t.s;
-          }
-        } else if constexpr (MODE == MODE_GREEDY || MODE == MODE_SAMPLE) {
+        if constexpr (MODE == MODE_GREEDY || MODE == MODE_SAMPLE) {
           const Top2 t = xp_top2(xp, lane, vg0);
           if (lane < 16) {
             red_m[q * N + c0 + lane] = t.m;
@@ -816,17 +806,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
         const int n = n0 + c;
         if (n >= p.B) continue;
         const size_t o = static_cast<size_t>(n) * p.n_vt + vt;   // records [B][n_vt]
-        if constexpr (MODE == MODE_INT) {
-          const int32_t* rm = reinterpret_cast<const int32_t*>(red_m);
-          const int32_t* rs = reinterpret_cast<const int32_t*>(red_s);
-          ITop2 t[4];
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) t[qq] = ITop2{rm[qq * N + c], red_i[qq * N + c], rs[qq * N + c]};
-          const ITop2 r = itop2_merge(itop2_merge(t[0], t[1]), itop2_merge(t[2], t[3]));
-          reinterpret_cast<int32_t*>(p.rec_m)[o] = r.m;
-          p.rec_i[o] = r.i;
-          reinterpret_cast<int32_t*>(p.rec_s)[o] = r.s;
-        } else {
+        {
           Top2 t[4];
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq)
