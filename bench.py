@@ -43,6 +43,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import subprocess
 import sys
@@ -395,6 +396,46 @@ def workload_config(name, c, calls, world):
 
 # ------------------------------------------------------------------ our arm
 
+def graph_steady(torch, stream, step, k, n_calls, n_copies, steps, heads, snapshot, first):
+    """The step's calls captured once into a CUDA graph (as many steps as make
+    the rotation over the W copies repeat) and replayed: the steady state
+    without host launch costs. Returns per-call time and bit stability, or
+    the capture error."""
+    reps_per_graph = n_copies // math.gcd(n_calls, n_copies)
+    k[0] = 0                       # the captured calls start on the first copy
+    g = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(g):
+            cs = torch.cuda.current_stream().cuda_stream
+            for _ in range(reps_per_graph):
+                step(stream_ptr=cs)
+    except Exception as e:          # reported, not fatal: the eager figures stand
+        return {"error": f"{type(e).__name__}: {e}"[:300]}
+    g.replay()
+    torch.cuda.synchronize()
+    replays = max(1, -(-steps // reps_per_graph))
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(replays):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    for hd in heads:
+        assert hd.check() == 0, "device error in the graph replays"
+    last = snapshot()
+    stable = all(
+        all(torch.equal(x.view(torch.int32), y.view(torch.int32)) for x, y in zip(p, q))
+        if isinstance(p, tuple) else torch.equal(p.view(torch.int32), q.view(torch.int32))
+        for p, q in zip(first, last))
+    calls = replays * reps_per_graph * n_calls
+    return {"us_per_call": round(a.elapsed_time(b) * 1e3 / calls, 2),
+            "calls_per_graph": reps_per_graph * n_calls, "replays": replays,
+            "bit_stable": bool(stable),
+            "note": "one graph of the step's calls, replayed back to back; frac against "
+                    "the sustained peak for tensor-bound workloads"}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -452,11 +493,11 @@ def run_ours(args, rank, world, local_rank):
         seeds_d = torch.from_numpy(c["seeds"]).to(dev)
         pos_d = torch.from_numpy(c["positions"]).to(dev)
     stream = torch.cuda.current_stream(dev)
-    sp = stream.cuda_stream
     n_calls = len(calls)
     k = [0]
 
-    def step(ev=None):
+    def step(ev=None, stream_ptr=None):
+        sp = stream.cuda_stream if stream_ptr is None else stream_ptr
         for j, (r0, B) in enumerate(calls):
             hd = heads[k[0] % n_copies]
             k[0] += 1
@@ -551,6 +592,8 @@ def run_ours(args, rank, world, local_rank):
     for s in range(kl_steps):
         step(ev[s])
     torch.cuda.synchronize()
+    graph = graph_steady(torch, stream, step, k, n_calls, n_copies, args.steps, heads,
+                         snapshot, first)
     clocks = sampler.stop() if rank == 0 else None
     for hd in heads:
         assert hd.check() == 0, "device error in the kernel-timing loop"
@@ -644,6 +687,12 @@ def run_ours(args, rank, world, local_rank):
     }
     if by_B is not None:
         res["roofline"]["per_B"] = by_B
+    if "us_per_call" in graph:
+        graph["frac"] = round((by_launch / (graph["us_per_call"] * 1e-6) / 1e9 / peaks["hbm_gbs"])
+                              if spec["bound"] == "hbm" else
+                              (fl_launch / (graph["us_per_call"] * 1e-6) / 1e12
+                               / peaks["bf16_tflops_sustained"]), 4)
+    res["roofline"]["graph_replay"] = graph
     if fmt == "int8" and spec["bound"] == "tensor" and rank == 0:
         ip = instruction_peaks(dev, torch.cuda.get_device_properties(dev).multi_processor_count)
         if ip.get("mma_f16_dense_tflops"):
