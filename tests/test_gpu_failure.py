@@ -218,3 +218,32 @@ def test_reserved_workspace_and_tiles(env):
     t, g, _ = head.greedy(dev(case["h"], "bf16"))
     z_ref, A = oracle_float_rows(case["W"], case["h"], "bf16")
     check_float_greedy(z_ref, A, host(t), host(g), label="reserved")
+
+
+def test_async_host_calls_with_large_logits(env):
+    """Asynchronous host-buffer calls with several MB of logits written into
+    pinned buffers (by the pair kernel, through the host mapping): several
+    calls in a row, one check at the end, every result bitwise the device
+    call's."""
+    torch, b = env
+    V, d, B = 6000, 256, 200                # 4.8 MB of logits per call
+    case = synth.small_float(17, V, d, B)
+    head = b.Head(dev(case["W"], "bf16"), "bf16")
+    hd = dev(case["h"], "bf16")
+    t, g, z = (host(x) for x in head.greedy(hd, with_logits=True))
+    h_pin = torch.from_numpy(np.ascontiguousarray(case["h"]).view(np.int16)).pin_memory()
+    s = torch.cuda.current_stream().cuda_stream
+    outs = []
+    for k in range(4):
+        o = (torch.empty(B, dtype=torch.int32).pin_memory(),
+             torch.empty(B, dtype=torch.float32).pin_memory(),
+             torch.empty((B, V), dtype=torch.float32).pin_memory())
+        b.detlm_head_greedy_host_async(head.handle, h_pin.data_ptr(), B, o[0].data_ptr(),
+                                       o[1].data_ptr(), o[2].data_ptr(), s)
+        outs.append(o)
+    assert head.check() == 0
+    for o in outs:
+        assert (o[0].numpy() == t).all()
+        assert (o[1].numpy().view(np.uint32) == g.view(np.uint32)).all()
+        assert (o[2].numpy().view(np.uint32) == z.view(np.uint32)).all()
+    head.close()
