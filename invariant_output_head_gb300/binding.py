@@ -306,6 +306,12 @@ class Head:
             detlm_head_destroy(self.handle)
             self.handle = None
 
+    def reserve(self, max_B: int) -> None:
+        """Workspace (and, for an int8 head, the wide path's fp16 copies) for
+        calls of up to max_B rows: such calls then allocate nothing and can be
+        captured into a CUDA graph (detlm_head_reserve)."""
+        detlm_head_reserve(self.handle, int(max_B))
+
     def __del__(self):
         try:
             self.close()

@@ -48,7 +48,7 @@ def test_float_calls_replay_bitwise(torch_cuda):
     V, d = 1000, 256
     case = synth.small_float(900, V, d, 300)
     head = Head(dev(case["W"], "bf16"), "bf16")
-    binding.detlm_head_reserve(head.handle, 300)
+    head.reserve(300)
     h = dev(case["h"], "bf16")
     t = dev(case["targets"], "int32")
     outs = []
