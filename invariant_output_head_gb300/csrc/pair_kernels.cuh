@@ -281,24 +281,25 @@ head_pair_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         tc_fence_after();
         const uint32_t sbase = tmem_base + tlane + cur * static_cast<uint32_t>(N) +
                                static_cast<uint32_t>(g * WBLK * 16);
-        // two groups of four 16-column loads, one wait each (a wait per
+        // two groups of two 32-column loads, one wait each (a wait per
         // load leaves the drain latency-bound)
 #pragma unroll
         for (int h4 = 0; h4 < 2; ++h4) {
-          uint32_t rr[4][16];
+          uint32_t rw[2][32];
 #pragma unroll
-          for (int b4 = 0; b4 < 4; ++b4) tmem_ld16(sbase + (h4 * 4 + b4) * 16, rr[b4]);
+          for (int b2 = 0; b2 < 2; ++b2) tmem_ld32(sbase + (h4 * 2 + b2) * 32, rw[b2]);
           tmem_wait_ld();
 #pragma unroll
           for (int b4 = 0; b4 < 4; ++b4) {
             const int bb = h4 * 4 + b4;
+            const uint32_t* rr = &rw[b4 >> 1][(b4 & 1) * 16];   // this block's 16 columns
             if constexpr (MODE == MODE_INT) {
               // exact integer chunk sums (|sum| <= 128 * 2^14 = 2^21): adding
               // 1.5 * 2^23 is exact and leaves the integer in the low
               // mantissa bits; int32 fold
 #pragma unroll
               for (int i = 0; i < 16; i += 2) {
-                float f0 = __uint_as_float(rr[b4][i]), f1 = __uint_as_float(rr[b4][i + 1]);
+                float f0 = __uint_as_float(rr[i]), f1 = __uint_as_float(rr[i + 1]);
                 add2_rn(f0, f1, 12582912.0f, 12582912.0f);
                 const int32_t x0 = __float_as_int(f0) - 0x4B400000;
                 const int32_t x1 = __float_as_int(f1) - 0x4B400000;
@@ -307,12 +308,12 @@ head_pair_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
               }
             } else if (c == 0) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) acc[bb][i] = __uint_as_float(rr[b4][i]);
+              for (int i = 0; i < 16; ++i) acc[bb][i] = __uint_as_float(rr[i]);
             } else {
 #pragma unroll
               for (int i = 0; i < 16; i += 2)
-                add2_rn(acc[bb][i], acc[bb][i + 1], __uint_as_float(rr[b4][i]),
-                        __uint_as_float(rr[b4][i + 1]));
+                add2_rn(acc[bb][i], acc[bb][i + 1], __uint_as_float(rr[i]),
+                        __uint_as_float(rr[i + 1]));
             }
           }
         }

@@ -263,25 +263,26 @@ head_rows_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         if (warp_rows) {
           const uint32_t sbase = tmem_base + tlane + cur * static_cast<uint32_t>(kRowsN) +
                                  static_cast<uint32_t>(g * 128);
-          // two groups of four 16-column loads, one wait each (a wait per
+          // two groups of two 32-column loads, one wait each (a wait per
           // load left the drain latency-bound)
 #pragma unroll
           for (int h4 = 0; h4 < 2; ++h4) {
-            uint32_t rr[4][16];
+            uint32_t rw[2][32];
 #pragma unroll
-            for (int b4 = 0; b4 < 4; ++b4) tmem_ld16(sbase + (h4 * 4 + b4) * 16, rr[b4]);
+            for (int b2 = 0; b2 < 2; ++b2) tmem_ld32(sbase + (h4 * 2 + b2) * 32, rw[b2]);
             tmem_wait_ld();
 #pragma unroll
             for (int b4 = 0; b4 < 4; ++b4) {
               const int bb = h4 * 4 + b4;
+              const uint32_t* rr = &rw[b4 >> 1][(b4 & 1) * 16];   // this block's 16 columns
               if (c == 0) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[bb][i] = __uint_as_float(rr[b4][i]);
+                for (int i = 0; i < 16; ++i) acc[bb][i] = __uint_as_float(rr[i]);
               } else {
 #pragma unroll
                 for (int i = 0; i < 16; i += 2)
-                  add2_rn(acc[bb][i], acc[bb][i + 1], __uint_as_float(rr[b4][i]),
-                          __uint_as_float(rr[b4][i + 1]));
+                  add2_rn(acc[bb][i], acc[bb][i + 1], __uint_as_float(rr[i]),
+                          __uint_as_float(rr[i + 1]));
               }
             }
           }
