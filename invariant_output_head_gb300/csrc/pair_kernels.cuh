@@ -19,10 +19,11 @@
 // and 128 consecutive vocabulary entries (one 128-row tile of W), and folds
 // its tile record (max, lowest index, runner-up) in registers, in ascending
 // vocabulary order, with no exchange between threads; the per-unit work after
-// the last chunk is short enough to run while the MMA fills both accumulator
-// slots with the next unit's first chunks. fp32 logits leave through a small
-// per-warp transpose in shared memory, so that a warp's stores cover whole
-// 64-byte runs of a hidden row's logits. The tensor core's result for an
+// the last chunk overlaps the MMA filling both accumulator slots with the
+// next unit's first chunks. fp32 logits go through per-warp staging buffers
+// in shared memory and leave by TMA tensor stores, which run while the warp
+// drains the next unit (plain stores of 64-byte row runs where the logits
+// are not 16-byte aligned device memory). The tensor core's result for an
 // element depends neither on the operand roles nor on the pair mode (checked
 // bit for bit on GB300 with standalone probes), so the logits are
 // head_gemm_kernel's bit for bit, and the greedy record is exact.
@@ -30,8 +31,9 @@
 // The pair protocol is the log-prob kernel's (rows_kernels.cuh): the leader
 // issues every MMA; both producers' loads complete on the leader's stage
 // barrier; MMA commits arrive on both CTAs' barriers (multicast); a chunk's
-// accumulator slot goes back to the MMA when the eight epilogue warps of both
-// CTAs have arrived on the leader's slot-empty barrier. Every wait is bounded.
+// accumulator slot goes back to the MMA when the epilogue warps of both CTAs
+// (eight each) have arrived on the leader's slot-empty barrier. Every wait is
+// bounded.
 #pragma once
 #include "head_kernels.cuh"
 #include "rows_kernels.cuh"
@@ -40,7 +42,7 @@ namespace detlm {
 
 constexpr int kPairThreads = 384;
 constexpr int kPairMaxStages = 7;
-constexpr int kPairN = 256;         // hidden rows per unit (MMA N)
+constexpr int kPairN = 256;         // hidden rows per unit (the pair's MMA M); also its N
 constexpr int kPairWarps = 8;       // epilogue warps 4 .. 11, 128 columns each
 
 // Logits staging: per epilogue warp two buffers of 32 hidden rows x 16
