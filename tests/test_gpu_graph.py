@@ -99,3 +99,44 @@ def test_int8_calls_replay_bitwise(torch_cuda):
     z = host(outs[-1]).astype(np.int64)
     assert (z[:4] == np.asarray(case["h"][:4], np.int64) @ np.asarray(case["W"], np.int64).T).all()
     head.close()
+
+
+def test_next_row_calls_replay_bitwise(torch_cuda):
+    """The gated, sampling and speculative-verify calls captured and replayed
+    (the verify call's per-request workspace words reset themselves, so
+    every replay accepts the same lengths)."""
+    from invariant_output_head_gb300 import Head, binding
+    torch = torch_cuda
+    V, d, B = 1000, 256, 160
+    case = synth.small_float(902, V, d, B)
+    head = Head(dev(case["W"], "bf16"), "bf16")
+    head.reserve(B)
+    h = dev(case["h"], "bf16")
+    f32 = lambda *shape: torch.empty(*shape, dtype=torch.float32, device="cuda")  # noqa: E731
+    i32 = lambda *shape: torch.empty(*shape, dtype=torch.int32, device="cuda")    # noqa: E731
+    g_out = (i32(B), f32(B), f32(B, V), i32(B), f32(B))
+    s_out = (i32(B), f32(B), f32(B, V))
+    v_out = (i32(B), f32(B), f32(B, V), i32(B // 16))
+    seeds = torch.arange(1, B + 1, dtype=torch.int64, device="cuda") * 0x3779B97F4A7C15 % (2**62)
+    pos = torch.arange(B, dtype=torch.int64, device="cuda") * 7 + 3
+    tok_ref, _, _ = head.greedy(h)
+    drafts = tok_ref.clone()
+    drafts[5] += 1                 # request 0 accepts 5 positions, the others all 16
+    torch.cuda.synchronize()
+
+    def run(sp):
+        binding.detlm_head_greedy_gated(head.handle, h.data_ptr(), B, 0.001, g_out[0].data_ptr(),
+                                        g_out[1].data_ptr(), g_out[2].data_ptr(),
+                                        g_out[3].data_ptr(), g_out[4].data_ptr(), sp)
+        binding.detlm_head_sample(head.handle, h.data_ptr(), B, 1.0, seeds.data_ptr(),
+                                  pos.data_ptr(), s_out[0].data_ptr(), s_out[1].data_ptr(),
+                                  s_out[2].data_ptr(), sp)
+        binding.detlm_head_verify(head.handle, h.data_ptr(), B // 16, 16, drafts.data_ptr(),
+                                  v_out[0].data_ptr(), v_out[1].data_ptr(), v_out[2].data_ptr(),
+                                  v_out[3].data_ptr(), sp)
+
+    _capture_and_compare(torch, run, list(g_out) + list(s_out) + list(v_out))
+    assert head.check() == 0
+    acc = host(v_out[3])
+    assert acc[0] == 5 and (acc[1:] == 16).all()
+    head.close()
