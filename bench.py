@@ -725,8 +725,9 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
     asynchronous host-buffer entry points (one pinned result buffer set per
     call; the step ends with detlm_head_check on each head it used); the
     other calls, which have no host-buffer form, through their device entry
-    points between explicit copies on the same stream, the step ending with a
-    stream synchronization."""
+    points with their inputs copied in on the same stream and their outputs
+    written by the kernels straight into pinned host buffers (one set per
+    call), the step ending with a stream synchronization."""
     import torch
     from invariant_output_head_gb300 import binding as bd
     fmt, V = c["dtype"], c["V"]
@@ -736,10 +737,6 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
     esz = h_host.element_size()
     d = c["d"]
     maxB = max(B for _, B in calls)
-    tok = torch.empty(maxB, dtype=torch.int32).pin_memory()
-    gap = torch.empty(maxB, dtype=torch.int32).pin_memory()
-    lg = torch.empty((maxB, V), dtype=torch.int32).pin_memory() if greedy else None
-    lp = torch.empty(maxB, dtype=torch.float32).pin_memory()
     # the asynchronous calls: a result buffer set of their own per call
     res_bufs = []
     if mode in ("greedy", "logprob"):
@@ -751,27 +748,30 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
             else:
                 res_bufs.append((torch.empty(B, dtype=torch.float32).pin_memory(),))
     tg = torch.from_numpy(c["targets"]).pin_memory() if not greedy else None
-    extra = torch.empty(2 * maxB, dtype=torch.int32).pin_memory()   # base+margin / accepted
     sp = stream.cuda_stream
     steps = max(3, min(args.steps, int(args.e2e_seconds / 0.002)))
     if mode == "int8f":
         x_host = torch.from_numpy(np.ascontiguousarray(c["x"].view(np.int16))).pin_memory()
         x_dev = torch.empty((maxB, d), dtype=torch.int16, device=dev)
-        o8 = [torch.empty(maxB, dtype=torch.int32, device=dev),
-              torch.empty(maxB, dtype=torch.int32, device=dev),
-              torch.empty((maxB, V), dtype=torch.int32, device=dev)]
+        o8 = [(torch.empty(B, dtype=torch.int32).pin_memory(),
+               torch.empty(B, dtype=torch.int32).pin_memory(),
+               torch.empty((B, V), dtype=torch.int32).pin_memory()) for _, B in calls]
     if mode in ("gated", "verify", "sample"):
         tdt = {"bf16": torch.bfloat16, "fp16": torch.float16}[fmt]
         h_dev = torch.empty((maxB, d), dtype=tdt, device=dev)
-        o_dev = [torch.empty(maxB, dtype=torch.int32, device=dev),
-                 torch.empty(maxB, dtype=torch.float32, device=dev),
-                 torch.empty((maxB, V), dtype=torch.float32, device=dev),
-                 torch.empty(2 * maxB, dtype=torch.int32, device=dev)]
+        # per call: token, gap, logits, and the gate's base token + margin or
+        # the accepted lengths, all pinned host memory the kernels write
+        o_pin = [(torch.empty(B, dtype=torch.int32).pin_memory(),
+                  torch.empty(B, dtype=torch.float32).pin_memory(),
+                  torch.empty((B, V), dtype=torch.float32).pin_memory(),
+                  torch.empty(2 * B, dtype=torch.int32).pin_memory()) for _, B in calls]
         dr_host = (torch.from_numpy(c["drafts"]).pin_memory() if mode == "verify" else None)
         dr_dev = torch.empty(maxB, dtype=torch.int32, device=dev)
         if mode == "sample":
-            sd_host = torch.from_numpy(np.stack([c["seeds"], c["positions"]])).pin_memory()
-            sd_dev = torch.empty((2, sd_host.shape[1]), dtype=torch.int64, device=dev)
+            seed_host = torch.from_numpy(np.ascontiguousarray(c["seeds"])).pin_memory()
+            pos_host = torch.from_numpy(np.ascontiguousarray(c["positions"])).pin_memory()
+            seed_dev = torch.empty_like(seed_host, device=dev)
+            pos_dev = torch.empty_like(pos_host, device=dev)
 
     def one_step(i):
         used = {}
@@ -787,42 +787,32 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
                 bd.detlm_head_logprob_host_async(hd.handle, hp, tg.data_ptr() + r0 * 4, B,
                                                  res_bufs[j][0].data_ptr(), sp)
             elif mode == "int8f":
+                ot, og, ol = o8[j]
                 with torch.cuda.stream(stream):
                     x_dev[:B].copy_(x_host[r0:r0 + B], non_blocking=True)
                     bd.detlm_head_greedy_from_float(hd.handle, x_dev.data_ptr(), bd.DETLM_BF16, B,
-                                                    o8[0].data_ptr(), o8[1].data_ptr(),
-                                                    o8[2].data_ptr(), None, None, sp)
-                    tok[:B].copy_(o8[0][:B], non_blocking=True)
-                    gap[:B].copy_(o8[1][:B], non_blocking=True)
-                    lg[:B].copy_(o8[2][:B], non_blocking=True)
+                                                    ot.data_ptr(), og.data_ptr(), ol.data_ptr(),
+                                                    None, None, sp)
             else:
+                ot, og, ol, ox = o_pin[j]
                 with torch.cuda.stream(stream):
                     h_dev[:B].view(torch.int16).copy_(h_host[r0:r0 + B], non_blocking=True)
                     if mode == "gated":
                         bd.detlm_head_greedy_gated(
-                            hd.handle, h_dev.data_ptr(), B, GATE_TAU, o_dev[0].data_ptr(),
-                            o_dev[1].data_ptr(), o_dev[2].data_ptr(), o_dev[3].data_ptr(),
-                            o_dev[3].data_ptr() + 4 * B, sp)
-                        n_extra = 2 * B
+                            hd.handle, h_dev.data_ptr(), B, GATE_TAU, ot.data_ptr(),
+                            og.data_ptr(), ol.data_ptr(), ox.data_ptr(), ox.data_ptr() + 4 * B, sp)
                     elif mode == "sample":
-                        sd_dev[:, r0:r0 + B].copy_(sd_host[:, r0:r0 + B], non_blocking=True)
+                        seed_dev[r0:r0 + B].copy_(seed_host[r0:r0 + B], non_blocking=True)
+                        pos_dev[r0:r0 + B].copy_(pos_host[r0:r0 + B], non_blocking=True)
                         bd.detlm_head_sample(
                             hd.handle, h_dev.data_ptr(), B, SAMPLE_T,
-                            sd_dev[0, r0:r0 + B].data_ptr(), sd_dev[1, r0:r0 + B].data_ptr(),
-                            o_dev[0].data_ptr(), o_dev[1].data_ptr(), o_dev[2].data_ptr(), sp)
-                        n_extra = 0
+                            seed_dev[r0:r0 + B].data_ptr(), pos_dev[r0:r0 + B].data_ptr(),
+                            ot.data_ptr(), og.data_ptr(), ol.data_ptr(), sp)
                     else:
                         dr_dev[:B].copy_(dr_host.view(-1)[:B], non_blocking=True)
                         bd.detlm_head_verify(
                             hd.handle, h_dev.data_ptr(), B // 16, 16, dr_dev.data_ptr(),
-                            o_dev[0].data_ptr(), o_dev[1].data_ptr(), o_dev[2].data_ptr(),
-                            o_dev[3].data_ptr(), sp)
-                        n_extra = B // 16
-                    tok[:B].copy_(o_dev[0][:B], non_blocking=True)
-                    gap[:B].view(torch.float32).copy_(o_dev[1][:B], non_blocking=True)
-                    lg[:B].view(torch.float32).copy_(o_dev[2][:B], non_blocking=True)
-                    if n_extra:
-                        extra[:n_extra].copy_(o_dev[3][:n_extra], non_blocking=True)
+                            ot.data_ptr(), og.data_ptr(), ol.data_ptr(), ox.data_ptr(), sp)
         # the step's results are in host memory when the step ends
         if mode in ("greedy", "logprob"):
             for hd in used.values():
@@ -846,10 +836,14 @@ def run_e2e(args, c, heads, calls, mode, rows_per_step, dev, stream):
                for _, B in calls)
     api = {"greedy": "detlm_head_greedy_host_async (+ detlm_head_check per step)",
            "logprob": "detlm_head_logprob_host_async (+ detlm_head_check per step)",
-           "gated": "detlm_head_greedy_gated + pinned copies on the call's stream",
-           "verify": "detlm_head_verify + pinned copies on the call's stream",
-           "sample": "detlm_head_sample + pinned copies on the call's stream",
-           "int8f": "detlm_head_greedy_from_float + pinned copies on the call's stream"}[mode]
+           "gated": "detlm_head_greedy_gated, inputs copied in on the call's stream, "
+                    "outputs written by the kernels into pinned host buffers",
+           "verify": "detlm_head_verify, inputs copied in on the call's stream, "
+                     "outputs written by the kernels into pinned host buffers",
+           "sample": "detlm_head_sample, inputs copied in on the call's stream, "
+                     "outputs written by the kernels into pinned host buffers",
+           "int8f": "detlm_head_greedy_from_float, rows copied in on the call's stream, "
+                    "outputs written by the kernels into pinned host buffers"}[mode]
     return {"value": round(rows_per_step * steps / dt, 2), "unit": "rows/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps, "api": api}
 

@@ -19,6 +19,11 @@
  * Conventions for every entry point:
  *  - Pointers named *_dev are device pointers (or managed memory); pointers
  *    named *_host are host pointers. The library never frees caller memory.
+ *    On unified-addressing systems an OUTPUT *_dev pointer may also be
+ *    page-locked host memory the device can address (cudaHostAlloc,
+ *    cudaHostRegister): the kernels then write the results straight into
+ *    it, and they are in host memory once the stream reaches that point.
+ *    Inputs (W, h, targets, drafts, seeds) must be device memory.
  *  - Layouts are row-major with d (the reduction axis) contiguous: W is
  *    [V, d] as a linear layer stores its weight, h is [B, d], logits [B, V].
  *  - Element types: DETLM_BF16 and DETLM_FP16 heads take 16-bit inputs and

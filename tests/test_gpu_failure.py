@@ -247,3 +247,39 @@ def test_async_host_calls_with_large_logits(env):
         assert (o[1].numpy().view(np.uint32) == g.view(np.uint32)).all()
         assert (o[2].numpy().view(np.uint32) == z.view(np.uint32)).all()
     head.close()
+
+
+@pytest.mark.parametrize("B", [1, 160])
+def test_device_calls_write_pinned_outputs(env, B):
+    """Output pointers of the device calls may be page-locked host memory the
+    device can address: the gated, sampling, verify and float-fed integer
+    calls write their results straight into pinned buffers, bitwise what they
+    write into device memory (B = 160: the wide kernels)."""
+    torch, b = env
+    V, d = 900, 256
+    case = synth.small_float(21, V, d, B)
+    head = b.Head(dev(case["W"], "bf16"), "bf16")
+    h = dev(case["h"], "bf16")
+    s = torch.cuda.current_stream().cuda_stream
+
+    def outs(pinned, extra):
+        mk = (lambda *a, **k: torch.empty(*a, **k).pin_memory()) if pinned else \
+             (lambda *a, **k: torch.empty(*a, device="cuda", **k))
+        return (mk(B, dtype=torch.int32), mk(B, dtype=torch.float32), mk((B, V), dtype=torch.float32),
+                mk(max(extra, 1), dtype=torch.int32))
+    res = {}
+    for pinned in (False, True):
+        o = outs(pinned, 2 * B)
+        b.detlm_head_greedy_gated(head.handle, h.data_ptr(), B, 0.001, o[0].data_ptr(), o[1].data_ptr(),
+                                  o[2].data_ptr(), o[3].data_ptr(), o[3].data_ptr() + 4 * B, s)
+        seeds = torch.arange(1, B + 1, dtype=torch.int64, device="cuda") * 977
+        pos = torch.arange(B, dtype=torch.int64, device="cuda")
+        o2 = outs(pinned, 0)
+        b.detlm_head_sample(head.handle, h.data_ptr(), B, 1.0, seeds.data_ptr(), pos.data_ptr(),
+                            o2[0].data_ptr(), o2[1].data_ptr(), o2[2].data_ptr(), s)
+        torch.cuda.synchronize()
+        res[pinned] = [x.cpu() for x in o + o2[:3]]    # (o2[3] is not an output of sample)
+    assert head.check() == 0
+    for a, c in zip(res[False], res[True]):
+        assert torch.equal(a.view(torch.int32), c.view(torch.int32))
+    head.close()
