@@ -37,11 +37,6 @@ struct detlm_head {
   const void* W = nullptr;
   CUtensorMap tmW;
   int n_vt = 0, nk = 0, num_sms = 0;
-  // the one-CTA kernel's balanced schedule (vocabulary tiles between one and
-  // two waves): bal_R rows per CTA, its second part's boxes (bal_R - 128 rows)
-  // through tmW2; n_rec: records per hidden row the workspace holds
-  CUtensorMap tmW2;
-  int bal_R = 0, n_rec = 0;
   int rows_pairs = 0;        // CTA pairs of the rows kernel that fit at once (0: not asked yet)
   int wide_pairs = 0;        // the same for the wide greedy kernel
   int* d_err = nullptr;
@@ -181,7 +176,7 @@ int status_from_cuda(cudaError_t e) {
 // aligned parts, laid out for the allocated row count
 size_t ws_part(int64_t n) { return (static_cast<size_t>(n) * 4 + 255) & ~static_cast<size_t>(255); }
 size_t ws_bytes_for(const detlm_head* h, int64_t B) {
-  return 4 * ws_part(static_cast<int64_t>(h->n_rec) * B) + ws_part(B);
+  return 4 * ws_part(static_cast<int64_t>(h->n_vt) * B) + ws_part(B);
 }
 
 int ensure_ws(detlm_head* h, int64_t B, cudaStream_t stream) {
@@ -204,7 +199,7 @@ int ensure_ws(detlm_head* h, int64_t B, cudaStream_t stream) {
 struct WsView { float* m; int32_t* i; float* s; int32_t* b; float* zt; };
 WsView ws_view(const detlm_head* h) {
   uint8_t* b = static_cast<uint8_t*>(h->ws);
-  const size_t part = ws_part(static_cast<int64_t>(h->n_rec) * h->ws_B);
+  const size_t part = ws_part(static_cast<int64_t>(h->n_vt) * h->ws_B);
   WsView w;
   w.m = reinterpret_cast<float*>(b);
   w.i = reinterpret_cast<int32_t*>(b + part);
@@ -268,8 +263,8 @@ cudaError_t prepare_kernel(int want_regs) {
 // Launch kernel 1 for N = 16 * nblk as a programmatic dependent of the
 // previous kernel on the stream (its prologue overlaps that kernel's tail).
 template <int MODE, int NBLK>
-cudaError_t launch_gemm_n(const CUtensorMap& tmW, const CUtensorMap& tmH, const CUtensorMap& tmW2,
-                          const HeadParams& p, int grid, size_t smem, cudaStream_t stream) {
+cudaError_t launch_gemm_n(const CUtensorMap& tmW, const CUtensorMap& tmH, const HeadParams& p,
+                          int grid, size_t smem, cudaStream_t stream) {
   auto kern = head_gemm_kernel<MODE, NBLK>;
   // the wide kernel's register split assumes exactly its launch budget
   cudaError_t e = prepare_kernel<head_gemm_kernel<MODE, NBLK>>(
@@ -286,22 +281,22 @@ cudaError_t launch_gemm_n(const CUtensorMap& tmW, const CUtensorMap& tmH, const 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmW, tmH, tmW2, p);
+  return cudaLaunchKernelEx(&cfg, kern, tmW, tmH, p);
 }
 
 template <int MODE>
-cudaError_t launch_gemm(const CUtensorMap& tmW, const CUtensorMap& tmH, const CUtensorMap& tmW2,
-                        const HeadParams& p, int grid, size_t smem, cudaStream_t stream) {
+cudaError_t launch_gemm(const CUtensorMap& tmW, const CUtensorMap& tmH, const HeadParams& p,
+                        int grid, size_t smem, cudaStream_t stream) {
   switch (p.N / 16) {
-    case 1: return launch_gemm_n<MODE, 1>(tmW, tmH, tmW2, p, grid, smem, stream);
-    case 2: return launch_gemm_n<MODE, 2>(tmW, tmH, tmW2, p, grid, smem, stream);
-    case 3: return launch_gemm_n<MODE, 3>(tmW, tmH, tmW2, p, grid, smem, stream);
-    case 4: return launch_gemm_n<MODE, 4>(tmW, tmH, tmW2, p, grid, smem, stream);
-    case 5: return launch_gemm_n<MODE, 5>(tmW, tmH, tmW2, p, grid, smem, stream);
-    case 6: return launch_gemm_n<MODE, 6>(tmW, tmH, tmW2, p, grid, smem, stream);
-    case 7: return launch_gemm_n<MODE, 7>(tmW, tmH, tmW2, p, grid, smem, stream);
-    case 8: return launch_gemm_n<MODE, 8>(tmW, tmH, tmW2, p, grid, smem, stream);
-    case 16: return launch_gemm_n<MODE, 16>(tmW, tmH, tmW2, p, grid, smem, stream);
+    case 1: return launch_gemm_n<MODE, 1>(tmW, tmH, p, grid, smem, stream);
+    case 2: return launch_gemm_n<MODE, 2>(tmW, tmH, p, grid, smem, stream);
+    case 3: return launch_gemm_n<MODE, 3>(tmW, tmH, p, grid, smem, stream);
+    case 4: return launch_gemm_n<MODE, 4>(tmW, tmH, p, grid, smem, stream);
+    case 5: return launch_gemm_n<MODE, 5>(tmW, tmH, p, grid, smem, stream);
+    case 6: return launch_gemm_n<MODE, 6>(tmW, tmH, p, grid, smem, stream);
+    case 7: return launch_gemm_n<MODE, 7>(tmW, tmH, p, grid, smem, stream);
+    case 8: return launch_gemm_n<MODE, 8>(tmW, tmH, p, grid, smem, stream);
+    case 16: return launch_gemm_n<MODE, 16>(tmW, tmH, p, grid, smem, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -530,11 +525,6 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
   } else {
     p.n_vt = h->n_vt;
     p.n_nt = static_cast<int32_t>((B + N - 1) / N);
-    if (h->bal_R != 0 && p.n_nt == 1) {
-      // balanced schedule: two units (records) per SM, encoded as n_nt = -R
-      p.n_vt = 2 * h->num_sms;
-      p.n_nt = -h->bal_R;
-    }
     p.n_slots = slots_for(N);
     p.stages = stages_for(N, kExtraSmem);
     p.n_issuers = issuers_for(N, p.stages, &p.n_slots);
@@ -566,8 +556,7 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
                      : wide ? pair_layout(p.stages).total + 1024
                             : smem_layout(N, p.stages, kExtraSmem).total + 1024;
   const int64_t units = wide ? static_cast<int64_t>((p.n_vt + 1) / 2) * p.n_nt
-                     : p.n_nt < 0 ? static_cast<int64_t>(p.n_vt)      // balanced: 2 per SM
-                                  : static_cast<int64_t>(p.n_vt) * p.n_nt;
+                             : static_cast<int64_t>(p.n_vt) * p.n_nt;
   const int grid = static_cast<int>(units < h->num_sms ? units : h->num_sms);
   CUtensorMap tmL = tmH;   // the pair kernel's logits map; not read unless valid
   if (wide) p.tma_logits = encode_logits(&tmL, logits, h->V, B, false) ? 1 : 0;
@@ -579,9 +568,9 @@ int launch_float(detlm_head* h, const void* h_dev, int64_t B, const int32_t* tar
     if (wide)
       e = launch_pair_kernel<MODE_GREEDY>(h, h->tmW, tmH, tmL, p, units, smem, stream);
     else
-      e = launch_gemm<MODE>(h->tmW, tmH, h->tmW2, p, grid, smem, stream);
+      e = launch_gemm<MODE>(h->tmW, tmH, p, grid, smem, stream);
   } else {
-    e = launch_gemm<MODE>(h->tmW, tmH, h->tmW2, p, grid, smem, stream);
+    e = launch_gemm<MODE>(h->tmW, tmH, p, grid, smem, stream);
   }
   if (h->t_stop) {
     cudaEventRecord(h->t_stop, stream);
@@ -1077,22 +1066,6 @@ int detlm_head_create(detlm_head_t** out, const void* W_dev, int64_t V, int64_t 
   if (!encode_2d(&h->tmW, dtype, W_dev, d, V, kBM)) {
     delete h;
     return DETLM_EINVAL;
-  }
-  // float heads whose 128-row tiles number between one and two waves: the
-  // one-CTA kernel gives each SM a contiguous range of R = ceil(V / SMs)
-  // rows (a 128-row part and an (R - 128)-row part) instead of one or two
-  // whole tiles
-  h->tmW2 = h->tmW;
-  h->n_rec = h->n_vt;
-  if (dtype != DETLM_INT8 && h->n_vt > sms && h->n_vt <= 2 * sms) {
-    const int64_t R = (V + sms - 1) / sms;
-    if (R > kBM && R <= 2 * kBM &&
-        encode_2d(&h->tmW2, dtype, W_dev, d, V, static_cast<uint32_t>(R - kBM))) {
-      h->bal_R = static_cast<int>(R);
-      h->n_rec = h->n_vt > 2 * sms ? h->n_vt : 2 * sms;
-    } else {
-      h->tmW2 = h->tmW;
-    }
   }
   int host_atomics = 0;
   cudaDeviceGetAttribute(&host_atomics, cudaDevAttrHostNativeAtomicSupported, dev);
@@ -1728,7 +1701,7 @@ extern "C" int detlm_greedy_noalloc(const void* W_dev, int64_t V, int64_t d, int
   const size_t smem = smem_layout(N, p.stages).total + 1024;
   const int64_t units = static_cast<int64_t>(p.n_vt) * p.n_nt;
   const int grid = static_cast<int>(units < sms ? units : sms);
-  e = launch_gemm<MODE_GREEDY>(tmW, tmH, tmW, p, grid, smem, stream);   // tile schedule
+  e = launch_gemm<MODE_GREEDY>(tmW, tmH, p, grid, smem, stream);
   if (e != cudaSuccess) return status_from_cuda(e);
 
   MergeParams mp;

@@ -441,8 +441,7 @@ __device__ __forceinline__ bool epi_bar_or(bool pred) {
 template <int MODE, int NBLK>
 __global__ void __launch_bounds__(threads_for(16 * NBLK), 1)
 head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
-                 const __grid_constant__ CUtensorMap tmH,
-                 const __grid_constant__ CUtensorMap tmW2, const HeadParams p) {
+                 const __grid_constant__ CUtensorMap tmH, const HeadParams p) {
   static_assert(MODE == MODE_GREEDY || MODE == MODE_GATED || MODE == MODE_SAMPLE,
                 "log-prob runs on head_rows_kernel, the integer wide path on head_pair_kernel");
   constexpr int N = 16 * NBLK;
@@ -483,28 +482,10 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   auto sB = [&](int s) { return sA(s) + L.a_bytes; };
 
   const int kElems = kRowBytes / 2;     // 16-bit elements per 128-byte row
-  // Units. Normally unit u is vocabulary tile u / n_nt (128 rows) x hidden
-  // tile u % n_nt. Balanced schedule (p.n_nt = -R; one hidden tile; the
-  // vocabulary tiles number between one and two waves): CTA b owns the
-  // contiguous rows [R b, R b + R) as two units, rows R b .. R b + 127 (unit
-  // b, W boxes of tmW) and R b + 128 .. R b + R - 1 (unit b + G, boxes of
-  // R - 128 rows from tmW2), so that every SM streams the same bytes instead
-  // of some SMs two tiles and the rest one. Records are per unit; their merge
-  // is exact, so the grouping changes no result.
-  const bool bal = p.n_nt < 0;
-  const int R = bal ? -p.n_nt : 0;
-  const int n_nt = bal ? 1 : p.n_nt;
-  const int G = static_cast<int>(gridDim.x);
-  const int n_units = bal ? 2 * G : p.n_vt * n_nt;
-  auto unit_r0 = [&](int u) { return bal ? (u < G ? R * u : R * (u - G) + kBM) : (u / n_nt) * kBM; };
-  auto unit_rows = [&](int u) { return bal && u >= G ? R - kBM : kBM; };   // W box rows
-  auto unit_rec = [&](int u) { return bal ? u : u / n_nt; };                 // record index
-  auto unit_nt = [&](int u) { return bal ? 0 : u - (u / n_nt) * n_nt; };
-  auto unit_map = [&](int u) { return bal && u >= G ? &tmW2 : &tmW; };
   // stages whose W boxes the producer requests before the previous kernels
   // on the stream have finished (at most the ring, at most this CTA's work)
   auto pre_stages = [&]() {
-    const int units = n_units, per_unit = (p.nk + KPS - 1) / KPS;
+    const int units = p.n_vt * p.n_nt, per_unit = (p.nk + KPS - 1) / KPS;
     const int n_my = (units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                      static_cast<int>(gridDim.x);
     return min(S, n_my > 0 ? n_my * per_unit : 0);
@@ -520,17 +501,16 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
     for (int s = 0; s < S; ++s) mbar_init(full_bar(s), 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmW);
-    if (bal) tma_prefetch_desc(&tmW2);
     const uint64_t pol_w = policy_evict_first();
     const int pre = pre_stages(), spu = (p.nk + KPS - 1) / KPS;
     for (int j = 0; j < pre; ++j) {
       const int u = blockIdx.x + (j / spu) * gridDim.x;
-      const int st = j - (j / spu) * spu;
+      const int vt = u / p.n_nt, st = j - (j / spu) * spu;
       const int kb0 = st * KPS;
       const int nb = min(KPS, p.nk - kb0);
-      mbar_expect_tx(full_bar(j), static_cast<uint32_t>(nb) * (unit_rows(u) + N) * kRowBytes);
+      mbar_expect_tx(full_bar(j), static_cast<uint32_t>(nb) * (kBM + N) * kRowBytes);
       for (int b = 0; b < nb; ++b)
-        tma_load_2d(sA(j) + b * kBM * kRowBytes, unit_map(u), (kb0 + b) * kElems, unit_r0(u),
+        tma_load_2d(sA(j) + b * kBM * kRowBytes, &tmW, (kb0 + b) * kElems, vt * kBM,
                     full_bar(j), pol_w);
     }
     for (int s = 0; s < S; ++s) mbar_init(empty_bar(s), 1);
@@ -554,6 +534,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
   // Launched as a dependent grid: the set-up above overlapped the previous
   // kernels on the stream.
   const uint32_t tmem_base = *tmem_holder;
+  const int n_units = p.n_vt * p.n_nt;
   const int spu = (p.nk + KPS - 1) / KPS;   // stages per unit
 
   if (warp == 0) {
@@ -569,9 +550,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       bool ok = true;
       int j = 0;                     // stages issued by this CTA
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const int nt = unit_nt(u), r0 = unit_r0(u);
-        const uint32_t wrows = static_cast<uint32_t>(unit_rows(u));
-        const CUtensorMap* tw = unit_map(u);
+        const int vt = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
         for (int st = 0; st < spu; ++st, ++j) {
           const int kb0 = st * KPS;
           const int nb = min(KPS, p.nk - kb0);
@@ -586,9 +565,9 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
               break;
             }
             mbar_arrive_expect_tx(full_bar(stage), static_cast<uint32_t>(nb) *
-                                                       (wrows + N) * kRowBytes);
+                                                       (kBM + N) * kRowBytes);
             for (int b = 0; b < nb; ++b) {
-              tma_load_2d(sA(stage) + b * kBM * kRowBytes, tw, (kb0 + b) * kElems, r0,
+              tma_load_2d(sA(stage) + b * kBM * kRowBytes, &tmW, (kb0 + b) * kElems, vt * kBM,
                           full_bar(stage), pol_w);
               tma_load_2d(sB(stage) + b * N * kRowBytes, &tmH, (kb0 + b) * kElems, nt * N,
                           full_bar(stage), pol_h);
@@ -709,8 +688,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
     uint32_t slot = 0, sph = 0;
     bool failed = false;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const int nt = unit_nt(u), r0 = unit_r0(u), rec = unit_rec(u);
-      const int rows_u = bal && u >= G ? R - kBM : kBM;   // this unit's vocabulary rows
+      const int vt = u / p.n_nt, nt = u - (u / p.n_nt) * p.n_nt;
       float acc[WBLK][16];
       for (int c = 0; c < p.n_chunks; ++c) {
         const uint32_t cur = slot, cph = sph;
@@ -754,10 +732,10 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
         if (et == 0) { *abort_flag = 1; atomicOr(p.err, ERR_TIMEOUT); }
         break;
       }
-      const int v = r0 + row;
-      const bool vok = row < rows_u && v < p.V;
+      const int v = vt * kBM + row;
+      const bool vok = v < p.V;
       const int n0 = nt * N;
-      const int vg0 = p.v_off + r0 + q * 32;   // vocabulary index of this warp's row 0
+      const int vg0 = p.v_off + vt * kBM + q * 32;   // vocabulary index of this warp's row 0
       if constexpr (MODE == MODE_SAMPLE) {
         // the unit's column keys, once per unit (ordered before the reads by
         // this barrier, after the previous unit's reads by the one above)
@@ -827,7 +805,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
       for (int c = et; c < N; c += ET) {
         const int n = n0 + c;
         if (n >= p.B) continue;
-        const size_t o = static_cast<size_t>(n) * p.n_vt + rec;   // records [B][n_vt]
+        const size_t o = static_cast<size_t>(n) * p.n_vt + vt;   // records [B][n_vt]
         {
           Top2 t[4];
 #pragma unroll
