@@ -902,7 +902,7 @@ def cpu_baseline(name, c, budget_s, gpu_rows=None):
     GPU's decisions for those rows (gpu_rows[r] = token or logp of row r), the
     sampled rows are also compared and every disagreement is listed: a token
     that differs inside the tolerance of the logits is a near-tie exception,
-    one outside it a mismatch (the benchmark spec: listed, not hidden)."""
+    one outside it a mismatch; both are listed, never dropped."""
     v, n, dt = oracle_rows_per_s(name, c, budget_s)
     res = {"value": round(v, 4), "unit": "rows/s", "cores": cpu_cores(), "kind": "oracle",
            "sample": f"{n} hidden rows of the {name} workload, one oracle call per row "
